@@ -1,0 +1,410 @@
+"""CPU oracle for one dropless top-k MoE FFN layer with SwiGLU experts.
+
+TEST INFRASTRUCTURE.  Only the test suite, the package's smoke check and the
+benchmark's CPU-baseline leg may import or run this module.  The CUDA library
+never calls it, and it shares no code, table or helper with the CUDA sources.
+
+What it computes, with the passages it follows:
+
+* Router and gating.  A trainable gate network scores every expert for each
+  token and the k experts with the highest probability are chosen; their
+  outputs are summed, weighted (DisagMoE, §2.1 "混合专家（MoE）结构"; the
+  MegaScale-MoE review lists the gate network as a component, §三 模型组件).
+  Probabilities are a softmax over all E router logits l = x Wg + b; the k
+  selected probabilities are renormalised to sum to one.  Ties go to the lower
+  expert id; the k slots are in descending logit order.
+* Dispatch.  Token copies are sorted by expert, then by source (MegaScale-MoE
+  digest §3.3 under Diagram C; the review's "extra scatter to keep memory
+  contiguous", §四 自适应EP通信策略详解).  On one GPU the source order is the
+  token order, so the permutation is a stable sort of assignments a = t*k + j
+  by expert id: counts, their exclusive scan (offsets) and the maps
+  perm_src[p] = a, perm_dst[a] = p.
+* Experts.  Each expert is a SwiGLU FFN (review §三 核心公式: "SwiGLU structure
+  with MoE", compute 3k*bsh*h_ffn multiply-adds at n = 1), run for all
+  experts as one GroupedGEMM (digest glossary "GroupedGEMM"; review 训练流程,
+  专家计算（GroupedGEMM）):  A = X W1,  B = X W3,  H = silu(A) * B,  O = H W2.
+* Combine.  y[t] = sum_j g[t,j] * O[perm_dst[t*k+j]] (DisagMoE §2.1 weighted sum;
+  review 训练流程 Token聚合).
+* Backward.  The layer's backward written out as explicit operators (digest §3.3:
+  forward and backward of the MoE layer are explicit operators, not autograd);
+  FC2's gradients take fc2_in (= H) and the gradient of fc2_out (review
+  选择性激活重计算).  Router gradient flows through the renormalised gates.
+
+Precision.  Inputs are the exact values of the bf16 / fp32 bytes the layer
+receives.  Every product and sum is float64, with no intermediate rounding.
+The one integer decision that floating point takes, the choice of the top-k
+experts, is taken on float32 logits (x Wg accumulated in float32, + b in
+float32), the precision the CUDA router decides in; inputs are conditioned
+(condition_router_margins) so that no float32 rounding order can flip it.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "as_f64", "router_logits", "route", "dispatch", "permute_rows",
+    "unpermute_rows", "silu", "expert_ffn_fwd", "combine", "layer_fwd",
+    "expert_ffn_bwd", "router_bwd", "layer_bwd", "token_fwd_bwd",
+    "expert_wgrad_columns", "condition_router_margins", "router_margin",
+    "gemm_macs_fwd", "dispatch_bytes_per_token", "activation_bytes",
+]
+
+
+# ----------------------------------------------------------------- inputs ---
+
+def as_f64(t) -> np.ndarray:
+    """Exact float64 value of a bf16 / fp32 tensor (torch or numpy)."""
+    if hasattr(t, "detach"):
+        return t.detach().to("cpu").double().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def _as_f32(t) -> np.ndarray:
+    if hasattr(t, "detach"):
+        return t.detach().to("cpu").float().numpy()
+    return np.asarray(t, dtype=np.float32)
+
+
+# ----------------------------------------------------------------- router ---
+
+def router_logits(x, Wg, b=None):
+    """l[t,e] = sum_i x[t,i] Wg[i,e] + b[e]: float64 values and float32 values.
+
+    The float32 copy (float32 products and sums, then + b in float32) is the
+    one the top-k decision is taken on.  DisagMoE §2.1 (gate network scores).
+    """
+    x64, W64 = as_f64(x), as_f64(Wg)
+    l64 = x64 @ W64
+    l32 = _as_f32(x) @ _as_f32(Wg)
+    if b is not None:
+        l64 = l64 + as_f64(b)[None, :]
+        l32 = (l32 + _as_f32(b)[None, :]).astype(np.float32)
+    return l64, l32
+
+
+def route(x, Wg, b, k):
+    """Softmax top-k gating.
+
+    Returns topk_idx [T,k] int32 (descending logit, ties -> lower id),
+    gates [T,k] float64 = p[sel] / sum(p[sel]) with p = softmax over all E,
+    and the float64 logits.  DisagMoE §2.1: the gate picks the k experts with
+    the highest probability scores.
+    """
+    l64, l32 = router_logits(x, Wg, b)
+    T, E = l64.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    # stable sort of -l: equal logits keep ascending expert id
+    order = np.argsort(-l32, axis=1, kind="stable")
+    topk_idx = order[:, :k].astype(np.int32)
+    m = l64.max(axis=1, keepdims=True)
+    ex = np.exp(l64 - m)
+    p = ex / ex.sum(axis=1, keepdims=True)
+    psel = np.take_along_axis(p, topk_idx.astype(np.int64), axis=1)
+    gates = psel / psel.sum(axis=1, keepdims=True)
+    return topk_idx, gates, l64
+
+
+def router_margin(l64, k):
+    """Smallest gap between consecutive values among each row's k+1 largest
+    logits (k largest when k = E)."""
+    s = -np.sort(-l64, axis=1)
+    top = s[:, : min(k + 1, s.shape[1])]
+    if top.shape[1] < 2:
+        return np.full(l64.shape[0], np.inf)
+    return (top[:, :-1] - top[:, 1:]).min(axis=1)
+
+
+def condition_router_margins(x, Wg, b, k, fresh_rows, margin=1e-3, max_attempts=64):
+    """Replace rows of x whose router decision is numerically ambiguous.
+
+    A row is ambiguous when two of its k+1 largest float64 logits are closer
+    than `margin`.  fresh_rows(row_ids, attempt) must return replacement bf16
+    rows (torch, CPU).  Returns (new x as torch bf16, number of rows replaced).
+    Input conditioning only: no value computed here is an expected output.
+    """
+    import torch
+    xc = x.detach().to("cpu").clone()
+    W64 = as_f64(Wg)
+    b64 = np.zeros(W64.shape[1]) if b is None else as_f64(b)
+    l64 = as_f64(xc) @ W64 + b64[None, :]
+    bad = np.nonzero(router_margin(l64, k) < margin)[0]
+    replaced = set()
+    attempt = 0
+    while bad.size:
+        attempt += 1
+        if attempt > max_attempts:
+            raise RuntimeError("router margin conditioning did not converge")
+        new = fresh_rows(bad, attempt)
+        xc[torch.as_tensor(bad, dtype=torch.int64)] = new.to(xc.dtype)
+        replaced.update(bad.tolist())
+        lb = as_f64(xc[torch.as_tensor(bad, dtype=torch.int64)]) @ W64 + b64[None, :]
+        bad = bad[router_margin(lb, k) < margin]
+    return xc, len(replaced)
+
+
+# --------------------------------------------------------------- dispatch ---
+
+def dispatch(topk_idx, E):
+    """Counts, offsets and the stable expert-major permutation.
+
+    counts[e] = #{a : topk_idx[a] = e};  offsets = exclusive scan, offsets[E] =
+    T*k;  perm_src[p] = the assignment a placed at permuted row p, ordered by
+    expert then by a (so by token);  perm_dst = inverse of perm_src.
+    MegaScale-MoE digest §3.3 (tokens sorted by expert, then by source).
+    """
+    flat = np.asarray(topk_idx, dtype=np.int64).ravel()
+    counts = np.bincount(flat, minlength=E).astype(np.int32)
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    perm_src = np.argsort(flat, kind="stable").astype(np.int32)
+    perm_dst = np.empty_like(perm_src)
+    perm_dst[perm_src] = np.arange(flat.size, dtype=np.int32)
+    return counts, offsets, perm_src, perm_dst
+
+
+def permute_rows(x, perm_src, k):
+    """x_perm[p] = x[perm_src[p] // k]: one copy of a token per assignment."""
+    return np.asarray(x)[np.asarray(perm_src, dtype=np.int64) // k]
+
+
+def unpermute_rows(rows_perm, perm_dst):
+    """rows_assign[a] = rows_perm[perm_dst[a]] (assignment order a = t*k+j)."""
+    return np.asarray(rows_perm)[np.asarray(perm_dst, dtype=np.int64)]
+
+
+# ---------------------------------------------------------------- experts ---
+
+def silu(z):
+    """silu(z) = z / (1 + exp(-z))."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def _sigmoid(z):
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+class MacCounter:
+    """Counts multiply-adds of the expert matmuls as they are performed."""
+
+    def __init__(self):
+        self.macs = 0
+
+    def matmul(self, a, b):
+        self.macs += a.shape[0] * a.shape[1] * b.shape[1]
+        return a @ b
+
+
+def expert_ffn_fwd(x_perm, offsets, W1, W3, W2, counter=None):
+    """Per-expert SwiGLU FFN over the expert-contiguous rows (GroupedGEMM).
+
+    For each e, rows p in [offsets[e], offsets[e+1]):  A = X_e W1[e],
+    B = X_e W3[e], H = silu(A) * B, O = H W2[e].  Returns A, B, H, O (float64).
+    Review §三 核心公式 (SwiGLU MoE compute) and 训练流程 (GroupedGEMM).
+    """
+    c = counter if counter is not None else MacCounter()
+    X = as_f64(x_perm)
+    W1, W3, W2 = as_f64(W1), as_f64(W3), as_f64(W2)
+    R = X.shape[0]
+    f, h = W1.shape[2], W1.shape[1]
+    A = np.zeros((R, f)); B = np.zeros((R, f)); O = np.zeros((R, h))
+    for e in range(W1.shape[0]):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        Xe = X[lo:hi]
+        A[lo:hi] = c.matmul(Xe, W1[e])
+        B[lo:hi] = c.matmul(Xe, W3[e])
+        O[lo:hi] = c.matmul(silu(A[lo:hi]) * B[lo:hi], W2[e])
+    H = silu(A) * B
+    return A, B, H, O
+
+
+def combine(O, gates, perm_dst, T, k):
+    """y[t] = sum_{j<k} g[t,j] * O[perm_dst[t*k+j]], summed in slot order.
+    DisagMoE §2.1 (outputs reduced by a weighted sum)."""
+    O = np.asarray(O)
+    idx = np.asarray(perm_dst, dtype=np.int64).reshape(T, k)
+    g = np.asarray(gates, dtype=np.float64).reshape(T, k)
+    y = np.zeros((T, O.shape[1]))
+    for j in range(k):
+        y += g[:, j:j + 1] * O[idx[:, j]]
+    return y
+
+
+def layer_fwd(x, Wg, b, W1, W3, W2, k, counter=None):
+    """route -> dispatch -> permute -> expert FFN -> combine.
+
+    Returns y (float64 [T,h]) and a context dict with every intermediate.
+    """
+    T = x.shape[0]
+    E = Wg.shape[1]
+    topk_idx, gates, l64 = route(x, Wg, b, k)
+    counts, offsets, perm_src, perm_dst = dispatch(topk_idx, E)
+    x64 = as_f64(x)
+    x_perm = permute_rows(x64, perm_src, k)
+    A, B, H, O = expert_ffn_fwd(x_perm, offsets, W1, W3, W2, counter)
+    y = combine(O, gates, perm_dst, T, k)
+    ctx = dict(topk_idx=topk_idx, gates=gates, logits=l64, counts=counts,
+               offsets=offsets, perm_src=perm_src, perm_dst=perm_dst,
+               x_perm=x_perm, A=A, B=B, H=H, O=O, k=k)
+    return y, ctx
+
+
+# --------------------------------------------------------------- backward ---
+
+def expert_ffn_bwd(dO, x_perm, offsets, W1, W3, W2, A, B, H, counter=None):
+    """Backward of the per-expert SwiGLU FFN given dO = dL/dO (float64).
+
+    dH = dO W2[e]^T;  dA = dH * B * sigma(A) (1 + A (1 - sigma(A)));
+    dB = dH * silu(A);  dW2[e] = H_e^T dO_e;  dW1[e] = X_e^T dA_e;
+    dW3[e] = X_e^T dB_e;  dX_perm = dA W1[e]^T + dB W3[e]^T.
+    FC2's weight gradient uses fc2_in (H) and d(fc2_out) (review 选择性激活重计算).
+    """
+    c = counter if counter is not None else MacCounter()
+    W1, W3, W2 = as_f64(W1), as_f64(W3), as_f64(W2)
+    E, h, f = W1.shape
+    X = np.asarray(x_perm, dtype=np.float64)
+    dW1 = np.zeros((E, h, f)); dW3 = np.zeros((E, h, f)); dW2 = np.zeros((E, f, h))
+    dA = np.zeros_like(A); dB = np.zeros_like(B); dX = np.zeros_like(X)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        dH = c.matmul(dO[lo:hi], W2[e].T)
+        a = A[lo:hi]
+        s = _sigmoid(a)
+        dA[lo:hi] = dH * B[lo:hi] * s * (1.0 + a * (1.0 - s))
+        dB[lo:hi] = dH * silu(a)
+        dW2[e] = c.matmul(H[lo:hi].T, dO[lo:hi])
+        dW1[e] = c.matmul(X[lo:hi].T, dA[lo:hi])
+        dW3[e] = c.matmul(X[lo:hi].T, dB[lo:hi])
+        dX[lo:hi] = c.matmul(dA[lo:hi], W1[e].T) + c.matmul(dB[lo:hi], W3[e].T)
+    return dict(dA=dA, dB=dB, dX_perm=dX, dW1=dW1, dW3=dW3, dW2=dW2)
+
+
+def router_bwd(gates, dg):
+    """dL/dl for the selected logits: dl_j = g_j (dg_j - sum_i g_i dg_i).
+
+    The renormalised gates equal a softmax over the k selected logits (the
+    full-softmax denominator cancels), whose Jacobian is g_j (delta_ij - g_i).
+    Unselected logits get zero (selection is piecewise constant).
+    """
+    g = np.asarray(gates, dtype=np.float64)
+    s = (g * dg).sum(axis=1, keepdims=True)
+    return g * (dg - s)
+
+
+def layer_bwd(dy, x, Wg, W1, W3, W2, ctx, counter=None):
+    """Gradients of L = <dy, y> with respect to x, Wg, W1, W3, W2, plus dg.
+
+    dO[p] = g[a] dy[t];  dg[a] = <dy[t], O[p]>;  expert backward;
+    dx[t] = sum_j dX_perm[perm_dst[t*k+j]] + sum_j dl[t,j] Wg[:, e_j];
+    dWg = x^T dl  (dl is zero outside each token's k selected experts).
+    """
+    k = ctx["k"]
+    dy64 = as_f64(dy)
+    T, h = dy64.shape
+    Wg64 = as_f64(Wg)
+    E = Wg64.shape[1]
+    perm_src = np.asarray(ctx["perm_src"], dtype=np.int64)
+    perm_dst = np.asarray(ctx["perm_dst"], dtype=np.int64)
+    g_flat = np.asarray(ctx["gates"], dtype=np.float64).ravel()
+    tok = perm_src // k
+    dO = g_flat[perm_src][:, None] * dy64[tok]
+    dg_perm = np.einsum("ph,ph->p", dy64[tok], ctx["O"])
+    dg = np.empty(T * k)
+    dg[perm_src] = dg_perm
+    dg = dg.reshape(T, k)
+    ex = expert_ffn_bwd(dO, ctx["x_perm"], ctx["offsets"], W1, W3, W2,
+                        ctx["A"], ctx["B"], ctx["H"], counter)
+    dl_sel = router_bwd(ctx["gates"], dg)
+    idx = np.asarray(ctx["topk_idx"], dtype=np.int64)
+    dl = np.zeros((T, E))
+    np.put_along_axis(dl, idx, dl_sel, axis=1)
+    dx = unpermute_rows(ex["dX_perm"], perm_dst).reshape(T, k, h).sum(axis=1)
+    dx = dx + dl @ Wg64.T
+    dWg = as_f64(x).T @ dl
+    out = dict(dx=dx, dWg=dWg, dg=dg, dl=dl, dO=dO)
+    out.update(ex)
+    return out
+
+
+# ---------------------------------------------- per-token / sampled forms ---
+
+def token_fwd_bwd(x_t, dy_t, Wg, b, k, expert):
+    """The layer for one token, straight from the definition (no dispatch).
+
+    expert(e) -> (W1[e], W3[e], W2[e]) as float64 arrays.  Returns a dict with
+    topk_idx, gates, y, dg, dx for this token: y = sum_j g_j FFN_{e_j}(x_t),
+    dx = sum_j g_j J_{e_j}(x_t)^T dy + sum_j dl_j Wg[:, e_j].
+    """
+    x = as_f64(x_t).reshape(1, -1)
+    dy = as_f64(dy_t).reshape(-1)
+    idx, gates, _ = route(x_t.reshape(1, -1), Wg, b, k)
+    idx, gates = idx[0], gates[0]
+    Wg64 = as_f64(Wg)
+    y = np.zeros(x.shape[1])
+    dx = np.zeros(x.shape[1])
+    dg = np.zeros(k)
+    for j, e in enumerate(idx):
+        W1e, W3e, W2e = expert(int(e))
+        a = (x @ W1e)[0]
+        bb = (x @ W3e)[0]
+        hh = silu(a) * bb
+        o = hh @ W2e
+        y += gates[j] * o
+        dg[j] = dy @ o
+        dh = gates[j] * (W2e @ dy)
+        s = _sigmoid(a)
+        da = dh * bb * s * (1.0 + a * (1.0 - s))
+        db = dh * silu(a)
+        dx += W1e @ da + W3e @ db
+    dl = router_bwd(gates[None, :], dg[None, :])[0]
+    for j, e in enumerate(idx):
+        dx += dl[j] * Wg64[:, int(e)]
+    return dict(topk_idx=idx, gates=gates, y=y, dg=dg, dx=dx)
+
+
+def expert_wgrad_columns(X_e, dO_e, W1e, W3e, W2e, cols):
+    """Columns `cols` of dW1[e] and dW3[e] and rows `cols` of dW2[e].
+
+    X_e [n,h] are the expert's token rows in permuted order, dO_e [n,h] the
+    matching g * dy rows.  Column c of the FFN width needs only A[:,c], B[:,c]
+    and dH[:,c] = dO_e W2[e][c,:]^T.
+    """
+    X = np.asarray(X_e, dtype=np.float64)
+    dO = np.asarray(dO_e, dtype=np.float64)
+    cols = np.asarray(cols, dtype=np.int64)
+    a = X @ W1e[:, cols]
+    bb = X @ W3e[:, cols]
+    dh = dO @ W2e[cols, :].T
+    s = _sigmoid(a)
+    da = dh * bb * s * (1.0 + a * (1.0 - s))
+    db = dh * silu(a)
+    hh = silu(a) * bb
+    return dict(dW1=X.T @ da, dW3=X.T @ db, dW2=hh.T @ dO)
+
+
+# ----------------------------------------------------- closed-form counts ---
+
+def gemm_macs_fwd(T, h, f, k):
+    """Forward expert multiply-adds, 3*k*T*h*f.
+
+    Review §三 核心公式: comp_time = 3k * bsh * h_ffn / n / peak, at n = 1,
+    with bs = T tokens (each MAC of the three h x h_ffn matmuls per copy).
+    """
+    return 3 * k * T * h * f
+
+
+def dispatch_bytes_per_token(k, h, elem_bytes=2):
+    """Bytes one token contributes to dispatch: k copies of its h-vector,
+    k*h*2 in BF16 (digest §3.2 table: 3 x 4096 x 2 = 24,576 B)."""
+    return k * h * elem_bytes
+
+
+def activation_bytes(b, s, h, elem_bytes=2):
+    """Bytes of a [b*s, h] activation, bsh*2 in BF16 (digest §3.2 table)."""
+    return b * s * h * elem_bytes
