@@ -1,0 +1,397 @@
+"""Benchmark: one MoE FFN layer, forward + backward, on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is moe_layer_fwd + moe_layer_bwd (route, dispatch, SwiGLU GroupedGEMM
+experts, combine and the full backward) over one batch of T synthetic tokens,
+inputs resident in HBM.  Under torchrun every rank runs its own replica (the
+path has no cross-GPU exchange); the time is the max over ranks.  Rank 0
+prints one JSON line.
+
+`--impl reference` times the CPU oracle instead (the only implementation of
+the method besides ours), on a bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from routing_grouped_expert_router_gb300 import configs as mcfg  # noqa: E402
+from routing_grouped_expert_router_gb300 import metrics  # noqa: E402
+from routing_grouped_expert_router_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s fwd+bwd; GroupedGEMM TFLOP/s as % of GB300 BF16 peak"
+GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc2_dgrad_swiglu_bwd", "gg_fc2_wgrad",
+         "gg_fc1_dgrad", "gg_fc1_wgrad")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--config", default=mcfg.BENCH_CONFIG, choices=sorted(mcfg.CONFIGS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-sample-tokens", type=int, default=16)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_desc(cfg):
+    return (f"{cfg.name}: T={cfg.T} h={cfg.h} h_ffn={cfg.f} E={cfg.E} top-{cfg.k}"
+            + (f" zipf{cfg.zipf_s}" if cfg.zipf_s else ""))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks ---
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.device = device
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [q.strip() for q in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ our layer ---
+class Layer:
+    def __init__(self, cfg, device):
+        from routing_grouped_expert_router_gb300 import binding as mb
+        self.mb = mb
+        self.cfg = cfg
+        self.d = mb.dims_of(cfg)
+        T, h, f, E = cfg.T, cfg.h, cfg.f, cfg.E
+        dev = device
+        self.saved = torch.zeros(mb.moe_saved_bytes(self.d), dtype=torch.uint8, device=dev)
+        self.ws_f = torch.zeros(mb.moe_workspace_bytes(self.d, mb.OP_LAYER_FWD), dtype=torch.uint8,
+                                device=dev)
+        self.ws_b = torch.zeros(mb.moe_workspace_bytes(self.d, mb.OP_LAYER_BWD), dtype=torch.uint8,
+                                device=dev)
+        self.y = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        self.dWg = torch.empty(h, E, dtype=torch.float32, device=dev)
+        self.dW1 = torch.empty(E, h, f, dtype=torch.float32, device=dev)
+        self.dW3 = torch.empty(E, h, f, dtype=torch.float32, device=dev)
+        self.dW2 = torch.empty(E, f, h, dtype=torch.float32, device=dev)
+
+    def step(self, inp, x=None, dy=None):
+        mb = self.mb
+        x = inp["x"] if x is None else x
+        dy = inp["dy"] if dy is None else dy
+        b = inp["b"] if self.d.has_bias else None
+        mb.moe_layer_fwd(self.d, x, inp["Wg"], b, inp["W1"], inp["W3"], inp["W2"], self.y,
+                         self.saved, self.ws_f)
+        mb.moe_layer_bwd(self.d, x, dy, inp["Wg"], inp["W1"], inp["W3"], inp["W2"], self.saved,
+                         self.dx, self.dWg, self.dW1, self.dW3, self.dW2, self.ws_b)
+
+
+def run_ours(args, cfg, world, rank, local):
+    from routing_grouped_expert_router_gb300 import binding as mb
+    from routing_grouped_expert_router_gb300 import build as mbuild
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0 or world == 1:
+        mbuild.build()
+    if world > 1:
+        dist.barrier()
+    mb.load()
+    cfg_r = mcfg.LayerConfig(**{**cfg.as_dict(), "seed": cfg.seed + 1000 * rank}) if rank else cfg
+    inp = synth.make_layer(cfg_r, device)
+    layer = Layer(cfg_r, device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        layer.step(inp)
+    torch.cuda.synchronize(device)
+    st = max(mb.moe_read_device_status(layer.ws_f), mb.moe_read_device_status(layer.ws_b))
+    if st != mb.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {mb.status_string(st)}")
+
+    # per-kernel events for every launch of the timed region
+    per_step = 32
+    nev = args.steps * per_step
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize(device)
+    handles = (ctypes.c_void_p * nev)(*[e.cuda_event for e in evs])
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    sampler.start()
+    mb.moe_profile_events(ctypes.addressof(handles), nev)
+    start.record(stream)
+    for _ in range(args.steps):
+        layer.step(inp)
+    end.record(stream)
+    launches = mb.moe_profile_events(None, 0)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = max(mb.moe_read_device_status(layer.ws_f), mb.moe_read_device_status(layer.ws_b))
+    if st != mb.MOE_OK:
+        raise RuntimeError(f"device status after timing: {mb.status_string(st)}")
+
+    # per-kernel durations: event i closes launch i; the step's first launch
+    # starts at the previous event (or `start`)
+    names = [mb.moe_profile_kernel_name(i) for i in range(launches)]
+    per_kernel = {}
+    prev = start
+    for i in range(launches):
+        dt = prev.elapsed_time(evs[i])
+        per_kernel.setdefault(names[i], []).append(dt)
+        prev = evs[i]
+
+    result = {"ms": ms, "per_kernel": per_kernel, "launches": launches, "clocks": clocks}
+
+    # e2e: host buffers, H2D of the step's inputs, D2H of its outputs
+    if not args.no_e2e:
+        x_h = inp["x"].cpu().pin_memory()
+        dy_h = inp["dy"].cpu().pin_memory()
+        y_h = torch.empty_like(x_h).pin_memory()
+        dx_h = torch.empty_like(x_h).pin_memory()
+        x_d = torch.empty_like(inp["x"])
+        dy_d = torch.empty_like(inp["dy"])
+
+        def e2e_step():
+            x_d.copy_(x_h, non_blocking=True)
+            dy_d.copy_(dy_h, non_blocking=True)
+            layer.step(inp, x_d, dy_d)
+            y_h.copy_(layer.y, non_blocking=True)
+            dx_h.copy_(layer.dx, non_blocking=True)
+
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize(device)
+        ms2 = s2.elapsed_time(e2)
+        if world > 1:
+            t = torch.tensor([ms2], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms2 = float(t.item())
+        nb = x_h.numel() * x_h.element_size()
+        result["e2e"] = {"ms": ms2, "h2d": 2 * nb, "d2h": 2 * nb}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+# ------------------------------------------------------- the CPU oracle ---
+def oracle_sample(cfg, ntok, seed_offset=0):
+    """Inputs of a bounded sample: the first `ntok` tokens of the workload
+    (all experts' weights), on the host."""
+    sub = mcfg.LayerConfig(**{**cfg.as_dict(), "T": ntok})
+    return synth.make_layer(sub, "cpu")
+
+
+def time_oracle(cfg, ntok, steps, warmup):
+    import oracle
+    inp = oracle_sample(cfg, ntok)
+    threads = torch.get_num_threads()
+
+    def one():
+        y, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
+                                  cfg.k)
+        oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    return ntok * steps / dt, dt, threads
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info()]
+        return max(n) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main ---
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    cfg = mcfg.get(args.config)
+    peaks, peak_src = load_peaks()
+    workload = workload_desc(cfg)
+    n = max(args.gpus, world)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ntok = args.cpu_sample_tokens
+        tps, dt, _ = time_oracle(cfg, ntok, args.steps, args.warmup)
+        cores = blas_threads()
+        line = {
+            "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+            "n_gpus": n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "sample_tokens_per_step": ntok},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {ntok} tokens of the workload per step, all "
+                                       f"{cfg.E} experts, fwd+bwd in float64"},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, cfg, world, rank, local)
+    if rank != 0:
+        return
+    K = args.steps
+    ms_step = r["ms"] / K
+    tokens_per_s = metrics.tokens_per_s(cfg.T * n * K, r["ms"])
+    work = metrics.kernel_work(cfg.T, cfg.h, cfg.f, cfg.E, cfg.k)
+    kern = {}
+    for name, ts in r["per_kernel"].items():
+        avg = sum(ts) / len(ts)
+        ent = {"launches": len(ts), "avg_ms": avg, "share": sum(ts) / r["ms"]}
+        if name in work["flops"]:
+            ent["tflops"] = metrics.tflops(work["flops"][name], avg)
+        elif name in work["bytes"]:
+            ent["gbs"] = metrics.gbs(work["bytes"][name], avg)
+            ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+        kern[name] = ent
+    gemm_ms = sum(sum(r["per_kernel"].get(g, [])) for g in GEMMS)
+    gemm_flops = cfg.gemm_flops_fwd_bwd() * K
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    dominant = max((g for g in GEMMS if g in r["per_kernel"]),
+                   key=lambda g: sum(r["per_kernel"][g]))
+    dom_avg = sum(r["per_kernel"][dominant]) / len(r["per_kernel"][dominant])
+    achieved = metrics.tflops(work["flops"][dominant], dom_avg)
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": n,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload, "T": cfg.T, "h": cfg.h, "h_ffn": cfg.f, "E": cfg.E,
+                   "top_k": cfg.k, "tokens_per_gpu_per_step": cfg.T,
+                   "parallelism": f"replicas{n}" if n > 1 else "single",
+                   "l2": "inputs larger than L2 (weights + activations ~ GBs per step), no flush"},
+        "gemm_tflops": gemm_tflops,
+        "gemm_pct_of_bf16_peak": (100.0 * gemm_tflops / peak_tf) if gemm_tflops else None,
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "kernels": kern,
+    }
+    if "e2e" in r:
+        e = r["e2e"]
+        line["e2e"] = {"value": metrics.tokens_per_s(cfg.T * n * K, e["ms"]), "unit": "tokens/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "note": "x, dy copied from pinned host memory each step; y, dx read back;"
+                               " weights and weight gradients stay resident"}
+    if not args.no_cpu_baseline and n == 1:
+        ntok = args.cpu_sample_tokens
+        tps, dt, _ = time_oracle(cfg, ntok, 1, 0)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"first {ntok} tokens of the workload, all {cfg.E} "
+                                          f"experts, one fwd+bwd in float64 ({dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

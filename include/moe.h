@@ -1,0 +1,225 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300: one dropless top-k Mixture-of-Experts FFN
+ * layer with SwiGLU experts, forward and backward, on one GB300 (sm_103a).
+ *
+ * The layer (sources named by page title and section):
+ *   - a trainable gate scores every expert per token; the k experts with the
+ *     highest probability are chosen and their outputs summed, weighted
+ *     (DisagMoE, §2.1 "混合专家（MoE）结构");
+ *   - token copies are sorted by expert, then by source, so that each expert's
+ *     rows are contiguous (MegaScale-MoE research digest, §3.3 under Diagram C);
+ *   - the experts are SwiGLU FFNs run together as one GroupedGEMM, "one kernel
+ *     for the matrix products of several experts" (digest, glossary; MegaScale-
+ *     MoE paper review, §三 核心公式 and 训练流程);
+ *   - forward and backward are explicit operators, not autograd (digest §3.3).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named x, Wg, W1 ... and every output are DEVICE pointers owned by
+ *     the caller.  The library never allocates device memory and never frees
+ *     any.  Scratch space is the caller's `ws` buffer of at least
+ *     moe_workspace_bytes() bytes; the layer context is the caller's `saved`
+ *     buffer of moe_saved_bytes() bytes.  Every pointer must be 16-byte
+ *     aligned; ws and saved must be 256-byte aligned.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream); the
+ *     library never synchronises except in moe_read_device_status().
+ *   - All matrices are row-major and dense:
+ *       x, dy, y, dx : [T, h]   bf16        Wg, dWg : [h, E] fp32    b : [E] fp32
+ *       W1, W3       : [E, h, f] bf16       W2      : [E, f, h] bf16
+ *       dW1, dW3     : [E, h, f] fp32       dW2     : [E, f, h] fp32
+ *       topk_idx     : [T, k] int32         gates   : [T, k] fp32
+ *     An assignment a = t*k + j is token t's j-th chosen expert.  A permuted
+ *     row p indexes the expert-major order: rows offsets[e] .. offsets[e+1]-1
+ *     belong to expert e, in ascending a.
+ *   - Gradients are written, not accumulated.  An expert that receives no
+ *     token gets zero weight gradients.
+ *   - Argument errors are found on the host before any launch and returned as
+ *     a status; nothing is launched then.  CUDA launch errors return
+ *     MOE_ERR_CUDA.  Device code never traps or prints: a kernel whose bounded
+ *     wait runs out records MOE_ERR_DEVICE_TIMEOUT in the status word at the
+ *     start of `ws` and returns; moe_read_device_status() reports it.
+ *   - Supported shapes: 1 <= k <= 8, k <= E <= 64, T*k < 2^31, h and f
+ *     multiples of 64 (the GEMMs' K blocks are 64 wide).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t;   /* == cudaStream_t */
+typedef struct CUevent_st* moe_event_t;     /* == cudaEvent_t */
+typedef uint16_t moe_bf16;                  /* bf16 bit pattern */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad dimension */
+  MOE_ERR_UNSUPPORTED = 2,     /* shape outside the supported set */
+  MOE_ERR_WORKSPACE = 3,       /* ws_bytes smaller than required */
+  MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait ran out */
+} moe_status;
+
+typedef struct {
+  int32_t T;         /* tokens */
+  int32_t h;         /* hidden size */
+  int32_t f;         /* expert FFN width (h_ffn) */
+  int32_t E;         /* experts */
+  int32_t k;         /* experts per token */
+  int32_t has_bias;  /* 1: router bias b[E] is added to the logits */
+} moe_dims;
+
+typedef enum {
+  MOE_OP_ROUTE = 0,
+  MOE_OP_PERMUTE = 1,
+  MOE_OP_EXPERT_FFN_FWD = 2,
+  MOE_OP_EXPERT_FFN_BWD = 3,
+  MOE_OP_ROUTER_BWD = 4,
+  MOE_OP_LAYER_FWD = 5,
+  MOE_OP_LAYER_BWD = 6
+} moe_op;
+
+/* Scratch bytes entry point `op` needs for `dims` (0 on invalid dims).  The
+ * first 256 bytes of every workspace hold the device status word; zero the
+ * workspace once before first use (or call moe_clear_device_status). */
+size_t moe_workspace_bytes(const moe_dims* dims, int op);
+
+/* Bytes of the forward->backward context that moe_layer_fwd writes into
+ * `saved` and moe_layer_bwd reads: routing, dispatch maps, the permuted token
+ * rows and the expert activations A = X W1, B = X W3, H = silu(A)*B, O = H W2
+ * (the expensive activations are kept, per the review's 选择性激活重计算). */
+size_t moe_saved_bytes(const moe_dims* dims);
+
+/* Router logits l = x Wg (+ b), softmax over the E experts, top-k selection
+ * (descending logit, ties to the lower expert id) and renormalisation of the
+ * k probabilities: gates[t,j] = p[e_j] / sum_j' p[e_j'].  DisagMoE §2.1.
+ * In: x [T,h] bf16, Wg [h,E] fp32, b [E] fp32 (ignored unless has_bias).
+ * Out: topk_idx [T,k] int32, gates [T,k] fp32.  Logits accumulate in fp32. */
+moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const float* Wg,
+                     const float* b, int32_t* topk_idx, float* gates,
+                     void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Dispatch: per-expert histogram, exclusive scan and the stable expert-major
+ * permutation (digest §3.3: sorted by expert, then by source; review §四:
+ * the scatter that makes each expert's tokens contiguous).  Deterministic,
+ * no atomics.
+ * In: topk_idx [T,k]; x [T,h] bf16 or NULL.
+ * Out: counts [E], offsets [E+1] (offsets[E] = T*k), perm_src [T*k]
+ * (permuted row -> assignment), perm_dst [T*k] (assignment -> permuted row),
+ * and, when x and x_perm are both non-NULL, x_perm [T*k,h] with
+ * x_perm[p] = x[perm_src[p] / k]. */
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx,
+                       const moe_bf16* x, int32_t* counts, int32_t* offsets,
+                       int32_t* perm_src, int32_t* perm_dst, moe_bf16* x_perm,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Inverse row move: rows_assign[a] = rows_perm[perm_dst[a]] for a < T*k.
+ * rows_perm, rows_assign: [T*k, h] bf16. */
+moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst,
+                         const moe_bf16* rows_perm, moe_bf16* rows_assign,
+                         moe_stream_t stream);
+
+/* Expert SwiGLU FFN as GroupedGEMMs over the expert-contiguous rows:
+ * for each e and rows p of e, with X[p] = x[perm_src[p] / k]:
+ *   A = X W1[e],  B = X W3[e],  H = silu(A) * B,  O = H W2[e]
+ * (review §三 核心公式: SwiGLU with MoE, 3k*bsh*h_ffn multiply-adds).
+ * bf16 operands, fp32 accumulation in tensor memory; A, B, H, O stored bf16
+ * [T*k, f] / [T*k, h].  offsets is read on the device only. */
+moe_status moe_expert_ffn_fwd(const moe_dims* dims, const moe_bf16* x,
+                              const int32_t* perm_src, const int32_t* offsets,
+                              const moe_bf16* W1, const moe_bf16* W3,
+                              const moe_bf16* W2, moe_bf16* A, moe_bf16* B,
+                              moe_bf16* H, moe_bf16* O,
+                              void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Gate-weighted combine: y[t] = sum_{j<k} gates[t,j] * O[perm_dst[t*k+j]],
+ * summed in fp32 in slot order, rounded once to bf16.  Deterministic (a
+ * gather, no scatter-add).  DisagMoE §2.1 (weighted sum). */
+moe_status moe_combine(const moe_dims* dims, const moe_bf16* O,
+                       const float* gates, const int32_t* perm_dst,
+                       moe_bf16* y, moe_stream_t stream);
+
+/* Backward of the expert FFN for the loss gradient dy [T,h]:
+ *   dO[p] = gates[a] * dy[t]          (a = perm_src[p], t = a / k)
+ *   dg[a] = <dy[t], O[p]>             (gradient of the gate, fp32 [T*k])
+ *   dH = dO W2[e]^T ; dA = dH * B * s (1 + A (1 - s)), s = sigmoid(A) ;
+ *   dB = dH * silu(A)
+ *   dW2[e] = H_e^T dO_e ; dW1[e] = X_e^T dA_e ; dW3[e] = X_e^T dB_e
+ *   dX_perm = dA W1[e]^T + dB W3[e]^T          (fp32 [T*k, h])
+ * FC2's gradients take fc2_in = H and the gradient of fc2_out (review
+ * 选择性激活重计算).  A, B, H, O are moe_expert_ffn_fwd's outputs. */
+moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x,
+                              const moe_bf16* dy, const float* gates,
+                              const int32_t* perm_src, const int32_t* offsets,
+                              const moe_bf16* W1, const moe_bf16* W3,
+                              const moe_bf16* W2, const moe_bf16* A,
+                              const moe_bf16* B, const moe_bf16* H,
+                              const moe_bf16* O, float* dX_perm, float* dg,
+                              float* dW1, float* dW3, float* dW2,
+                              void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Router backward and the token gradient:
+ *   dl[t,j] = g_j (dg_j - sum_i g_i dg_i)     (softmax over the k selected)
+ *   dx[t]   = sum_j dX_perm[perm_dst[t*k+j]] + sum_j dl[t,j] Wg[:, e_j]  (bf16)
+ *   dWg     = x^T dl (fp32 [h,E]; a fixed-order two-level reduction)
+ * In: x, Wg, topk_idx, gates, dg [T*k], dX_perm [T*k,h] fp32, perm_src,
+ * perm_dst, offsets. */
+moe_status moe_router_bwd(const moe_dims* dims, const moe_bf16* x,
+                          const float* Wg, const int32_t* topk_idx,
+                          const float* gates, const float* dg,
+                          const float* dX_perm, const int32_t* perm_src,
+                          const int32_t* perm_dst, const int32_t* offsets,
+                          moe_bf16* dx, float* dWg,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Whole layer forward: route, permute, expert FFN, combine.  Writes y [T,h]
+ * and the context `saved` (moe_saved_bytes) for moe_layer_bwd. */
+moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x,
+                         const float* Wg, const float* b, const moe_bf16* W1,
+                         const moe_bf16* W3, const moe_bf16* W2, moe_bf16* y,
+                         void* saved, void* ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* Whole layer backward from `saved`: writes dx [T,h] bf16 and the fp32
+ * gradients dWg, dW1, dW3, dW2.  The router bias gets no gradient. */
+moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x,
+                         const moe_bf16* dy, const float* Wg,
+                         const moe_bf16* W1, const moe_bf16* W3,
+                         const moe_bf16* W2, const void* saved, moe_bf16* dx,
+                         float* dWg, float* dW1, float* dW3, float* dW2,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Views into a `saved` context (device pointers at fixed offsets; NULL on
+ * invalid dims).  Names: "topk_idx", "gates", "counts", "offsets",
+ * "perm_src", "perm_dst", "x_perm", "A", "B", "H", "O". */
+void* moe_saved_view(const moe_dims* dims, void* saved, const char* name);
+
+/* Human-readable name of a status. */
+const char* moe_status_string(moe_status status);
+
+/* Synchronises `stream`, returns the status word at the start of `ws` and
+ * clears it.  MOE_ERR_CUDA if the synchronisation itself failed. */
+moe_status moe_read_device_status(void* ws, moe_stream_t stream);
+
+/* Zeroes the status word at the start of `ws` (asynchronous). */
+moe_status moe_clear_device_status(void* ws, moe_stream_t stream);
+
+/* Measurement hook: while `events` is non-NULL, every kernel the library
+ * launches from this host thread is followed by cudaEventRecord of the next
+ * event on the launching stream (up to `capacity`).  Pass NULL to stop; the
+ * return value is the number of events recorded since the previous call.
+ * moe_profile_kernel_name(i) names the kernel recorded by event i. */
+int moe_profile_events(moe_event_t* events, int capacity);
+const char* moe_profile_kernel_name(int i);
+
+/* Library build string (arch, version). */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

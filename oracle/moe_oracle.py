@@ -44,7 +44,8 @@ import numpy as np
 __all__ = [
     "as_f64", "router_logits", "route", "dispatch", "permute_rows",
     "unpermute_rows", "silu", "expert_ffn_fwd", "combine", "layer_fwd",
-    "expert_ffn_bwd", "router_bwd", "layer_bwd", "token_fwd_bwd",
+    "expert_ffn_bwd", "router_bwd", "layer_bwd", "token_fwd_bwd", "expert_terms",
+    "assemble_token",
     "expert_wgrad_columns", "condition_router_margins", "router_margin",
     "gemm_macs_fwd", "dispatch_bytes_per_token", "activation_bytes",
 ]
@@ -334,6 +335,45 @@ def layer_bwd(dy, x, Wg, W1, W3, W2, ctx, counter=None):
 
 # ---------------------------------------------- per-token / sampled forms ---
 
+def expert_terms(X, dY, g, W1e, W3e, W2e):
+    """Rows X [n,h] through one expert, with their gates g [n] and loss rows dY.
+
+    Returns o = FFN_e(X) [n,h], dg = <dY, o> [n] and dx_e = g * J_e(X)^T dY
+    [n,h], the expert's part of the token gradient (the SwiGLU chain rule:
+    dH = g dY W2^T, dA = dH * B * s (1 + A (1 - s)), dB = dH * silu(A),
+    dx = dA W1^T + dB W3^T).
+    """
+    X = np.asarray(X, dtype=np.float64).reshape(-1, W1e.shape[0])
+    dY = np.asarray(dY, dtype=np.float64).reshape(X.shape[0], -1)
+    g = np.asarray(g, dtype=np.float64).reshape(-1, 1)
+    a = X @ W1e
+    bb = X @ W3e
+    o = (silu(a) * bb) @ W2e
+    dg = np.einsum("nh,nh->n", dY, o)
+    dh = g * (dY @ W2e.T)
+    s = _sigmoid(a)
+    da = dh * bb * s * (1.0 + a * (1.0 - s))
+    db = dh * silu(a)
+    return dict(o=o, dg=dg, dx=da @ W1e.T + db @ W3e.T)
+
+
+def assemble_token(gates, idx, terms, Wg):
+    """y, dg and dx of one token from its k per-expert terms (slot order).
+
+    terms[j] = expert_terms(...) of slot j for this token (one row each).
+    dx adds the router path: sum_j dl_j Wg[:, e_j], dl = router_bwd(g, dg).
+    """
+    g = np.asarray(gates, dtype=np.float64)
+    y = sum(g[j] * terms[j]["o"][0] for j in range(len(idx)))
+    dg = np.array([terms[j]["dg"][0] for j in range(len(idx))])
+    dl = router_bwd(g[None, :], dg[None, :])[0]
+    Wg64 = as_f64(Wg)
+    dx = sum(terms[j]["dx"][0] for j in range(len(idx)))
+    for j, e in enumerate(idx):
+        dx = dx + dl[j] * Wg64[:, int(e)]
+    return dict(y=y, dg=dg, dx=dx)
+
+
 def token_fwd_bwd(x_t, dy_t, Wg, b, k, expert):
     """The layer for one token, straight from the definition (no dispatch).
 
@@ -342,30 +382,13 @@ def token_fwd_bwd(x_t, dy_t, Wg, b, k, expert):
     dx = sum_j g_j J_{e_j}(x_t)^T dy + sum_j dl_j Wg[:, e_j].
     """
     x = as_f64(x_t).reshape(1, -1)
-    dy = as_f64(dy_t).reshape(-1)
+    dy = as_f64(dy_t).reshape(1, -1)
     idx, gates, _ = route(x_t.reshape(1, -1), Wg, b, k)
     idx, gates = idx[0], gates[0]
-    Wg64 = as_f64(Wg)
-    y = np.zeros(x.shape[1])
-    dx = np.zeros(x.shape[1])
-    dg = np.zeros(k)
-    for j, e in enumerate(idx):
-        W1e, W3e, W2e = expert(int(e))
-        a = (x @ W1e)[0]
-        bb = (x @ W3e)[0]
-        hh = silu(a) * bb
-        o = hh @ W2e
-        y += gates[j] * o
-        dg[j] = dy @ o
-        dh = gates[j] * (W2e @ dy)
-        s = _sigmoid(a)
-        da = dh * bb * s * (1.0 + a * (1.0 - s))
-        db = dh * silu(a)
-        dx += W1e @ da + W3e @ db
-    dl = router_bwd(gates[None, :], dg[None, :])[0]
-    for j, e in enumerate(idx):
-        dx += dl[j] * Wg64[:, int(e)]
-    return dict(topk_idx=idx, gates=gates, y=y, dg=dg, dx=dx)
+    terms = [expert_terms(x, dy, gates[j], *expert(int(e))) for j, e in enumerate(idx)]
+    out = assemble_token(gates, idx, terms, Wg)
+    out.update(topk_idx=idx, gates=gates)
+    return out
 
 
 def expert_wgrad_columns(X_e, dO_e, W1e, W3e, W2e, cols):

@@ -1,0 +1,540 @@
+// api.cu -- the C ABI of libmoe_gb300 (declared in include/moe.h).
+//
+// Host-side only: validates arguments before any launch, carves the caller's
+// workspace and context buffers, and enqueues the kernels of each operation on
+// the caller's stream.  No device memory is allocated here and no call
+// synchronises except moe_read_device_status.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/moe.h"
+#include "grouped_gemm.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+using moe::GemmProblem;
+
+constexpr size_t kAlign = 256;
+constexpr size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// ------------------------------------------------------- measurement hook
+struct ProfileState {
+  cudaEvent_t* events = nullptr;
+  int capacity = 0;
+  int count = 0;
+  const char* names[4096];
+};
+thread_local ProfileState g_prof;
+
+bool note(cudaStream_t s, const char* name) {
+  if (!g_prof.events) return true;
+  if (g_prof.count >= g_prof.capacity) return true;
+  if (g_prof.count < 4096) g_prof.names[g_prof.count] = name;
+  return cudaEventRecord(g_prof.events[g_prof.count++], s) == cudaSuccess;
+}
+
+// ----------------------------------------------------------- validation
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool ptr_ok(const void* p) { return p != nullptr && aligned(p, 16); }
+// A buffer of `bytes` bytes: may be NULL only when it is empty.
+bool buf_ok(const void* p, size_t bytes) {
+  return bytes == 0 ? (p == nullptr || aligned(p, 16)) : ptr_ok(p);
+}
+
+moe_status check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->h <= 0 || d->f <= 0 || d->E <= 0 || d->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->k > d->E) return MOE_ERR_INVALID_ARG;
+  if (d->k > 8 || d->E > moe::kRouterMaxE) return MOE_ERR_UNSUPPORTED;
+  if (d->h % 64 != 0 || d->f % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->T) * d->k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// ------------------------------------------------------------- layouts
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t o = off;
+    off += align_up(bytes);
+    return o;
+  }
+};
+
+size_t rows_of(const moe_dims& d) { return static_cast<size_t>(d.T) * d.k; }
+
+struct SavedLayout {
+  size_t topk_idx, gates, counts, offsets, perm_src, perm_dst, x_perm, A, B, H, O, total;
+};
+SavedLayout saved_layout(const moe_dims& d) {
+  const size_t R = rows_of(d);
+  Carve c;
+  SavedLayout L;
+  L.topk_idx = c.take(R * 4);
+  L.gates = c.take(R * 4);
+  L.counts = c.take(static_cast<size_t>(d.E) * 4);
+  L.offsets = c.take(static_cast<size_t>(d.E + 1) * 4);
+  L.perm_src = c.take(R * 4);
+  L.perm_dst = c.take(R * 4);
+  L.x_perm = c.take(R * d.h * 2);
+  L.A = c.take(R * d.f * 2);
+  L.B = c.take(R * d.f * 2);
+  L.H = c.take(R * d.f * 2);
+  L.O = c.take(R * d.h * 2);
+  L.total = c.off;
+  return L;
+}
+
+struct WsLayout {
+  size_t status = 0;
+  size_t blk_counts = 0, bases = 0;          // dispatch
+  size_t x_perm = 0, dO = 0, dA = 0, dB = 0;  // expert backward
+  size_t dX = 0, dg = 0;                     // layer backward
+  size_t dl = 0, WgT = 0, partial = 0;       // router backward
+  size_t total = 0;
+};
+WsLayout ws_layout(const moe_dims& d, int op) {
+  const size_t R = rows_of(d);
+  const size_t nblk = static_cast<size_t>(moe::dispatch_blocks(static_cast<long long>(R)));
+  Carve c;
+  WsLayout L;
+  L.status = c.take(kAlign);
+  auto dispatch = [&] {
+    L.blk_counts = c.take(nblk * d.E * 4);
+    L.bases = c.take(nblk * d.E * 4);
+  };
+  auto router_bwd = [&] {
+    L.dl = c.take(static_cast<size_t>(d.T) * d.E * 4);
+    L.WgT = c.take(static_cast<size_t>(d.E) * d.h * 4);
+    L.partial = c.take(static_cast<size_t>(moe::wgrad_router_chunks(d.T)) * d.h * d.E * 4);
+  };
+  auto expert_bwd = [&](bool with_x) {
+    if (with_x) L.x_perm = c.take(R * d.h * 2);
+    L.dO = c.take(R * d.h * 2);
+    L.dA = c.take(R * d.f * 2);
+    L.dB = c.take(R * d.f * 2);
+  };
+  switch (op) {
+    case MOE_OP_ROUTE: break;
+    case MOE_OP_PERMUTE: dispatch(); break;
+    case MOE_OP_EXPERT_FFN_FWD: L.x_perm = c.take(R * d.h * 2); break;
+    case MOE_OP_EXPERT_FFN_BWD: expert_bwd(true); break;
+    case MOE_OP_ROUTER_BWD: router_bwd(); break;
+    case MOE_OP_LAYER_FWD: dispatch(); break;
+    case MOE_OP_LAYER_BWD:
+      expert_bwd(false);
+      L.dX = c.take(R * d.h * 4);
+      L.dg = c.take(R * 4);
+      router_bwd();
+      break;
+    default: return WsLayout{};
+  }
+  L.total = c.off;
+  return L;
+}
+
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+template <class T>
+const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const uint8_t*>(base) + off);
+}
+
+moe_status ws_check(const moe_dims& d, int op, const void* ws, size_t ws_bytes) {
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(d, op).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+#define MOE_CU(expr)                                   \
+  do {                                                 \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA;    \
+  } while (0)
+#define MOE_RUN(expr, name)                            \
+  do {                                                 \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA;    \
+    if (!note(stream, name)) return MOE_ERR_CUDA;      \
+  } while (0)
+
+GemmProblem problem(const moe_dims& d, const int32_t* offsets, void* ws) {
+  GemmProblem p;
+  p.E = d.E;
+  p.offsets = offsets;
+  p.rows = static_cast<int>(rows_of(d));
+  p.h = d.h;
+  p.f = d.f;
+  p.status = at<int>(ws, 0);
+  p.num_sms = num_sms();
+  return p;
+}
+
+// --------------------------------------------------------- the steps
+moe_status do_route(const moe_dims& d, const uint16_t* x, const float* Wg, const float* b,
+                    int32_t* idx, float* gates, cudaStream_t stream) {
+  MOE_RUN(moe::launch_router(x, Wg, d.has_bias ? b : nullptr, d.T, d.h, d.E, d.k, idx, gates,
+                             num_sms(), stream),
+          "router_topk");
+  return MOE_OK;
+}
+
+moe_status do_dispatch(const moe_dims& d, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                       int32_t* psrc, int32_t* pdst, void* ws, const WsLayout& L,
+                       cudaStream_t stream) {
+  const long long R = static_cast<long long>(rows_of(d));
+  const int nblk = moe::dispatch_blocks(R);
+  int32_t* blk = at<int32_t>(ws, L.blk_counts);
+  int32_t* bases = at<int32_t>(ws, L.bases);
+  MOE_RUN(moe::launch_dispatch_hist(idx, R, d.E, blk, stream), "dispatch_hist");
+  MOE_RUN(moe::launch_dispatch_scan(blk, nblk, d.E, counts, offsets, bases, stream),
+          "dispatch_scan");
+  MOE_RUN(moe::launch_dispatch_scatter(idx, R, d.E, bases, psrc, pdst, stream),
+          "dispatch_scatter");
+  return MOE_OK;
+}
+
+moe_status do_ffn_fwd(const moe_dims& d, const uint16_t* x_perm, const int32_t* offsets,
+                      const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, uint16_t* A,
+                      uint16_t* B, uint16_t* H, uint16_t* O, void* ws, cudaStream_t stream) {
+  if (rows_of(d) == 0) return MOE_OK;
+  const GemmProblem g = problem(d, offsets, ws);
+  MOE_RUN(moe::gemm_fc1_fwd(g, x_perm, W1, W3, A, B, H, stream), moe::kGemmNames[0]);
+  MOE_RUN(moe::gemm_fc2_fwd(g, H, W2, O, stream), moe::kGemmNames[1]);
+  return MOE_OK;
+}
+
+moe_status do_ffn_bwd(const moe_dims& d, const uint16_t* x_perm, const uint16_t* dO,
+                      const int32_t* offsets, const uint16_t* W1, const uint16_t* W3,
+                      const uint16_t* W2, const uint16_t* A, const uint16_t* B, const uint16_t* H,
+                      uint16_t* dA, uint16_t* dB, float* dX, float* dW1, float* dW3, float* dW2,
+                      void* ws, cudaStream_t stream) {
+  if (rows_of(d) == 0) {
+    const size_t wbytes = static_cast<size_t>(d.E) * d.h * d.f * 4;
+    MOE_RUN(cudaMemsetAsync(dW1, 0, wbytes, stream), "zero_dW1");
+    MOE_RUN(cudaMemsetAsync(dW3, 0, wbytes, stream), "zero_dW3");
+    MOE_RUN(cudaMemsetAsync(dW2, 0, wbytes, stream), "zero_dW2");
+    return MOE_OK;
+  }
+  const GemmProblem g = problem(d, offsets, ws);
+  MOE_RUN(moe::gemm_fc2_dgrad(g, dO, W2, A, B, dA, dB, stream), moe::kGemmNames[2]);
+  MOE_RUN(moe::gemm_fc2_wgrad(g, H, dO, dW2, stream), moe::kGemmNames[4]);
+  MOE_RUN(moe::gemm_fc1_dgrad(g, dA, dB, W1, W3, dX, stream), moe::kGemmNames[3]);
+  MOE_RUN(moe::gemm_fc1_wgrad(g, x_perm, dA, dB, dW1, dW3, stream), moe::kGemmNames[5]);
+  return MOE_OK;
+}
+
+moe_status do_router_bwd(const moe_dims& d, const uint16_t* x, const float* Wg,
+                         const int32_t* idx, const float* gates, const float* dg,
+                         const float* dX, const int32_t* pdst, uint16_t* dx, float* dWg, void* ws,
+                         const WsLayout& L, cudaStream_t stream) {
+  float* WgT = at<float>(ws, L.WgT);
+  float* dl = at<float>(ws, L.dl);
+  float* partial = at<float>(ws, L.partial);
+  MOE_RUN(moe::launch_transpose_wg(Wg, d.h, d.E, WgT, stream), "transpose_wg");
+  MOE_RUN(moe::launch_token_grad(dX, pdst, idx, gates, dg, WgT, d.T, d.k, d.h, d.E, dl, dx,
+                                 num_sms(), stream),
+          "token_grad");
+  MOE_RUN(moe::launch_router_wgrad(x, dl, d.T, d.h, d.E, partial, dWg, stream), "router_wgrad");
+  return MOE_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null, misaligned or inconsistent argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape outside the supported set";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace smaller than required";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+  }
+  return "unknown moe_status";
+}
+
+const char* moe_version(void) { return "libmoe_gb300 0.1 (sm_103a, tcgen05 GroupedGEMM)"; }
+
+size_t moe_workspace_bytes(const moe_dims* dims, int op) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return ws_layout(*dims, op).total;
+}
+
+size_t moe_saved_bytes(const moe_dims* dims) {
+  if (check_dims(dims) != MOE_OK) return 0;
+  return saved_layout(*dims).total;
+}
+
+void* moe_saved_view(const moe_dims* dims, void* saved, const char* name) {
+  if (check_dims(dims) != MOE_OK || !saved || !name) return nullptr;
+  const SavedLayout L = saved_layout(*dims);
+  struct {
+    const char* n;
+    size_t off;
+  } tab[] = {{"topk_idx", L.topk_idx}, {"gates", L.gates},       {"counts", L.counts},
+             {"offsets", L.offsets},   {"perm_src", L.perm_src}, {"perm_dst", L.perm_dst},
+             {"x_perm", L.x_perm},     {"A", L.A},               {"B", L.B},
+             {"H", L.H},               {"O", L.O}};
+  for (auto& e : tab)
+    if (strcmp(e.n, name) == 0) return at<uint8_t>(saved, e.off);
+  return nullptr;
+}
+
+int moe_profile_events(moe_event_t* events, int capacity) {
+  const int n = g_prof.count;
+  g_prof.events = reinterpret_cast<cudaEvent_t*>(events);
+  g_prof.capacity = events ? capacity : 0;
+  g_prof.count = 0;
+  return n;
+}
+
+const char* moe_profile_kernel_name(int i) {
+  if (i < 0 || i >= 4096) return "";
+  return g_prof.names[i] ? g_prof.names[i] : "";
+}
+
+moe_status moe_read_device_status(void* ws, moe_stream_t stream) {
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  MOE_CU(cudaStreamSynchronize(s));
+  MOE_CU(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost));
+  MOE_CU(cudaMemset(ws, 0, sizeof(int)));
+  return static_cast<moe_status>(v);
+}
+
+moe_status moe_clear_device_status(void* ws, moe_stream_t stream) {
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  MOE_CU(cudaMemsetAsync(ws, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const float* Wg, const float* b,
+                     int32_t* topk_idx, float* gates, void* ws, size_t ws_bytes,
+                     moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t T = d.T, R = rows_of(d);
+  if (!buf_ok(x, T * d.h) || !ptr_ok(Wg) || !buf_ok(topk_idx, R) || !buf_ok(gates, R) ||
+      (d.has_bias && !ptr_ok(b)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_ROUTE, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  return do_route(d, x, Wg, b, topk_idx, gates, stream);
+}
+
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const moe_bf16* x,
+                       int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* perm_dst,
+                       moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t R = rows_of(d);
+  if (!buf_ok(topk_idx, R) || !ptr_ok(counts) || !ptr_ok(offsets) || !buf_ok(perm_src, R) ||
+      !buf_ok(perm_dst, R))
+    return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned(x, 16)) || (x_perm && !aligned(x_perm, 16))) return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_PERMUTE, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_PERMUTE);
+  if ((st = do_dispatch(d, topk_idx, counts, offsets, perm_src, perm_dst, ws, L, stream)) != MOE_OK)
+    return st;
+  if (x && x_perm)
+    MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(rows_of(d)), d.T,
+                                    d.h, x_perm, num_sms(), stream),
+            "permute_rows");
+  return MOE_OK;
+}
+
+moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst, const moe_bf16* rows_perm,
+                         moe_bf16* rows_assign, moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t R = rows_of(d);
+  if (!buf_ok(perm_dst, R) || !buf_ok(rows_perm, R) || !buf_ok(rows_assign, R))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  MOE_RUN(moe::launch_gather_rows(rows_perm, perm_dst, 1, static_cast<long long>(rows_of(d)),
+                                  static_cast<long long>(rows_of(d)), d.h, rows_assign, num_sms(),
+                                  stream),
+          "unpermute_rows");
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn_fwd(const moe_dims* dims, const moe_bf16* x, const int32_t* perm_src,
+                              const int32_t* offsets, const moe_bf16* W1, const moe_bf16* W3,
+                              const moe_bf16* W2, moe_bf16* A, moe_bf16* B, moe_bf16* H,
+                              moe_bf16* O, void* ws, size_t ws_bytes, moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t T = d.T, R = rows_of(d);
+  if (!buf_ok(x, T) || !buf_ok(perm_src, R) || !ptr_ok(offsets) || !ptr_ok(W1) || !ptr_ok(W3) ||
+      !ptr_ok(W2) || !buf_ok(A, R) || !buf_ok(B, R) || !buf_ok(H, R) || !buf_ok(O, R))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_EXPERT_FFN_FWD, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_EXPERT_FFN_FWD);
+  uint16_t* xp = at<uint16_t>(ws, L.x_perm);
+  MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(rows_of(d)), d.T, d.h,
+                                  xp, num_sms(), stream),
+          "permute_rows");
+  return do_ffn_fwd(d, xp, offsets, W1, W3, W2, A, B, H, O, ws, stream);
+}
+
+moe_status moe_combine(const moe_dims* dims, const moe_bf16* O, const float* gates,
+                       const int32_t* perm_dst, moe_bf16* y, moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t T = d.T, R = rows_of(d);
+  if (!buf_ok(O, R) || !buf_ok(gates, R) || !buf_ok(perm_dst, R) || !buf_ok(y, T))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  MOE_RUN(moe::launch_combine(O, gates, perm_dst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* dy,
+                              const float* gates, const int32_t* perm_src, const int32_t* offsets,
+                              const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2,
+                              const moe_bf16* A, const moe_bf16* B, const moe_bf16* H,
+                              const moe_bf16* O, float* dX_perm, float* dg, float* dW1,
+                              float* dW3, float* dW2, void* ws, size_t ws_bytes,
+                              moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t T = d.T, R = rows_of(d);
+  if (!buf_ok(x, T) || !buf_ok(dy, T) || !buf_ok(gates, R) || !buf_ok(perm_src, R) ||
+      !ptr_ok(offsets) || !ptr_ok(W1) || !ptr_ok(W3) || !ptr_ok(W2) || !buf_ok(A, R) ||
+      !buf_ok(B, R) || !buf_ok(H, R) || !buf_ok(O, R) || !buf_ok(dX_perm, R) || !buf_ok(dg, R) ||
+      !ptr_ok(dW1) || !ptr_ok(dW3) || !ptr_ok(dW2))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_EXPERT_FFN_BWD, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_EXPERT_FFN_BWD);
+  uint16_t* xp = at<uint16_t>(ws, L.x_perm);
+  uint16_t* dO = at<uint16_t>(ws, L.dO);
+  const long long nrows = static_cast<long long>(R);
+  MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, nrows, d.T, d.h, xp, num_sms(), stream),
+          "permute_rows");
+  MOE_RUN(moe::launch_bwd_prep(dy, O, gates, perm_src, nrows, d.k, d.h, dO, dg, num_sms(), stream),
+          "bwd_prep");
+  return do_ffn_bwd(d, xp, dO, offsets, W1, W3, W2, A, B, H, at<uint16_t>(ws, L.dA),
+                    at<uint16_t>(ws, L.dB), dX_perm, dW1, dW3, dW2, ws, stream);
+}
+
+moe_status moe_router_bwd(const moe_dims* dims, const moe_bf16* x, const float* Wg,
+                          const int32_t* topk_idx, const float* gates, const float* dg,
+                          const float* dX_perm, const int32_t* perm_src, const int32_t* perm_dst,
+                          const int32_t* offsets, moe_bf16* dx, float* dWg, void* ws,
+                          size_t ws_bytes, moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t T = d.T, R = rows_of(d);
+  if (!buf_ok(x, T) || !ptr_ok(Wg) || !buf_ok(topk_idx, R) || !buf_ok(gates, R) ||
+      !buf_ok(dg, R) || !buf_ok(dX_perm, R) || !buf_ok(perm_src, R) || !buf_ok(perm_dst, R) ||
+      !ptr_ok(offsets) || !buf_ok(dx, T) || !ptr_ok(dWg))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_ROUTER_BWD, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_ROUTER_BWD);
+  return do_router_bwd(d, x, Wg, topk_idx, gates, dg, dX_perm, perm_dst, dx, dWg, ws, L, stream);
+}
+
+moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* Wg, const float* b,
+                         const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, moe_bf16* y,
+                         void* saved, void* ws, size_t ws_bytes, moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t T = d.T;
+  if (!buf_ok(x, T) || !ptr_ok(Wg) || !ptr_ok(W1) || !ptr_ok(W3) || !ptr_ok(W2) || !buf_ok(y, T) ||
+      (d.has_bias && !ptr_ok(b)) || !saved || !aligned(saved, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_LAYER_FWD, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_LAYER_FWD);
+  const SavedLayout S = saved_layout(d);
+  int32_t* idx = at<int32_t>(saved, S.topk_idx);
+  float* gates = at<float>(saved, S.gates);
+  int32_t* offsets = at<int32_t>(saved, S.offsets);
+  int32_t* psrc = at<int32_t>(saved, S.perm_src);
+  int32_t* pdst = at<int32_t>(saved, S.perm_dst);
+  uint16_t* xp = at<uint16_t>(saved, S.x_perm);
+  uint16_t* O = at<uint16_t>(saved, S.O);
+  if ((st = do_route(d, x, Wg, b, idx, gates, stream)) != MOE_OK) return st;
+  if ((st = do_dispatch(d, idx, at<int32_t>(saved, S.counts), offsets, psrc, pdst, ws, L,
+                        stream)) != MOE_OK)
+    return st;
+  MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, static_cast<long long>(rows_of(d)), d.T, d.h, xp,
+                                  num_sms(), stream),
+          "permute_rows");
+  if ((st = do_ffn_fwd(d, xp, offsets, W1, W3, W2, at<uint16_t>(saved, S.A),
+                       at<uint16_t>(saved, S.B), at<uint16_t>(saved, S.H), O, ws, stream)) != MOE_OK)
+    return st;
+  MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
+  return MOE_OK;
+}
+
+moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* dy,
+                         const float* Wg, const moe_bf16* W1, const moe_bf16* W3,
+                         const moe_bf16* W2, const void* saved, moe_bf16* dx, float* dWg,
+                         float* dW1, float* dW3, float* dW2, void* ws, size_t ws_bytes,
+                         moe_stream_t stream_) {
+  moe_status st = check_dims(dims);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  const size_t T = d.T;
+  if (!buf_ok(x, T) || !buf_ok(dy, T) || !ptr_ok(Wg) || !ptr_ok(W1) || !ptr_ok(W3) ||
+      !ptr_ok(W2) || !saved || !aligned(saved, kAlign) || !buf_ok(dx, T) || !ptr_ok(dWg) ||
+      !ptr_ok(dW1) || !ptr_ok(dW3) || !ptr_ok(dW2))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_LAYER_BWD, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_LAYER_BWD);
+  const SavedLayout S = saved_layout(d);
+  const int32_t* idx = at<int32_t>(saved, S.topk_idx);
+  const float* gates = at<float>(saved, S.gates);
+  const int32_t* offsets = at<int32_t>(saved, S.offsets);
+  const int32_t* psrc = at<int32_t>(saved, S.perm_src);
+  const int32_t* pdst = at<int32_t>(saved, S.perm_dst);
+  uint16_t* dO = at<uint16_t>(ws, L.dO);
+  float* dX = at<float>(ws, L.dX);
+  float* dg = at<float>(ws, L.dg);
+  const long long R = static_cast<long long>(rows_of(d));
+  MOE_RUN(moe::launch_bwd_prep(dy, at<uint16_t>(saved, S.O), gates, psrc, R, d.k, d.h, dO, dg,
+                               num_sms(), stream),
+          "bwd_prep");
+  if ((st = do_ffn_bwd(d, at<uint16_t>(saved, S.x_perm), dO, offsets, W1, W3, W2,
+                       at<uint16_t>(saved, S.A), at<uint16_t>(saved, S.B),
+                       at<uint16_t>(saved, S.H), at<uint16_t>(ws, L.dA), at<uint16_t>(ws, L.dB),
+                       dX, dW1, dW3, dW2, ws, stream)) != MOE_OK)
+    return st;
+  return do_router_bwd(d, x, Wg, idx, gates, dg, dX, pdst, dx, dWg, ws, L, stream);
+}
+
+}  // extern "C"

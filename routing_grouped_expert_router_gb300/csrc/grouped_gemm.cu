@@ -1,0 +1,632 @@
+// grouped_gemm.cu -- persistent tcgen05/TMEM GroupedGEMM for the SwiGLU experts.
+//
+// One kernel template serves all six expert matmuls of the layer (forward FC1
+// and FC2, the two dgrads and the two ragged-K wgrads).  Design (sm_103a):
+//   * persistent grid, one CTA per SM, 192 threads in three roles:
+//       warp 0     TMA producer: 128B-swizzled tiles into a 4-stage smem ring
+//       warp 1     tensor-memory allocator and MMA issuer (tcgen05.mma,
+//                  128 x 256 x 16 per instruction, fp32 accumulator in TMEM)
+//       warps 2-5  epilogue: tcgen05.ld of the accumulator, fused elementwise
+//                  work (SwiGLU, SwiGLU backward), stores to global memory
+//   * two 256-column TMEM accumulators, so the epilogue of tile i overlaps the
+//     main loop of tile i+1;
+//   * groups come from the device-resident expert offsets: M-grouped matmuls
+//     (forward, dgrad) tile each expert's row range; K-grouped ones (wgrad)
+//     reduce over it, zeroing the k-rows of the last block that belong to the
+//     next expert before they reach the tensor core.
+// Shapes: M tile 128, K block 64 (one 128-byte swizzle row of bf16), N tile
+// 256 accumulator columns (one B operand of 256, or two of 128 sharing A).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "grouped_gemm.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+const char* const kGemmNames[6] = {"gg_fc1_fwd_swiglu", "gg_fc2_fwd",
+                                   "gg_fc2_dgrad_swiglu_bwd", "gg_fc1_dgrad",
+                                   "gg_fc2_wgrad", "gg_fc1_wgrad"};
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KiB
+constexpr int CHUNK_BYTES = 64 * BK * 2;        // one 64 x 64 MN-major box: 8 KiB
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_E = 256;
+constexpr int kTimeoutCode = 5;  // MOE_ERR_DEVICE_TIMEOUT
+
+// Shared memory after the stage ring.
+struct alignas(8) Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int off[MAX_E + 1];   // expert offsets
+  int cum[MAX_E + 1];   // M-grouped: prefix of m-tiles per expert
+};
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + static_cast<int>(sizeof(Ctrl));
+
+enum Epi { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_SWIGLU_BWD = 2, EPI_F32 = 3, EPI_WGRAD = 4 };
+
+struct Params {
+  int E;
+  const int32_t* offsets;
+  int rows;          // permuted rows; offsets are clamped into [0, rows]
+  int M;             // K-grouped: output rows per expert
+  int N;             // output columns per B operand
+  int kblocks;       // M-grouped: K blocks per operand pair
+  int kconcat;       // M-grouped: 2 = after kblocks, continue with (a1, b1)
+  int b_rows;        // rows per expert of the weight tensor viewed 2-D
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* in0;
+  const void* in1;
+  int ldo;           // row stride (elements) of M-grouped outputs and inputs
+  int* status;
+  int ktiles;        // K-grouped: tiles in total
+};
+
+struct Maps {
+  CUtensorMap a0, a1, b0, b1;
+};
+
+struct Tile {
+  int e, mb, nb;
+  int row0;     // M-grouped: first permuted row; K-grouped: first K row
+  int row_end;  // end of the expert's rows
+  int nkb;      // K blocks
+};
+
+template <bool GROUP_K, bool INNER_N, int NUM_B>
+__device__ __forceinline__ bool decode(const Params& p, const Ctrl& c, int t, Tile& tl) {
+  const int NT = (p.N + (BN / NUM_B) - 1) / (BN / NUM_B);
+  if (!GROUP_K) {
+    const int total = NT * c.cum[p.E];
+    if (t >= total) return false;
+    int e = 0;
+    while (NT * c.cum[e + 1] <= t) ++e;
+    const int local = t - NT * c.cum[e];
+    const int mt = c.cum[e + 1] - c.cum[e];
+    tl.e = e;
+    tl.nb = local / mt;
+    tl.mb = local % mt;
+    tl.row0 = c.off[e] + tl.mb * BM;
+    tl.row_end = c.off[e + 1];
+    tl.nkb = p.kblocks * p.kconcat;
+  } else {
+    if (t >= p.ktiles) return false;
+    const int MT = (p.M + BM - 1) / BM;
+    const int per = MT * NT;
+    const int e = t / per;
+    const int local = t - e * per;
+    tl.e = e;
+    if (INNER_N) {
+      tl.mb = local / NT;
+      tl.nb = local % NT;
+    } else {
+      tl.nb = local / MT;
+      tl.mb = local % MT;
+    }
+    tl.row0 = c.off[e];
+    tl.row_end = c.off[e + 1];
+    tl.nkb = (tl.row_end - tl.row0 + BK - 1) / BK;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void store_bf16x32(void* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16(v[8 * i + 0], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+}
+
+__device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 q = __ldg(s + i);
+    uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_f32x32(void* dst, const float* v) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K, bool INNER_N>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gg_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int BNB = BN / NUM_B;  // accumulator columns per B operand
+
+  // ------------------------------------------------------------ set-up
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&c.full[s]), 1);
+      mbar_init(smem_u32(&c.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&c.tfull[b]), 1);
+      mbar_init(smem_u32(&c.tempty[b]), 128);
+    }
+    mbar_init(smem_u32(&c.drain), 1);
+    c.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&maps.a0);
+    tma_prefetch_desc(&maps.b0);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (warp >= 2) {
+    for (int e = threadIdx.x - 64; e <= p.E; e += 128) {
+      const int o = __ldg(p.offsets + e);
+      c.off[e] = o < 0 ? 0 : (o > p.rows ? p.rows : o);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 64) {
+    // ranges must not run backwards; this keeps every store inside its buffer
+    for (int e = 1; e <= p.E; ++e) c.off[e] = max(c.off[e], c.off[e - 1]);
+  }
+  __syncthreads();
+  if (!GROUP_K && threadIdx.x == 64) {
+    c.cum[0] = 0;
+    for (int e = 0; e < p.E; ++e) c.cum[e + 1] = c.cum[e] + (c.off[e + 1] - c.off[e] + BM - 1) / BM;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  volatile int* abort_flag = &c.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int q = 0;
+      bool ok = true;
+      Tile tl;
+      for (int t = blockIdx.x; ok && decode<GROUP_K, INNER_N, NUM_B>(p, c, t, tl); t += gridDim.x) {
+        for (int kb = 0; kb < tl.nkb; ++kb, ++q) {
+          const int s = q % STAGES;
+          const uint32_t ph = (q / STAGES) & 1;
+          if (*abort_flag || !mbar_wait(smem_u32(&c.empty[s]), ph ^ 1, p.status, kTimeoutCode)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&c.full[s]);
+          mbar_expect_tx(full, STAGE_BYTES);
+          const uint32_t a_dst = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t b_dst = a_dst + A_BYTES;
+          if (!GROUP_K) {
+            const bool second = p.kconcat == 2 && kb >= p.kblocks;
+            const int kx = (second ? kb - p.kblocks : kb) * BK;
+            tma_load_2d(a_dst, second ? &maps.a1 : &maps.a0, kx, tl.row0, full);
+            if (!B_MN) {
+              tma_load_2d(b_dst, second ? &maps.b1 : &maps.b0, kx, tl.e * p.b_rows + tl.nb * BNB,
+                          full);
+            } else {
+#pragma unroll
+              for (int i = 0; i < NUM_B; ++i)
+#pragma unroll
+                for (int ch = 0; ch < BNB / 64; ++ch)
+                  tma_load_2d(b_dst + i * (B_BYTES / NUM_B) + ch * CHUNK_BYTES,
+                              i ? &maps.b1 : &maps.b0, tl.nb * BNB + ch * 64,
+                              tl.e * p.b_rows + kx, full);
+            }
+          } else {
+            const int ky = tl.row0 + kb * BK;
+#pragma unroll
+            for (int ch = 0; ch < BM / 64; ++ch)
+              tma_load_2d(a_dst + ch * CHUNK_BYTES, &maps.a0, tl.mb * BM + ch * 64, ky, full);
+#pragma unroll
+            for (int i = 0; i < NUM_B; ++i)
+#pragma unroll
+              for (int ch = 0; ch < BNB / 64; ++ch)
+                tma_load_2d(b_dst + i * (B_BYTES / NUM_B) + ch * CHUNK_BYTES,
+                            i ? &maps.b1 : &maps.b0, tl.nb * BNB + ch * 64, ky, full);
+          }
+        }
+      }
+      if (!ok) {
+        // let every load already issued land before the CTA can exit
+        const int first = q > STAGES ? q - STAGES : 0;
+        for (int r = first; r < q; ++r)
+          mbar_wait(smem_u32(&c.full[r % STAGES]), (r / STAGES) & 1, p.status, kTimeoutCode);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    constexpr uint32_t IDESC = idesc_bf16(BM, BNB, A_MN, B_MN);
+    constexpr uint32_t A_LBO = A_MN ? CHUNK_BYTES : 16;
+    constexpr uint32_t B_LBO = B_MN ? CHUNK_BYTES : 16;
+    constexpr uint32_t A_KSTEP = A_MN ? 2048 : 32;  // bytes per 16-deep K step
+    constexpr uint32_t B_KSTEP = B_MN ? 2048 : 32;
+    int q = 0, it = 0;
+    bool ok = true;
+    Tile tl;
+    for (int t = blockIdx.x; ok && decode<GROUP_K, INNER_N, NUM_B>(p, c, t, tl); t += gridDim.x) {
+      if (tl.nkb == 0) continue;
+      const int buf = it & 1;
+      const uint32_t u = (it >> 1) & 1;
+      ++it;
+      if (*abort_flag || !mbar_wait(smem_u32(&c.tempty[buf]), u ^ 1, p.status, kTimeoutCode)) {
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t acc = tmem_base + buf * BN;
+      for (int kb = 0; kb < tl.nkb; ++kb, ++q) {
+        const int s = q % STAGES;
+        const uint32_t ph = (q / STAGES) & 1;
+        if (*abort_flag || !mbar_wait(smem_u32(&c.full[s]), ph, p.status, kTimeoutCode)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        uint8_t* a_tile = smem + s * STAGE_BYTES;
+        if (GROUP_K) {
+          const int kv = tl.row_end - (tl.row0 + kb * BK);
+          if (kv < BK) {
+            // k-rows kv..63 hold the next expert's rows (or the zero fill):
+            // clear them in A so they add nothing.
+            const int per_chunk = (BK - kv) * 8;  // 16-byte words per chunk
+            for (int w = lane; w < per_chunk * (BM / 64); w += 32) {
+              const int ch = w / per_chunk;
+              const int rem = w - ch * per_chunk;
+              *reinterpret_cast<uint4*>(a_tile + ch * CHUNK_BYTES + kv * 128 + rem * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(a_tile);
+          const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = smem_desc(a_base + kk * A_KSTEP, A_LBO, 1024);
+#pragma unroll
+            for (int i = 0; i < NUM_B; ++i) {
+              const uint64_t bd = smem_desc(b_base + i * (B_BYTES / NUM_B) + kk * B_KSTEP, B_LBO, 1024);
+              umma_bf16(acc + i * BNB, ad, bd, IDESC, (kb | kk) != 0);
+            }
+          }
+          umma_commit(smem_u32(&c.empty[s]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(smem_u32(&c.tfull[buf]));
+      __syncwarp();
+    }
+    // every MMA this thread issued must finish before tensor memory is freed
+    if (lane == 0) {
+      umma_commit(smem_u32(&c.drain));
+      mbar_wait(smem_u32(&c.drain), 0, p.status, kTimeoutCode);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int r = quarter * 32 + lane;
+    int it = 0;
+    Tile tl;
+    for (int t = blockIdx.x; decode<GROUP_K, INNER_N, NUM_B>(p, c, t, tl); t += gridDim.x) {
+      if (*abort_flag) break;
+      if (GROUP_K && tl.nkb == 0) {
+        // expert without tokens: its weight gradient is zero
+        const int orow = tl.mb * BM + r;
+        if (orow < p.M) {
+          float z[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0.f;
+          for (int ch = 0; ch < BNB / 32; ++ch) {
+            const int col = tl.nb * BNB + ch * 32;
+            if (col >= p.N) break;
+            const size_t o = (static_cast<size_t>(tl.e) * p.M + orow) * p.N + col;
+            store_f32x32(static_cast<float*>(p.out0) + o, z);
+            if (NUM_B == 2) store_f32x32(static_cast<float*>(p.out1) + o, z);
+          }
+        }
+        continue;
+      }
+      const int buf = it & 1;
+      const uint32_t u = (it >> 1) & 1;
+      ++it;
+      if (!mbar_wait(smem_u32(&c.tfull[buf]), u, p.status, kTimeoutCode)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+      const int grow = tl.row0 + r;                        // M-grouped row
+      const bool row_ok = GROUP_K ? (tl.mb * BM + r < p.M) : (grow < tl.row_end);
+#pragma unroll 1
+      for (int ch = 0; ch < BNB / 32; ++ch) {
+        float v0[32];
+        float v1[32];
+        tmem_ld32(tbase + ch * 32, v0);
+        if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
+        const int col = tl.nb * BNB + ch * 32;
+        if (!row_ok || col >= p.N) continue;
+        if (EPI == EPI_SWIGLU) {
+          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+          float hv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) hv[i] = silu_f(v0[i]) * v1[i];
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, v1);
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, hv);
+        } else if (EPI == EPI_BF16) {
+          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
+        } else if (EPI == EPI_SWIGLU_BWD) {
+          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+          float av[32], bv[32];
+          load_bf16x32(static_cast<const __nv_bfloat16*>(p.in0) + o, av);
+          load_bf16x32(static_cast<const __nv_bfloat16*>(p.in1) + o, bv);
+          float da[32], db[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = av[i];
+            const float sg = 1.0f / (1.0f + expf(-a));
+            const float dh = v0[i];
+            da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
+            db[i] = dh * a * sg;
+          }
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
+        } else if (EPI == EPI_F32) {
+          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+          store_f32x32(static_cast<float*>(p.out0) + o, v0);
+        } else {  // EPI_WGRAD
+          const int orow = tl.mb * BM + r;
+          const size_t o = (static_cast<size_t>(tl.e) * p.M + orow) * p.N + col;
+          store_f32x32(static_cast<float*>(p.out0) + o, v0);
+          if (NUM_B == 2) store_f32x32(static_cast<float*>(p.out1) + o, v1);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&c.tempty[buf]));
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// bf16 matrix [outer, inner] (row-major), box {box_inner, box_outer}, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K, bool INNER_N>
+cudaError_t launch(const Params& prm, const Maps& maps, int grid, cudaStream_t s) {
+  auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K, INNER_N>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(prm, maps);
+  return cudaGetLastError();
+}
+
+Params base_params(const GemmProblem& g) {
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.E = g.E;
+  p.offsets = g.offsets;
+  p.rows = g.rows;
+  p.status = g.status;
+  p.kconcat = 1;
+  return p;
+}
+
+// Upper bound of an M-grouped tile count without reading the offsets.
+int mgrouped_grid(const GemmProblem& g, int N, int bnb) {
+  const long long nt = (N + bnb - 1) / bnb;
+  const long long mt = (g.rows + BM - 1) / BM + g.E;
+  const long long tiles = nt * mt;
+  return static_cast<int>(tiles < g.num_sms ? tiles : g.num_sms);
+}
+
+}  // namespace
+
+cudaError_t gemm_fc1_fwd(const GemmProblem& g, const void* x_perm, const void* W1,
+                         const void* W3, void* A, void* B, void* H, cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  if (!make_map(&m.a0, x_perm, g.h, g.rows, BK, BM) ||
+      !make_map(&m.b0, W1, g.f, static_cast<uint64_t>(g.E) * g.h, 64, BK) ||
+      !make_map(&m.b1, W3, g.f, static_cast<uint64_t>(g.E) * g.h, 64, BK))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  Params p = base_params(g);
+  p.N = g.f;
+  p.kblocks = g.h / BK;
+  p.b_rows = g.h;
+  p.out0 = A;
+  p.out1 = B;
+  p.out2 = H;
+  p.ldo = g.f;
+  return launch<false, true, 2, EPI_SWIGLU, false, false>(p, m, mgrouped_grid(g, g.f, BN / 2), s);
+}
+
+cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, void* O,
+                         cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  if (!make_map(&m.a0, H, g.f, g.rows, BK, BM) ||
+      !make_map(&m.b0, W2, g.h, static_cast<uint64_t>(g.E) * g.f, 64, BK))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Params p = base_params(g);
+  p.N = g.h;
+  p.kblocks = g.f / BK;
+  p.b_rows = g.f;
+  p.out0 = O;
+  p.ldo = g.h;
+  return launch<false, true, 1, EPI_BF16, false, false>(p, m, mgrouped_grid(g, g.h, BN), s);
+}
+
+cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2, const void* A,
+                           const void* B, void* dA, void* dB, cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  // B operand: W2[e] viewed as [f rows (N), h (K)] -- K-major
+  if (!make_map(&m.a0, dO, g.h, g.rows, BK, BM) ||
+      !make_map(&m.b0, W2, g.h, static_cast<uint64_t>(g.E) * g.f, BK, BN))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Params p = base_params(g);
+  p.N = g.f;
+  p.kblocks = g.h / BK;
+  p.b_rows = g.f;
+  p.in0 = A;
+  p.in1 = B;
+  p.out0 = dA;
+  p.out1 = dB;
+  p.ldo = g.f;
+  return launch<false, false, 1, EPI_SWIGLU_BWD, false, false>(p, m, mgrouped_grid(g, g.f, BN), s);
+}
+
+cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB, const void* W1,
+                           const void* W3, float* dX, cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  // B operands: W1[e], W3[e] viewed as [h rows (N), f (K)] -- K-major
+  if (!make_map(&m.a0, dA, g.f, g.rows, BK, BM) || !make_map(&m.a1, dB, g.f, g.rows, BK, BM) ||
+      !make_map(&m.b0, W1, g.f, static_cast<uint64_t>(g.E) * g.h, BK, BN) ||
+      !make_map(&m.b1, W3, g.f, static_cast<uint64_t>(g.E) * g.h, BK, BN))
+    return cudaErrorInvalidValue;
+  Params p = base_params(g);
+  p.N = g.h;
+  p.kblocks = g.f / BK;
+  p.kconcat = 2;
+  p.b_rows = g.h;
+  p.out0 = dX;
+  p.ldo = g.h;
+  return launch<false, false, 1, EPI_F32, false, false>(p, m, mgrouped_grid(g, g.h, BN), s);
+}
+
+cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, float* dW2,
+                           cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  if (!make_map(&m.a0, H, g.f, g.rows, 64, BK) || !make_map(&m.b0, dO, g.h, g.rows, 64, BK))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Params p = base_params(g);
+  p.M = g.f;
+  p.N = g.h;
+  p.out0 = dW2;
+  const int MT = (g.f + BM - 1) / BM, NT = (g.h + BN - 1) / BN;
+  p.ktiles = g.E * MT * NT;
+  const int grid = p.ktiles < g.num_sms ? p.ktiles : g.num_sms;
+  // N (= h) innermost: the expert's dO rows stay in L2 while H streams once
+  return launch<true, true, 1, EPI_WGRAD, true, true>(p, m, grid, s);
+}
+
+cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void* dA,
+                           const void* dB, float* dW1, float* dW3, cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  if (!make_map(&m.a0, x_perm, g.h, g.rows, 64, BK) || !make_map(&m.b0, dA, g.f, g.rows, 64, BK) ||
+      !make_map(&m.b1, dB, g.f, g.rows, 64, BK))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  Params p = base_params(g);
+  p.M = g.h;
+  p.N = g.f;
+  p.out0 = dW1;
+  p.out1 = dW3;
+  const int MT = (g.h + BM - 1) / BM, NT = (g.f + BN / 2 - 1) / (BN / 2);
+  p.ktiles = g.E * MT * NT;
+  const int grid = p.ktiles < g.num_sms ? p.ktiles : g.num_sms;
+  // M (= h) innermost: the expert's X rows stay in L2 while dA, dB stream once
+  return launch<true, true, 2, EPI_WGRAD, true, false>(p, m, grid, s);
+}
+
+}  // namespace moe

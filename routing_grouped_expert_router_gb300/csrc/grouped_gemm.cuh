@@ -1,0 +1,46 @@
+// grouped_gemm.cuh -- host-side interface of the tcgen05 GroupedGEMMs.
+//
+// "A GroupedGEMM runs the matrix products of several experts in one kernel"
+// (MegaScale-MoE research digest, glossary and §3.3).  One persistent kernel
+// per matmul family handles every expert: the per-expert row ranges come from
+// the device-resident `offsets` array, so no count ever travels to the host.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+struct GemmProblem {
+  int E;                    // experts
+  const int32_t* offsets;   // [E+1] expert row ranges in the permuted order (device)
+  int rows;                 // T*k permuted rows
+  int h, f;                 // hidden size, expert width
+  int* status;              // device status word
+  int num_sms;              // persistent grid size
+};
+
+// A = X W1, B = X W3, H = silu(A) * B for the rows of each expert.
+// X: x_perm [rows, h]; W1, W3: [E, h, f]; outputs [rows, f] bf16.
+cudaError_t gemm_fc1_fwd(const GemmProblem& p, const void* x_perm, const void* W1,
+                         const void* W3, void* A, void* B, void* H, cudaStream_t s);
+// O = H W2 for the rows of each expert.  H: [rows, f]; W2: [E, f, h]; O: [rows, h].
+cudaError_t gemm_fc2_fwd(const GemmProblem& p, const void* H, const void* W2, void* O,
+                         cudaStream_t s);
+// dH = dO W2^T, fused with the SwiGLU backward: dA = dH * B * s (1 + A (1 - s)),
+// dB = dH * silu(A).  dO: [rows, h]; A, B, dA, dB: [rows, f] bf16.
+cudaError_t gemm_fc2_dgrad(const GemmProblem& p, const void* dO, const void* W2,
+                           const void* A, const void* B, void* dA, void* dB, cudaStream_t s);
+// dX_perm = dA W1^T + dB W3^T (K = 2f), fp32 [rows, h].
+cudaError_t gemm_fc1_dgrad(const GemmProblem& p, const void* dA, const void* dB,
+                           const void* W1, const void* W3, float* dX, cudaStream_t s);
+// dW2[e] = H_e^T dO_e, ragged K = rows of e.  fp32 [E, f, h].
+cudaError_t gemm_fc2_wgrad(const GemmProblem& p, const void* H, const void* dO, float* dW2,
+                           cudaStream_t s);
+// dW1[e] = X_e^T dA_e, dW3[e] = X_e^T dB_e.  fp32 [E, h, f].
+cudaError_t gemm_fc1_wgrad(const GemmProblem& p, const void* x_perm, const void* dA,
+                           const void* dB, float* dW1, float* dW3, cudaStream_t s);
+
+// Kernel names, in launch order of a layer, for the measurement hook.
+extern const char* const kGemmNames[6];
+
+}  // namespace moe

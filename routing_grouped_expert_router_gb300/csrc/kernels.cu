@@ -1,0 +1,598 @@
+// kernels.cu -- router, dispatch, row-move, combine and router-backward kernels.
+//
+// Everything here is HBM- or FP32-bound; none of it uses tensor cores.  Every
+// reduction has a fixed order and no kernel uses atomics, so results are
+// bitwise reproducible run to run.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& q, float* v) {
+  v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x);
+  v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+  v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z);
+  v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+}
+
+int grid_for(long long warps_needed, int num_sms, int warps_per_block, int blocks_per_sm) {
+  long long blocks = (warps_needed + warps_per_block - 1) / warps_per_block;
+  long long cap = static_cast<long long>(num_sms) * blocks_per_sm;
+  if (blocks > cap) blocks = cap;
+  return blocks < 1 ? 1 : static_cast<int>(blocks);
+}
+
+// ------------------------------------------------------------------ router
+// A warp owns TOK consecutive tokens.  Lanes split the hidden dimension in
+// 8-element (16-byte) pieces; each lane keeps EP partial logits per token and
+// reuses every router-weight row it loads for all TOK tokens.  A butterfly
+// then gives every lane the full logits; lane j selects for token j.
+template <int EP, int TOK, bool VEC>
+__global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict__ x,
+                                                     const float* __restrict__ Wg,
+                                                     const float* __restrict__ b, int T, int h,
+                                                     int E, int k, int32_t* __restrict__ topk_idx,
+                                                     float* __restrict__ gates) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int t0 = gw * TOK; t0 < T; t0 += nw * TOK) {
+    float acc[TOK][EP];
+#pragma unroll
+    for (int u = 0; u < TOK; ++u)
+#pragma unroll
+      for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
+
+    for (int i0 = lane * 8; i0 < h; i0 += 256) {
+      uint4 xq[TOK];
+#pragma unroll
+      for (int u = 0; u < TOK; ++u)
+        xq[u] = (t0 + u < T)
+                    ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + u) * h + i0))
+                    : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float xv[TOK];
+#pragma unroll
+        for (int u = 0; u < TOK; ++u) {
+          const uint32_t w = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
+          xv[u] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
+        }
+        const float* wrow = Wg + static_cast<size_t>(i0 + j) * E;
+        if (VEC) {
+#pragma unroll
+          for (int e4 = 0; e4 < EP / 4; ++e4) {
+            if (e4 * 4 < E) {
+              const float4 wv = __ldg(reinterpret_cast<const float4*>(wrow) + e4);
+#pragma unroll
+              for (int u = 0; u < TOK; ++u) {
+                acc[u][4 * e4 + 0] = fmaf(xv[u], wv.x, acc[u][4 * e4 + 0]);
+                acc[u][4 * e4 + 1] = fmaf(xv[u], wv.y, acc[u][4 * e4 + 1]);
+                acc[u][4 * e4 + 2] = fmaf(xv[u], wv.z, acc[u][4 * e4 + 2]);
+                acc[u][4 * e4 + 3] = fmaf(xv[u], wv.w, acc[u][4 * e4 + 3]);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < EP; ++e) {
+            if (e < E) {
+              const float wv = __ldg(wrow + e);
+#pragma unroll
+              for (int u = 0; u < TOK; ++u) acc[u][e] = fmaf(xv[u], wv, acc[u][e]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < TOK; ++u)
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[u][e] += __shfl_xor_sync(kFull, acc[u][e], off);
+
+#pragma unroll
+    for (int u = 0; u < TOK; ++u) {
+      const int t = t0 + u;
+      if (lane != u || t >= T) continue;
+      float l[EP];
+#pragma unroll
+      for (int e = 0; e < EP; ++e) l[e] = (e < E) ? acc[u][e] + (b ? __ldg(b + e) : 0.f) : 0.f;
+      uint64_t taken = 0;
+      float sel_l[8];
+      int sel_e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        int best = -1;
+        float bv = 0.f;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+          if (e < E && !((taken >> e) & 1ull) && (best < 0 || l[e] > bv)) {
+            best = e;
+            bv = l[e];
+          }
+        }
+        if (best < 0) {  // only when logits are NaN: keep the index in range
+          best = 0;
+          while (best < E - 1 && ((taken >> best) & 1ull)) ++best;
+          bv = l[0];
+        }
+        taken |= 1ull << best;
+        sel_e[j] = best;
+        sel_l[j] = bv;
+      }
+      // renormalised gates: exp(l_j - l_top) / sum over the selected
+      float sj[8];
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        sj[j] = expf(sel_l[j] - sel_l[0]);
+        sum += sj[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        topk_idx[static_cast<size_t>(t) * k + j] = sel_e[j];
+        gates[static_cast<size_t>(t) * k + j] = sj[j] / sum;
+      }
+    }
+  }
+}
+
+template <int EP, int TOK>
+cudaError_t router_launch(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
+                          int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
+  const long long warps = (T + TOK - 1) / TOK;
+  const int grid = grid_for(warps, num_sms, 8, 8);
+  if (E % 4 == 0)
+    router_kernel<EP, TOK, true><<<grid, 256, 0, s>>>(x, Wg, b, T, h, E, k, idx, gates);
+  else
+    router_kernel<EP, TOK, false><<<grid, 256, 0, s>>>(x, Wg, b, T, h, E, k, idx, gates);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- dispatch
+// A block takes kDispatchChunk consecutive assignments in four rounds of 256.
+// Within a round a warp groups equal experts with __match_any_sync; the
+// group's lowest lane records the group size.  The stable rank of an
+// assignment inside its block is then
+//   running[e] (earlier rounds) + sizes of earlier warps (this round)
+//   + lanes below it in its own group.
+constexpr int kDispThreads = 256;
+constexpr int kDispWarps = kDispThreads / 32;
+constexpr int kDispMaxE = 256;
+
+template <bool WRITE>
+__global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
+    const int32_t* __restrict__ topk_idx, long long n, int E, int32_t* __restrict__ blk_counts,
+    const int32_t* __restrict__ bases, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ perm_dst) {
+  __shared__ int running[kDispMaxE];
+  __shared__ int wc[kDispWarps][kDispMaxE];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const long long base = static_cast<long long>(blockIdx.x) * kDispatchChunk;
+  for (int e = tid; e < E; e += kDispThreads) running[e] = 0;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r = 0; r < kDispatchChunk / kDispThreads; ++r) {
+    for (int i = tid; i < kDispWarps * E; i += kDispThreads) wc[i / E][i % E] = 0;
+    __syncthreads();
+    const long long a = base + r * kDispThreads + tid;
+    const bool valid = a < n;
+    int e = -1;
+    if (valid) {
+      e = __ldg(topk_idx + a);
+      e = e < 0 ? 0 : (e >= E ? E - 1 : e);  // keep every index in range
+    }
+    const unsigned grp = __match_any_sync(kFull, e);
+    const int lrank = __popc(grp & lt_mask);
+    if (valid && lrank == 0) wc[warp][e] = __popc(grp);
+    __syncthreads();
+    if (valid && WRITE) {
+      int rank = running[e] + lrank;
+      for (int w = 0; w < warp; ++w) rank += wc[w][e];
+      const int dst = __ldg(bases + static_cast<size_t>(blockIdx.x) * E + e) + rank;
+      perm_dst[a] = dst;
+      perm_src[dst] = static_cast<int32_t>(a);
+    }
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += kDispThreads) {
+      int add = 0;
+      for (int w = 0; w < kDispWarps; ++w) add += wc[w][ee];
+      running[ee] += add;
+    }
+  }
+  if (!WRITE) {
+    __syncthreads();
+    for (int e = tid; e < E; e += kDispThreads)
+      blk_counts[static_cast<size_t>(blockIdx.x) * E + e] = running[e];
+  }
+}
+
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t* __restrict__ blk_counts,
+                                                            int nblk, int E,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ bases) {
+  __shared__ int tot[kDispMaxE + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int bk = 0; bk < nblk; ++bk) s += blk_counts[static_cast<size_t>(bk) * E + e];
+    tot[e] = s;
+    counts[e] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = tot[e];
+      tot[e] = run;
+      offsets[e] = run;
+      run += c;
+    }
+    offsets[E] = run;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = tot[e];
+    for (int bk = 0; bk < nblk; ++bk) {
+      bases[static_cast<size_t>(bk) * E + e] = run;
+      run += blk_counts[static_cast<size_t>(bk) * E + e];
+    }
+  }
+}
+
+// --------------------------------------------------------------- row moves
+// Warp per row, 16-byte pieces.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ in,
+                                                          const int32_t* __restrict__ idx, int div,
+                                                          long long rows, long long src_rows,
+                                                          int h8, uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long p = gw; p < rows; p += nw) {
+    long long src = __ldg(idx + p) / div;
+    src = src < 0 ? 0 : (src >= src_rows ? src_rows - 1 : src);  // stay inside `in`
+    const uint4* s = in + src * h8;
+    uint4* d = out + p * h8;
+#pragma unroll 4
+    for (int c = lane; c < h8; c += 32) d[c] = __ldg(s + c);
+  }
+}
+
+// y[t] = sum_j g[t,j] * O[perm_dst[t*k+j]], fp32 in slot order.
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ O,
+                                                      const float* __restrict__ gates,
+                                                      const int32_t* __restrict__ perm_dst, int T,
+                                                      int k, int h8, uint4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int t = gw; t < T; t += nw) {
+    long long rows[8];
+    float g[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const long long r = __ldg(perm_dst + static_cast<size_t>(t) * k + j);
+        rows[j] = r < 0 ? 0 : (r >= static_cast<long long>(T) * k ? static_cast<long long>(T) * k - 1 : r);
+        g[j] = __ldg(gates + static_cast<size_t>(t) * k + j);
+      }
+    }
+    for (int c = lane; c < h8; c += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        float v[8];
+        unpack8(__ldg(O + rows[j] * h8 + c), v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g[j], v[i], acc[i]);
+      }
+      y[static_cast<size_t>(t) * h8 + c] = pack8(acc);
+    }
+  }
+}
+
+// dO[p] = bf16(g[a] * dy[t]); dg[a] = <dy[t], O[p]>.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ dy,
+                                                       const uint4* __restrict__ O,
+                                                       const float* __restrict__ gates,
+                                                       const int32_t* __restrict__ perm_src,
+                                                       long long rows, int k, int h8,
+                                                       uint4* __restrict__ dO,
+                                                       float* __restrict__ dg) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long p = gw; p < rows; p += nw) {
+    int a = __ldg(perm_src + p);
+    a = a < 0 ? 0 : (a >= rows ? static_cast<int>(rows - 1) : a);
+    const long long t = a / k;
+    const float g = __ldg(gates + a);
+    float dot = 0.f;
+    for (int c = lane; c < h8; c += 32) {
+      float d[8], o[8];
+      unpack8(__ldg(dy + t * h8 + c), d);
+      unpack8(__ldg(O + p * h8 + c), o);
+      float s[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dot = fmaf(d[i], o[i], dot);
+        s[i] = g * d[i];
+      }
+      dO[p * h8 + c] = pack8(s);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+    if (lane == 0) dg[a] = dot;
+  }
+}
+
+__global__ void transpose_wg_kernel(const float* __restrict__ Wg, int h, int E,
+                                    float* __restrict__ WgT) {
+  const long long n = static_cast<long long>(h) * E;
+  for (long long q = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; q < n;
+       q += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long e = q / h;
+    const long long i = q - e * h;
+    WgT[q] = Wg[i * E + e];
+  }
+}
+
+// Router backward per token + dx.  dl_j = g_j (dg_j - sum_i g_i dg_i).
+__global__ void __launch_bounds__(256) token_grad_kernel(
+    const float4* __restrict__ dX, const int32_t* __restrict__ perm_dst,
+    const int32_t* __restrict__ topk_idx, const float* __restrict__ gates,
+    const float* __restrict__ dg, const float4* __restrict__ WgT, int T, int k, int h8, int E,
+    float* __restrict__ dl, uint4* __restrict__ dx) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int t = gw; t < T; t += nw) {
+    long long rows[8];
+    int ex[8];
+    float g[8], d[8];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const size_t a = static_cast<size_t>(t) * k + j;
+        const long long r = __ldg(perm_dst + a);
+        rows[j] = r < 0 ? 0 : (r >= static_cast<long long>(T) * k ? static_cast<long long>(T) * k - 1 : r);
+        const int e = __ldg(topk_idx + a);
+        ex[j] = e < 0 ? 0 : (e >= E ? E - 1 : e);
+        g[j] = __ldg(gates + a);
+        d[j] = __ldg(dg + a);
+        s = fmaf(g[j], d[j], s);
+      }
+    }
+    float dlj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < k) dlj[j] = g[j] * (d[j] - s);
+    for (int e = lane; e < E; e += 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k && ex[j] == e) v = dlj[j];
+      dl[static_cast<size_t>(t) * E + e] = v;
+    }
+    for (int c = lane; c < h8; c += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        const float4 u0 = __ldg(dX + (rows[j] * h8 + c) * 2);
+        const float4 u1 = __ldg(dX + (rows[j] * h8 + c) * 2 + 1);
+        acc[0] += u0.x; acc[1] += u0.y; acc[2] += u0.z; acc[3] += u0.w;
+        acc[4] += u1.x; acc[5] += u1.y; acc[6] += u1.z; acc[7] += u1.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        const size_t wo = (static_cast<size_t>(ex[j]) * h8 + c) * 2;
+        const float4 w0 = __ldg(WgT + wo);
+        const float4 w1 = __ldg(WgT + wo + 1);
+        acc[0] = fmaf(dlj[j], w0.x, acc[0]); acc[1] = fmaf(dlj[j], w0.y, acc[1]);
+        acc[2] = fmaf(dlj[j], w0.z, acc[2]); acc[3] = fmaf(dlj[j], w0.w, acc[3]);
+        acc[4] = fmaf(dlj[j], w1.x, acc[4]); acc[5] = fmaf(dlj[j], w1.y, acc[5]);
+        acc[6] = fmaf(dlj[j], w1.z, acc[6]); acc[7] = fmaf(dlj[j], w1.w, acc[7]);
+      }
+      dx[static_cast<size_t>(t) * h8 + c] = pack8(acc);
+    }
+  }
+}
+
+// dWg partials: block (i-tile of 256, token chunk of kWgChunk); thread owns one i
+// and EP experts; dl rows of the chunk are staged in shared memory.
+constexpr int kWgChunk = 256;
+constexpr int kWgStage = 32;
+
+template <int EP>
+__global__ void __launch_bounds__(256) router_wgrad_kernel(const uint16_t* __restrict__ x,
+                                                           const float* __restrict__ dl, int T,
+                                                           int h, int E,
+                                                           float* __restrict__ partial) {
+  __shared__ float sdl[kWgStage][EP];
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  const int chunk = blockIdx.y;
+  const int t0 = chunk * kWgChunk;
+  const int t1 = min(T, t0 + kWgChunk);
+  float acc[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+  for (int ts = t0; ts < t1; ts += kWgStage) {
+    __syncthreads();
+    for (int q = threadIdx.x; q < kWgStage * EP; q += 256) {
+      const int tt = ts + q / EP;
+      const int e = q % EP;
+      sdl[q / EP][e] = (tt < t1 && e < E) ? dl[static_cast<size_t>(tt) * E + e] : 0.f;
+    }
+    __syncthreads();
+    if (i < h) {
+      const int n = min(kWgStage, t1 - ts);
+      for (int u = 0; u < n; ++u) {
+        const float xv = __uint_as_float(static_cast<uint32_t>(x[static_cast<size_t>(ts + u) * h + i])
+                                         << 16);
+#pragma unroll
+        for (int e = 0; e < EP; ++e) acc[e] = fmaf(xv, sdl[u][e], acc[e]);
+      }
+    }
+  }
+  if (i < h) {
+    float* dst = partial + (static_cast<size_t>(chunk) * h + i) * E;
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e < E) dst[e] = acc[e];
+  }
+}
+
+__global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, int nchunks, int h,
+                                           int E, float* __restrict__ dWg) {
+  const long long n = static_cast<long long>(h) * E;
+  for (long long q = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; q < n;
+       q += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int c = 0; c < nchunks; ++c) s += partial[static_cast<size_t>(c) * n + q];
+    dWg[q] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
+                          int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (E <= 8) return router_launch<8, 8>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+  if (E <= 16) return router_launch<16, 4>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+  if (E <= 32) return router_launch<32, 2>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+  return router_launch<64, 1>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+}
+
+cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E, int32_t* blk_counts,
+                                 cudaStream_t s) {
+  const int nblk = dispatch_blocks(n);
+  if (nblk == 0) return cudaSuccess;
+  dispatch_kernel<false><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, blk_counts, nullptr,
+                                                        nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* counts,
+                                 int32_t* offsets, int32_t* bases, cudaStream_t s) {
+  dispatch_scan_kernel<<<1, 256, 0, s>>>(blk_counts, nblk, E, counts, offsets, bases);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
+                                    const int32_t* bases, int32_t* perm_src, int32_t* perm_dst,
+                                    cudaStream_t s) {
+  const int nblk = dispatch_blocks(n);
+  if (nblk == 0) return cudaSuccess;
+  dispatch_kernel<true><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, nullptr, bases, perm_src,
+                                                       perm_dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
+                               long long src_rows, int h, uint16_t* out, int num_sms,
+                               cudaStream_t s) {
+  if (rows == 0 || src_rows == 0) return cudaSuccess;
+  const int grid = grid_for(rows, num_sms, 8, 16);
+  gather_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(in), idx, div, rows,
+                                          src_rows, h / 8, reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t* perm_dst, int T,
+                           int k, int h, uint16_t* y, int num_sms, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = grid_for(T, num_sms, 8, 16);
+  combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(O), gates, perm_dst, T, k,
+                                      h / 8, reinterpret_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const uint16_t* dy, const uint16_t* O, const float* gates,
+                            const int32_t* perm_src, long long rows, int k, int h, uint16_t* dO,
+                            float* dg, int num_sms, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int grid = grid_for(rows, num_sms, 8, 16);
+  bwd_prep_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(dy),
+                                       reinterpret_cast<const uint4*>(O), gates, perm_src, rows, k,
+                                       h / 8, reinterpret_cast<uint4*>(dO), dg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_wg(const float* Wg, int h, int E, float* WgT, cudaStream_t s) {
+  const long long n = static_cast<long long>(h) * E;
+  int grid = static_cast<int>((n + 255) / 256);
+  if (grid > 1024) grid = 1024;
+  transpose_wg_kernel<<<grid, 256, 0, s>>>(Wg, h, E, WgT);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
+                              const int32_t* topk_idx, const float* gates, const float* dg,
+                              const float* WgT, int T, int k, int h, int E, float* dl,
+                              uint16_t* dx, int num_sms, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = grid_for(T, num_sms, 8, 16);
+  token_grad_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(dX_perm), perm_dst,
+                                         topk_idx, gates, dg,
+                                         reinterpret_cast<const float4*>(WgT), T, k, h / 8, E, dl,
+                                         reinterpret_cast<uint4*>(dx));
+  return cudaGetLastError();
+}
+
+int wgrad_router_chunks(int T) { return (T + kWgChunk - 1) / kWgChunk; }
+
+cudaError_t launch_router_wgrad(const uint16_t* x, const float* dl, int T, int h, int E,
+                                float* partial, float* dWg, cudaStream_t s) {
+  const int nchunks = wgrad_router_chunks(T);
+  if (nchunks > 0) {
+    dim3 grid((h + 255) / 256, nchunks);
+    if (E <= 8)
+      router_wgrad_kernel<8><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+    else if (E <= 16)
+      router_wgrad_kernel<16><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+    else if (E <= 32)
+      router_wgrad_kernel<32><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+    else
+      router_wgrad_kernel<64><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const long long n = static_cast<long long>(h) * E;
+  int grid2 = static_cast<int>((n + 255) / 256);
+  if (grid2 > 2048) grid2 = 2048;
+  router_wgrad_reduce_kernel<<<grid2, 256, 0, s>>>(partial, nchunks, h, E, dWg);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

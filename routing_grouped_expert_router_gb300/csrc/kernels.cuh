@@ -1,0 +1,61 @@
+// kernels.cuh -- launchers of the memory-bound and FP32 kernels of the layer:
+// router, dispatch (histogram, scan, stable scatter), row moves, combine and
+// the router/token backward.  All are deterministic and use no atomics.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kDispatchChunk = 1024;  // assignments per dispatch block
+constexpr int kRouterMaxE = 64;
+
+inline int dispatch_blocks(long long assignments) {
+  return static_cast<int>((assignments + kDispatchChunk - 1) / kDispatchChunk);
+}
+
+// Router + softmax + top-k + renormalisation (warp per token group).
+cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
+                          int k, int32_t* topk_idx, float* gates, int num_sms, cudaStream_t s);
+
+// Per-block expert counts [nblk, E] of the assignments.
+cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E, int32_t* blk_counts,
+                                 cudaStream_t s);
+// counts [E], offsets [E+1] and block bases [nblk, E].
+cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* counts,
+                                 int32_t* offsets, int32_t* bases, cudaStream_t s);
+// perm_dst[a], perm_src[p] from block bases and in-block stable ranks.
+cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
+                                    const int32_t* bases, int32_t* perm_src, int32_t* perm_dst,
+                                    cudaStream_t s);
+
+// out[p] = in[idx[p] / div] for p < rows (bf16 rows of h elements); `in` has
+// src_rows rows and source indices are clamped into it.
+cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
+                               long long src_rows, int h, uint16_t* out, int num_sms,
+                               cudaStream_t s);
+
+// y[t] = sum_j g[t,j] O[perm_dst[t*k+j]].
+cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t* perm_dst, int T,
+                           int k, int h, uint16_t* y, int num_sms, cudaStream_t s);
+
+// dO[p] = bf16(g[a] dy[t]), dg[a] = <dy[t], O[p]> with a = perm_src[p], t = a / k.
+cudaError_t launch_bwd_prep(const uint16_t* dy, const uint16_t* O, const float* gates,
+                            const int32_t* perm_src, long long rows, int k, int h, uint16_t* dO,
+                            float* dg, int num_sms, cudaStream_t s);
+
+// WgT[e][i] = Wg[i][e].
+cudaError_t launch_transpose_wg(const float* Wg, int h, int E, float* WgT, cudaStream_t s);
+
+// dl (dense [T, E]) and dx[t] = sum_j dX_perm[perm_dst[t*k+j]] + sum_j dl_j WgT[e_j].
+cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
+                              const int32_t* topk_idx, const float* gates, const float* dg,
+                              const float* WgT, int T, int k, int h, int E, float* dl,
+                              uint16_t* dx, int num_sms, cudaStream_t s);
+
+// dWg = x^T dl via fixed-order partial sums over token chunks.
+int wgrad_router_chunks(int T);
+cudaError_t launch_router_wgrad(const uint16_t* x, const float* dl, int T, int h, int E,
+                                float* partial, float* dWg, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads, exports
+every declared entry point, and rejects bad arguments before any launch."""
+import ctypes
+
+import pytest
+
+from routing_grouped_expert_router_gb300 import binding as mb
+from routing_grouped_expert_router_gb300 import build as mbuild
+from routing_grouped_expert_router_gb300.configs import CONFIGS
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return mb.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = mb.declared_symbols()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(mb._SIGS), set(names) ^ set(mb._SIGS)
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in mb.moe_version()
+    for code in range(6):
+        s = mb.status_string(code)
+        assert s.startswith("MOE_")
+    assert mb.status_string(99) == "unknown moe_status"
+
+
+FAKE = 1 << 20          # aligned, non-null address; never dereferenced
+MISALIGNED = FAKE + 8
+
+
+def _d(**kw):
+    base = dict(T=64, h=128, f=256, E=8, k=2, has_bias=0)
+    base.update(kw)
+    return mb.moe_dims(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=0), mb.MOE_ERR_INVALID_ARG),
+    (dict(k=9, E=16), mb.MOE_ERR_UNSUPPORTED),
+    (dict(k=5, E=4), mb.MOE_ERR_INVALID_ARG),
+    (dict(E=65), mb.MOE_ERR_UNSUPPORTED),
+    (dict(h=100), mb.MOE_ERR_UNSUPPORTED),
+    (dict(f=72), mb.MOE_ERR_UNSUPPORTED),
+    (dict(T=-1), mb.MOE_ERR_INVALID_ARG),
+    (dict(T=1 << 29, k=8), mb.MOE_ERR_UNSUPPORTED),
+])
+def test_bad_dims_rejected(lib, kw, code):
+    d = _d(**kw)
+    st = lib.moe_route(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert st == code
+    assert lib.moe_workspace_bytes(ctypes.byref(d), mb.OP_LAYER_FWD) == 0
+    assert lib.moe_saved_bytes(ctypes.byref(d)) == 0
+
+
+def test_null_dims(lib):
+    assert lib.moe_route(None, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None) \
+        == mb.MOE_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers(lib):
+    d = _d()
+    big = 1 << 40
+    assert lib.moe_route(ctypes.byref(d), None, FAKE, None, FAKE, FAKE, FAKE, big, None) \
+        == mb.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(ctypes.byref(d), MISALIGNED, FAKE, None, FAKE, FAKE, FAKE, big, None) \
+        == mb.MOE_ERR_INVALID_ARG
+    d.has_bias = 1
+    assert lib.moe_route(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE, big, None) \
+        == mb.MOE_ERR_INVALID_ARG
+    d.has_bias = 0
+    # workspace must be 256-byte aligned
+    assert lib.moe_route(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE + 16, big, None) \
+        == mb.MOE_ERR_INVALID_ARG
+    args = [FAKE] * 12
+    args[3] = None
+    assert lib.moe_layer_bwd(ctypes.byref(d), *args, FAKE, big, None) == mb.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(ctypes.byref(d), FAKE, FAKE, None, FAKE, None) == mb.MOE_ERR_INVALID_ARG
+    assert lib.moe_unpermute(ctypes.byref(d), FAKE, MISALIGNED, FAKE, None) \
+        == mb.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("op", range(7))
+def test_workspace_too_small(lib, op):
+    d = _d()
+    need = lib.moe_workspace_bytes(ctypes.byref(d), op)
+    assert need >= 256
+    P = FAKE
+    calls = {
+        mb.OP_ROUTE: lambda n: lib.moe_route(ctypes.byref(d), P, P, None, P, P, P, n, None),
+        mb.OP_PERMUTE: lambda n: lib.moe_permute(ctypes.byref(d), P, None, P, P, P, P, None, P,
+                                                 n, None),
+        mb.OP_EXPERT_FFN_FWD: lambda n: lib.moe_expert_ffn_fwd(ctypes.byref(d), *([P] * 10), P,
+                                                               n, None),
+        mb.OP_EXPERT_FFN_BWD: lambda n: lib.moe_expert_ffn_bwd(ctypes.byref(d), *([P] * 17), P,
+                                                               n, None),
+        mb.OP_ROUTER_BWD: lambda n: lib.moe_router_bwd(ctypes.byref(d), *([P] * 11), P, n, None),
+        mb.OP_LAYER_FWD: lambda n: lib.moe_layer_fwd(ctypes.byref(d), P, P, None, P, P, P, P, P,
+                                                     P, n, None),
+        mb.OP_LAYER_BWD: lambda n: lib.moe_layer_bwd(ctypes.byref(d), *([P] * 12), P, n, None),
+    }
+    assert calls[op](need - 1) == mb.MOE_ERR_WORKSPACE
+
+
+def test_sizes_cover_tensors(lib):
+    for cfg in CONFIGS.values():
+        d = mb.dims_of(cfg)
+        R = cfg.T * cfg.k
+        saved = lib.moe_saved_bytes(ctypes.byref(d))
+        acts = R * (cfg.h * 2 * 2 + cfg.f * 2 * 3) + R * 16
+        assert saved >= acts
+        bw = lib.moe_workspace_bytes(ctypes.byref(d), mb.OP_LAYER_BWD)
+        assert bw >= R * (cfg.h * 2 + cfg.f * 4 + cfg.h * 4)
+        # views are inside the buffer, in declaration order, 256-byte aligned
+        offs = [mb.moe_saved_view(d, FAKE, n) - FAKE for n in
+                ("topk_idx", "gates", "counts", "offsets", "perm_src", "perm_dst", "x_perm",
+                 "A", "B", "H", "O")]
+        assert offs == sorted(offs) and offs[0] == 0 and offs[-1] < saved
+        assert all(o % 256 == 0 for o in offs)
+    with pytest.raises(mb.MoeError):
+        mb.moe_saved_view(_d(), FAKE, "nope")
+
+
+def test_profile_hook_without_events(lib):
+    assert mb.moe_profile_events(None, 0) == 0
+    assert mb.moe_profile_kernel_name(-1) == ""
