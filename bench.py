@@ -274,7 +274,10 @@ def oracle_sample(cfg, ntok, seed_offset=0):
     """Inputs of a bounded sample: the first `ntok` tokens of the workload
     (all experts' weights), on the host."""
     sub = mcfg.LayerConfig(**{**cfg.as_dict(), "T": ntok})
-    return synth.make_layer(sub, "cpu")
+    # the generator is the same on either device; the GPU makes the GBs of
+    # weights in seconds, the host would take minutes
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    return {k: v.cpu() for k, v in synth.make_layer(sub, dev).items()}
 
 
 def time_oracle(cfg, ntok, steps, warmup):

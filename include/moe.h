@@ -162,7 +162,8 @@ moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x,
                               void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Router backward and the token gradient:
- *   dl[t,j] = g_j (dg_j - sum_i g_i dg_i)     (softmax over the k selected)
+ *   dl[t,j] = g_j (dg_j - sum_i g_i dg_i)     (softmax over the k selected),
+ *             evaluated as g_j sum_i g_i (dg_j - dg_i) since sum_i g_i = 1
  *   dx[t]   = sum_j dX_perm[perm_dst[t*k+j]] + sum_j dl[t,j] Wg[:, e_j]  (bf16)
  *   dWg     = x^T dl (fp32 [h,E]; a fixed-order two-level reduction)
  * In: x, Wg, topk_idx, gates, dg [T*k], dX_perm [T*k,h] fp32, perm_src,

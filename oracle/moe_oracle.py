@@ -291,11 +291,15 @@ def router_bwd(gates, dg):
 
     The renormalised gates equal a softmax over the k selected logits (the
     full-softmax denominator cancels), whose Jacobian is g_j (delta_ij - g_i).
-    Unselected logits get zero (selection is piecewise constant).
+    With sum_i g_i = 1 the product is evaluated as g_j sum_i g_i (dg_j - dg_i),
+    the same value without the cancellation of dg_j - sum_i g_i dg_i when one
+    gate is close to 1.  Unselected logits get zero (selection is piecewise
+    constant).
     """
     g = np.asarray(gates, dtype=np.float64)
-    s = (g * dg).sum(axis=1, keepdims=True)
-    return g * (dg - s)
+    d = np.asarray(dg, dtype=np.float64)
+    diff = d[:, :, None] - d[:, None, :]          # [T, j, i] = dg_j - dg_i
+    return g * np.einsum("ti,tji->tj", g, diff)
 
 
 def layer_bwd(dy, x, Wg, W1, W3, W2, ctx, counter=None):

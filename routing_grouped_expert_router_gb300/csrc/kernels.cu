@@ -364,7 +364,7 @@ __global__ void transpose_wg_kernel(const float* __restrict__ Wg, int h, int E,
   }
 }
 
-// Router backward per token + dx.  dl_j = g_j (dg_j - sum_i g_i dg_i).
+// Router backward per token + dx.
 __global__ void __launch_bounds__(256) token_grad_kernel(
     const float4* __restrict__ dX, const int32_t* __restrict__ perm_dst,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ gates,
@@ -377,7 +377,6 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
     long long rows[8];
     int ex[8];
     float g[8], d[8];
-    float s = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j < k) {
@@ -388,13 +387,21 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
         ex[j] = e < 0 ? 0 : (e >= E ? E - 1 : e);
         g[j] = __ldg(gates + a);
         d[j] = __ldg(dg + a);
-        s = fmaf(g[j], d[j], s);
       }
     }
+    // dl_j = g_j (dg_j - sum_i g_i dg_i), evaluated as g_j sum_i g_i (dg_j - dg_i)
+    // (sum_i g_i = 1): no cancellation when one gate is close to 1, and
+    // exactly 0 for k = 1.
     float dlj[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < k) dlj[j] = g[j] * (d[j] - s);
+    for (int j = 0; j < 8; ++j) {
+      if (j >= k) break;
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i < k && i != j) acc = fmaf(g[i], d[j] - d[i], acc);
+      dlj[j] = g[j] * acc;
+    }
     for (int e = lane; e < E; e += 32) {
       float v = 0.f;
 #pragma unroll
