@@ -57,6 +57,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest `value` over all ranks (one float all-reduce; 1 rank: itself)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, n_ranks: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return metrics.tokens_per_s(tokens_per_rank * n_ranks * steps, ms)
+
+
 def workload_desc(cfg):
     return (f"{cfg.name}: T={cfg.T} h={cfg.h} h_ffn={cfg.f} E={cfg.E} top-{cfg.k}"
             + (f" zipf{cfg.zipf_s}" if cfg.zipf_s else ""))
@@ -207,11 +222,7 @@ def run_ours(args, cfg, world, rank, local):
     clocks = sampler.stop()
     if world > 1:
         dist.barrier()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), device)
     st = max(mb.moe_read_device_status(layer.ws_f), mb.moe_read_device_status(layer.ws_b))
     if st != mb.MOE_OK:
         raise RuntimeError(f"device status after timing: {mb.status_string(st)}")
@@ -256,11 +267,7 @@ def run_ours(args, cfg, world, rank, local):
             e2e_step()
         e2.record(stream)
         torch.cuda.synchronize(device)
-        ms2 = s2.elapsed_time(e2)
-        if world > 1:
-            t = torch.tensor([ms2], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms2 = float(t.item())
+        ms2 = max_over_ranks(s2.elapsed_time(e2), device)
         nb = x_h.numel() * x_h.element_size()
         result["e2e"] = {"ms": ms2, "h2d": 2 * nb, "d2h": 2 * nb}
     if world > 1:
@@ -343,7 +350,7 @@ def main():
         return
     K = args.steps
     ms_step = r["ms"] / K
-    tokens_per_s = metrics.tokens_per_s(cfg.T * n * K, r["ms"])
+    tokens_per_s = job_tokens_per_s(cfg.T, n, K, r["ms"])
     work = metrics.kernel_work(cfg.T, cfg.h, cfg.f, cfg.E, cfg.k)
     kern = {}
     for name, ts in r["per_kernel"].items():
@@ -382,7 +389,7 @@ def main():
     }
     if "e2e" in r:
         e = r["e2e"]
-        line["e2e"] = {"value": metrics.tokens_per_s(cfg.T * n * K, e["ms"]), "unit": "tokens/s",
+        line["e2e"] = {"value": job_tokens_per_s(cfg.T, n, K, e["ms"]), "unit": "tokens/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "note": "x, dy copied from pinned host memory each step; y, dx read back;"
                                " weights and weight gradients stay resident"}
