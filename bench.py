@@ -47,6 +47,10 @@ def parse():
     p.add_argument("--cpu-sample-tokens", type=int, default=16)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    # size overrides for small profiling captures (the bench line itself uses
+    # the named workload unchanged)
+    p.add_argument("--tokens", type=int, default=0, help="override T")
+    p.add_argument("--experts", type=int, default=0, help="override E (k = min(k, E))")
     return p.parse_args()
 
 
@@ -320,6 +324,10 @@ def main():
     args = parse()
     world, rank, local = dist_env()
     cfg = mcfg.get(args.config)
+    if args.tokens or args.experts:
+        E = args.experts or cfg.E
+        cfg = mcfg.LayerConfig(**{**cfg.as_dict(), "T": args.tokens or cfg.T, "E": E,
+                                  "k": min(cfg.k, E), "name": cfg.name + "-resized"})
     peaks, peak_src = load_peaks()
     workload = workload_desc(cfg)
     n = max(args.gpus, world)

@@ -276,7 +276,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    constexpr uint32_t IDESC = idesc_bf16(BM, BNB, A_MN, B_MN);
+    // MN-major B tiles are stored as 64-column chunks 8 KiB apart, so the two
+    // 128-column operands of NUM_B = 2 form one 256-column operand: a single
+    // N = 256 MMA fills both accumulators and reads the A tile once per K step.
+    constexpr bool B_FUSED = B_MN || NUM_B == 1;
+    constexpr uint32_t IDESC = idesc_bf16(BM, B_FUSED ? BN : BNB, A_MN, B_MN);
     constexpr uint32_t A_LBO = A_MN ? CHUNK_BYTES : 16;
     constexpr uint32_t B_LBO = B_MN ? CHUNK_BYTES : 16;
     constexpr uint32_t A_KSTEP = A_MN ? 2048 : 32;  // bytes per 16-deep K step
@@ -328,10 +332,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc(a_base + kk * A_KSTEP, A_LBO, 1024);
+            if (B_FUSED) {
+              umma_bf16(acc, ad, smem_desc(b_base + kk * B_KSTEP, B_LBO, 1024), IDESC,
+                        (kb | kk) != 0);
+            } else {
 #pragma unroll
-            for (int i = 0; i < NUM_B; ++i) {
-              const uint64_t bd = smem_desc(b_base + i * (B_BYTES / NUM_B) + kk * B_KSTEP, B_LBO, 1024);
-              umma_bf16(acc + i * BNB, ad, bd, IDESC, (kb | kk) != 0);
+              for (int i = 0; i < NUM_B; ++i) {
+                const uint64_t bd =
+                    smem_desc(b_base + i * (B_BYTES / NUM_B) + kk * B_KSTEP, B_LBO, 1024);
+                umma_bf16(acc + i * BNB, ad, bd, IDESC, (kb | kk) != 0);
+              }
             }
           }
           umma_commit(smem_u32(&c.empty[s]));
