@@ -116,6 +116,22 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx,
                        int32_t* perm_src, int32_t* perm_dst, moe_bf16* x_perm,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_permute with no workspace argument (the pages have no counterpart; this
+ * is an interface convenience).  For callers that cannot allocate device
+ * memory when they dispatch: code running while a stream is captured into a
+ * CUDA graph, or a runtime that owns a fixed memory budget.  Same arguments
+ * and outputs as moe_permute minus ws/ws_bytes.  Its scratch is a 1 MiB array
+ * in the library's device memory (held by every GPU that loads the library
+ * until exit), so it supports ceil(T*k / 1024) * E <= 131072 and returns
+ * MOE_ERR_UNSUPPORTED beyond that.  The first call on a device looks up the
+ * array's device address; make it before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU race.  Allocates nothing. */
+moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* topk_idx,
+                               const moe_bf16* x, int32_t* counts,
+                               int32_t* offsets, int32_t* perm_src,
+                               int32_t* perm_dst, moe_bf16* x_perm,
+                               moe_stream_t stream);
+
 /* Inverse row move: rows_assign[a] = rows_perm[perm_dst[a]] for a < T*k.
  * rows_perm, rows_assign: [T*k, h] bf16. */
 moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst,

@@ -58,6 +58,7 @@ _SIGS = {
     "moe_saved_bytes": (_SZ, [_D]),
     "moe_route": (_I, [_D, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_noalloc": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_unpermute": (_I, [_D, _P, _P, _P, _P]),
     "moe_expert_ffn_fwd": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_D, _P, _P, _P, _P, _P]),
@@ -159,6 +160,13 @@ def moe_permute(d, topk_idx, x, counts, offsets, perm_src, perm_dst, x_perm, ws,
     _check(load().moe_permute(ctypes.byref(d), _addr(topk_idx), _addr(x), _addr(counts),
                               _addr(offsets), _addr(perm_src), _addr(perm_dst), _addr(x_perm),
                               _addr(ws), ws_bytes, _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(d, topk_idx, x, counts, offsets, perm_src, perm_dst, x_perm,
+                        stream=None):
+    _check(load().moe_permute_noalloc(ctypes.byref(d), _addr(topk_idx), _addr(x), _addr(counts),
+                                      _addr(offsets), _addr(perm_src), _addr(perm_dst),
+                                      _addr(x_perm), _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_unpermute(d, perm_dst, rows_perm, rows_assign, stream=None):
