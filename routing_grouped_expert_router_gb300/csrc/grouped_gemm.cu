@@ -93,7 +93,23 @@ struct Tile {
   int nkb;      // K blocks
 };
 
-template <bool GROUP_K, bool INNER_N, int NUM_B>
+// Tile order inside one expert's MT x NT tile grid: groups of GM m-tiles,
+// and within a group n-major, m fastest.  The ~152 tiles in flight at once then
+// cover about GM m-tiles x (152 / GM) n-tiles, so the A row-blocks and B
+// column-slabs they stream stay shared in L2 instead of the whole A operand
+// being streamed again for every column of tiles.
+constexpr int GM = 16;
+
+__device__ __forceinline__ void raster(int local, int MT, int& mb, int& nb, int NT) {
+  const int g = local / (GM * NT);
+  const int base = g * GM;
+  const int gsz = min(GM, MT - base);
+  const int r = local - g * GM * NT;
+  nb = r / gsz;
+  mb = base + r % gsz;
+}
+
+template <bool GROUP_K, int NUM_B>
 __device__ __forceinline__ bool decode(const Params& p, const Ctrl& c, int t, Tile& tl) {
   const int NT = (p.N + (BN / NUM_B) - 1) / (BN / NUM_B);
   if (!GROUP_K) {
@@ -104,8 +120,7 @@ __device__ __forceinline__ bool decode(const Params& p, const Ctrl& c, int t, Ti
     const int local = t - NT * c.cum[e];
     const int mt = c.cum[e + 1] - c.cum[e];
     tl.e = e;
-    tl.nb = local / mt;
-    tl.mb = local % mt;
+    raster(local, mt, tl.mb, tl.nb, NT);
     tl.row0 = c.off[e] + tl.mb * BM;
     tl.row_end = c.off[e + 1];
     tl.nkb = p.kblocks * p.kconcat;
@@ -114,15 +129,8 @@ __device__ __forceinline__ bool decode(const Params& p, const Ctrl& c, int t, Ti
     const int MT = (p.M + BM - 1) / BM;
     const int per = MT * NT;
     const int e = t / per;
-    const int local = t - e * per;
     tl.e = e;
-    if (INNER_N) {
-      tl.mb = local / NT;
-      tl.nb = local % NT;
-    } else {
-      tl.nb = local / MT;
-      tl.mb = local % MT;
-    }
+    raster(t - e * per, MT, tl.mb, tl.nb, NT);
     tl.row0 = c.off[e];
     tl.row_end = c.off[e + 1];
     tl.nkb = (tl.row_end - tl.row0 + BK - 1) / BK;
@@ -165,7 +173,7 @@ __device__ __forceinline__ void store_f32x32(void* dst, const float* v) {
   for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K, bool INNER_N>
+template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gg_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int q = 0;
       bool ok = true;
       Tile tl;
-      for (int t = blockIdx.x; ok && decode<GROUP_K, INNER_N, NUM_B>(p, c, t, tl); t += gridDim.x) {
+      for (int t = blockIdx.x; ok && decode<GROUP_K, NUM_B>(p, c, t, tl); t += gridDim.x) {
         for (int kb = 0; kb < tl.nkb; ++kb, ++q) {
           const int s = q % STAGES;
           const uint32_t ph = (q / STAGES) & 1;
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int q = 0, it = 0;
     bool ok = true;
     Tile tl;
-    for (int t = blockIdx.x; ok && decode<GROUP_K, INNER_N, NUM_B>(p, c, t, tl); t += gridDim.x) {
+    for (int t = blockIdx.x; ok && decode<GROUP_K, NUM_B>(p, c, t, tl); t += gridDim.x) {
       if (tl.nkb == 0) continue;
       const int buf = it & 1;
       const uint32_t u = (it >> 1) & 1;
@@ -364,7 +372,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = quarter * 32 + lane;
     int it = 0;
     Tile tl;
-    for (int t = blockIdx.x; decode<GROUP_K, INNER_N, NUM_B>(p, c, t, tl); t += gridDim.x) {
+    for (int t = blockIdx.x; decode<GROUP_K, NUM_B>(p, c, t, tl); t += gridDim.x) {
       if (*abort_flag) break;
       if (GROUP_K && tl.nkb == 0) {
         // expert without tokens: its weight gradient is zero
@@ -485,9 +493,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K, bool INNER_N>
+template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
 cudaError_t launch(const Params& prm, const Maps& maps, int grid, cudaStream_t s) {
-  auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K, INNER_N>;
+  auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -538,7 +546,7 @@ cudaError_t gemm_fc1_fwd(const GemmProblem& g, const void* x_perm, const void* W
   p.out1 = B;
   p.out2 = H;
   p.ldo = g.f;
-  return launch<false, true, 2, EPI_SWIGLU, false, false>(p, m, mgrouped_grid(g, g.f, BN / 2), s);
+  return launch<false, true, 2, EPI_SWIGLU, false>(p, m, mgrouped_grid(g, g.f, BN / 2), s);
 }
 
 cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, void* O,
@@ -556,7 +564,7 @@ cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, vo
   p.b_rows = g.f;
   p.out0 = O;
   p.ldo = g.h;
-  return launch<false, true, 1, EPI_BF16, false, false>(p, m, mgrouped_grid(g, g.h, BN), s);
+  return launch<false, true, 1, EPI_BF16, false>(p, m, mgrouped_grid(g, g.h, BN), s);
 }
 
 cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2, const void* A,
@@ -578,7 +586,7 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.out0 = dA;
   p.out1 = dB;
   p.ldo = g.f;
-  return launch<false, false, 1, EPI_SWIGLU_BWD, false, false>(p, m, mgrouped_grid(g, g.f, BN), s);
+  return launch<false, false, 1, EPI_SWIGLU_BWD, false>(p, m, mgrouped_grid(g, g.f, BN), s);
 }
 
 cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB, const void* W1,
@@ -597,7 +605,7 @@ cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB,
   p.b_rows = g.h;
   p.out0 = dX;
   p.ldo = g.h;
-  return launch<false, false, 1, EPI_F32, false, false>(p, m, mgrouped_grid(g, g.h, BN), s);
+  return launch<false, false, 1, EPI_F32, false>(p, m, mgrouped_grid(g, g.h, BN), s);
 }
 
 cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, float* dW2,
@@ -615,8 +623,7 @@ cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, 
   const int MT = (g.f + BM - 1) / BM, NT = (g.h + BN - 1) / BN;
   p.ktiles = g.E * MT * NT;
   const int grid = p.ktiles < g.num_sms ? p.ktiles : g.num_sms;
-  // N (= h) innermost: the expert's dO rows stay in L2 while H streams once
-  return launch<true, true, 1, EPI_WGRAD, true, true>(p, m, grid, s);
+  return launch<true, true, 1, EPI_WGRAD, true>(p, m, grid, s);
 }
 
 cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void* dA,
@@ -635,8 +642,7 @@ cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void*
   const int MT = (g.h + BM - 1) / BM, NT = (g.f + BN / 2 - 1) / (BN / 2);
   p.ktiles = g.E * MT * NT;
   const int grid = p.ktiles < g.num_sms ? p.ktiles : g.num_sms;
-  // M (= h) innermost: the expert's X rows stay in L2 while dA, dB stream once
-  return launch<true, true, 2, EPI_WGRAD, true, false>(p, m, grid, s);
+  return launch<true, true, 2, EPI_WGRAD, true>(p, m, grid, s);
 }
 
 }  // namespace moe
