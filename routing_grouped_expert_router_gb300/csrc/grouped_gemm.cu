@@ -21,12 +21,15 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "grouped_gemm.cuh"
 #include "ptx.cuh"
 
 namespace moe {
+
+int g_pair_clusters = 0;  // co-resident CTA pairs of the last pair launch (diagnostics)
 
 const char* const kGemmNames[6] = {"gg_fc1_fwd_swiglu", "gg_fc2_fwd",
                                    "gg_fc2_dgrad_swiglu_bwd", "gg_fc1_dgrad",
@@ -44,7 +47,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KiB
 constexpr int CHUNK_BYTES = 64 * BK * 2;        // one 64 x 64 MN-major box: 8 KiB
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
-constexpr int MAX_E = 256;
+constexpr int MAX_E = 64;   // the C ABI limits E to 64
 constexpr int kTimeoutCode = 5;  // MOE_ERR_DEVICE_TIMEOUT
 
 // Shared memory after the stage ring.
@@ -109,30 +112,34 @@ __device__ __forceinline__ void raster(int local, int MT, int& mb, int& nb, int 
   mb = base + r % gsz;
 }
 
-template <bool GROUP_K, int NUM_B>
-__device__ __forceinline__ bool decode(const Params& p, const Ctrl& c, int t, Tile& tl) {
+// Tile t of the launch -> expert, m-tile, n-tile and K range.  TM = rows per
+// tile (128 for one CTA, 256 for a CTA pair); off = clamped expert offsets;
+// cum = M-grouped prefix of m-tiles per expert.
+template <int TM, bool GROUP_K, int NUM_B>
+__device__ __forceinline__ bool decode(const Params& p, const int* off, const int* cum, int t,
+                                       Tile& tl) {
   const int NT = (p.N + (BN / NUM_B) - 1) / (BN / NUM_B);
   if (!GROUP_K) {
-    const int total = NT * c.cum[p.E];
+    const int total = NT * cum[p.E];
     if (t >= total) return false;
     int e = 0;
-    while (NT * c.cum[e + 1] <= t) ++e;
-    const int local = t - NT * c.cum[e];
-    const int mt = c.cum[e + 1] - c.cum[e];
+    while (NT * cum[e + 1] <= t) ++e;
+    const int local = t - NT * cum[e];
+    const int mt = cum[e + 1] - cum[e];
     tl.e = e;
     raster(local, mt, tl.mb, tl.nb, NT);
-    tl.row0 = c.off[e] + tl.mb * BM;
-    tl.row_end = c.off[e + 1];
+    tl.row0 = off[e] + tl.mb * TM;
+    tl.row_end = off[e + 1];
     tl.nkb = p.kblocks * p.kconcat;
   } else {
     if (t >= p.ktiles) return false;
-    const int MT = (p.M + BM - 1) / BM;
+    const int MT = (p.M + TM - 1) / TM;
     const int per = MT * NT;
     const int e = t / per;
     tl.e = e;
     raster(t - e * per, MT, tl.mb, tl.nb, NT);
-    tl.row0 = c.off[e];
-    tl.row_end = c.off[e + 1];
+    tl.row0 = off[e];
+    tl.row_end = off[e + 1];
     tl.nkb = (tl.row_end - tl.row0 + BK - 1) / BK;
   }
   return true;
@@ -171,6 +178,80 @@ __device__ __forceinline__ void store_f32x32(void* dst, const float* v) {
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
   for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+// One 32-column chunk of the epilogue for one accumulator row.
+//   grow: M-grouped output row (permuted row);  orow: K-grouped output row.
+//   v0 (and v1 for two B operands): the fp32 accumulator values.
+template <int NUM_B, int EPI>
+__device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, int grow, int orow,
+                                               int col, const float* v0, const float* v1) {
+  if (EPI == EPI_SWIGLU) {
+    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+    float hv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) hv[i] = silu_f(v0[i]) * v1[i];
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, v1);
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, hv);
+  } else if (EPI == EPI_BF16) {
+    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
+  } else if (EPI == EPI_SWIGLU_BWD) {
+    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+    float av[32], bv[32];
+    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in0) + o, av);
+    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in1) + o, bv);
+    float da[32], db[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = av[i];
+      const float sg = 1.0f / (1.0f + expf(-a));
+      const float dh = v0[i];
+      da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
+      db[i] = dh * a * sg;
+    }
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
+  } else if (EPI == EPI_F32) {
+    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+    store_f32x32(static_cast<float*>(p.out0) + o, v0);
+  } else {  // EPI_WGRAD
+    const size_t o = (static_cast<size_t>(tl.e) * p.M + orow) * p.N + col;
+    store_f32x32(static_cast<float*>(p.out0) + o, v0);
+    if (NUM_B == 2) store_f32x32(static_cast<float*>(p.out1) + o, v1);
+  }
+}
+
+// Weight gradient of an expert without tokens: zeros for this row's columns.
+template <int NUM_B>
+__device__ __forceinline__ void zero_wgrad_row(const Params& p, const Tile& tl, int orow) {
+  constexpr int BNB = BN / NUM_B;
+  if (orow >= p.M) return;
+  float z[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) z[i] = 0.f;
+  for (int ch = 0; ch < BNB / 32; ++ch) {
+    const int col = tl.nb * BNB + ch * 32;
+    if (col >= p.N) break;
+    const size_t o = (static_cast<size_t>(tl.e) * p.M + orow) * p.N + col;
+    store_f32x32(static_cast<float*>(p.out0) + o, z);
+    if (NUM_B == 2) store_f32x32(static_cast<float*>(p.out1) + o, z);
+  }
+}
+
+// Zero k-rows kv..63 of an MN-major 128-wide A tile (two 64-column chunks):
+// they hold the next expert's rows (or the zero fill) and must add nothing.
+__device__ __forceinline__ void zero_a_tail(uint8_t* a_tile, int kv, int lane) {
+  const int per_chunk = (BK - kv) * 8;  // 16-byte words per chunk
+  for (int w = lane; w < per_chunk * 2; w += 32) {
+    const int ch = w / per_chunk;
+    const int rem = w - ch * per_chunk;
+    *reinterpret_cast<uint4*>(a_tile + ch * CHUNK_BYTES + kv * 128 + rem * 16) =
+        make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
 }
 
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
@@ -232,7 +313,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int q = 0;
       bool ok = true;
       Tile tl;
-      for (int t = blockIdx.x; ok && decode<GROUP_K, NUM_B>(p, c, t, tl); t += gridDim.x) {
+      for (int t = blockIdx.x; ok && decode<BM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += gridDim.x) {
         for (int kb = 0; kb < tl.nkb; ++kb, ++q) {
           const int s = q % STAGES;
           const uint32_t ph = (q / STAGES) & 1;
@@ -296,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int q = 0, it = 0;
     bool ok = true;
     Tile tl;
-    for (int t = blockIdx.x; ok && decode<GROUP_K, NUM_B>(p, c, t, tl); t += gridDim.x) {
+    for (int t = blockIdx.x; ok && decode<BM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += gridDim.x) {
       if (tl.nkb == 0) continue;
       const int buf = it & 1;
       const uint32_t u = (it >> 1) & 1;
@@ -319,19 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* a_tile = smem + s * STAGE_BYTES;
         if (GROUP_K) {
           const int kv = tl.row_end - (tl.row0 + kb * BK);
-          if (kv < BK) {
-            // k-rows kv..63 hold the next expert's rows (or the zero fill):
-            // clear them in A so they add nothing.
-            const int per_chunk = (BK - kv) * 8;  // 16-byte words per chunk
-            for (int w = lane; w < per_chunk * (BM / 64); w += 32) {
-              const int ch = w / per_chunk;
-              const int rem = w - ch * per_chunk;
-              *reinterpret_cast<uint4*>(a_tile + ch * CHUNK_BYTES + kv * 128 + rem * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
+          if (kv < BK) zero_a_tail(a_tile, kv, lane);
         }
         if (lane == 0) {
           tc_fence_after();
@@ -372,23 +441,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = quarter * 32 + lane;
     int it = 0;
     Tile tl;
-    for (int t = blockIdx.x; decode<GROUP_K, NUM_B>(p, c, t, tl); t += gridDim.x) {
+    for (int t = blockIdx.x; decode<BM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += gridDim.x) {
       if (*abort_flag) break;
-      if (GROUP_K && tl.nkb == 0) {
-        // expert without tokens: its weight gradient is zero
-        const int orow = tl.mb * BM + r;
-        if (orow < p.M) {
-          float z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0.f;
-          for (int ch = 0; ch < BNB / 32; ++ch) {
-            const int col = tl.nb * BNB + ch * 32;
-            if (col >= p.N) break;
-            const size_t o = (static_cast<size_t>(tl.e) * p.M + orow) * p.N + col;
-            store_f32x32(static_cast<float*>(p.out0) + o, z);
-            if (NUM_B == 2) store_f32x32(static_cast<float*>(p.out1) + o, z);
-          }
-        }
+      if (GROUP_K && tl.nkb == 0) {  // expert without tokens: zero weight gradient
+        zero_wgrad_row<NUM_B>(p, tl, tl.mb * BM + r);
         continue;
       }
       const int buf = it & 1;
@@ -410,42 +466,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
         const int col = tl.nb * BNB + ch * 32;
         if (!row_ok || col >= p.N) continue;
-        if (EPI == EPI_SWIGLU) {
-          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-          float hv[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) hv[i] = silu_f(v0[i]) * v1[i];
-          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
-          store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, v1);
-          store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, hv);
-        } else if (EPI == EPI_BF16) {
-          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
-        } else if (EPI == EPI_SWIGLU_BWD) {
-          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-          float av[32], bv[32];
-          load_bf16x32(static_cast<const __nv_bfloat16*>(p.in0) + o, av);
-          load_bf16x32(static_cast<const __nv_bfloat16*>(p.in1) + o, bv);
-          float da[32], db[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = av[i];
-            const float sg = 1.0f / (1.0f + expf(-a));
-            const float dh = v0[i];
-            da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
-            db[i] = dh * a * sg;
-          }
-          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
-          store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
-        } else if (EPI == EPI_F32) {
-          const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-          store_f32x32(static_cast<float*>(p.out0) + o, v0);
-        } else {  // EPI_WGRAD
-          const int orow = tl.mb * BM + r;
-          const size_t o = (static_cast<size_t>(tl.e) * p.M + orow) * p.N + col;
-          store_f32x32(static_cast<float*>(p.out0) + o, v0);
-          if (NUM_B == 2) store_f32x32(static_cast<float*>(p.out1) + o, v1);
-        }
+        epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&c.tempty[buf]));
@@ -457,6 +478,316 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ========================================================= CTA-pair kernel
+// Two CTAs of a cluster compute one 256 x 256 tile with tcgen05.mma.cta_group::2:
+// CTA r stages rows [128 r, 128 r + 128) of the A tile and B columns
+// [128 r, 128 r + 128) in its own shared memory; the even CTA's single issuer
+// thread runs the MMAs for both, and each CTA's TMEM holds its 128 rows of the
+// 256-column accumulator.  Per SM this halves the B bytes staged and read per
+// MAC (a 32 KiB stage feeds 128 x 256 x 64 MACs instead of 48 KiB), which is
+// what lets the tensor pipe run close to its peak rather than at the shared-
+// memory bandwidth limit of a one-SM 128 x 256 tile.
+// Synchronisation: the even CTA's `full` barrier counts both CTAs' bytes: its
+// own loads signal it directly, and the odd CTA's loads signal it across the
+// pair (TMA .cta_group::2).  The exception is the last K block of a wgrad tile
+// whose rows run into the next expert: the odd CTA then loads against its own
+// barrier, and its warp 1 waits for the bytes, clears the stale k-rows and
+// arrives on the even CTA's barrier (count 2 = the even producer's arrivals
+// plus, for such a block, that relay).  The issuer's commits are multicast to
+// the `empty` and `tfull` barriers of both CTAs; all eight epilogue warps
+// arrive on the even CTA's `tempty` barrier.
+constexpr int PM = 256;                           // rows of a pair tile
+constexpr int STAGES2 = 6;
+constexpr int A2_BYTES = 128 * BK * 2;            // this CTA's 128 rows: 16 KiB
+constexpr int B2_BYTES = 128 * BK * 2;            // this CTA's 128 columns: 16 KiB
+constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;  // 32 KiB
+
+struct alignas(8) Ctrl2 {
+  uint64_t full[STAGES2];
+  uint64_t empty[STAGES2];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int off[MAX_E + 1];
+  int cum[MAX_E + 1];
+};
+constexpr int SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + static_cast<int>(sizeof(Ctrl2));
+static_assert(SMEM2_BYTES <= 232448, "pair kernel exceeds the 227 KiB shared-memory limit");
+static_assert(SMEM_BYTES <= 232448, "one-CTA kernel exceeds the 227 KiB shared-memory limit");
+
+template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gg2_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctrl2& c = *reinterpret_cast<Ctrl2*>(smem + STAGES2 * STAGE2_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();     // 0: issues the MMAs of the pair
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(cluster_count_x());
+  constexpr int BNB = BN / NUM_B;
+
+  // ------------------------------------------------------------ set-up
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(smem_u32(&c.full[s]), rank == 0 ? 2 : 1);
+      mbar_init(smem_u32(&c.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&c.tfull[b]), 1);
+      mbar_init(smem_u32(&c.tempty[b]), 8);
+    }
+    mbar_init(smem_u32(&c.drain), 1);
+    c.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&maps.a0);
+    tma_prefetch_desc(&maps.b0);
+  }
+  if (warp == 1) {
+    tmem_alloc2(smem_u32(&c.tmem_base), TMEM_COLS);
+    tmem_relinquish2();
+    tc_fence_before();
+  }
+  if (warp >= 2) {
+    for (int e = threadIdx.x - 64; e <= p.E; e += 128) {
+      const int o = __ldg(p.offsets + e);
+      c.off[e] = o < 0 ? 0 : (o > p.rows ? p.rows : o);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 64) {
+    for (int e = 1; e <= p.E; ++e) c.off[e] = max(c.off[e], c.off[e - 1]);
+    if (!GROUP_K) {
+      c.cum[0] = 0;
+      for (int e = 0; e < p.E; ++e) c.cum[e + 1] = c.cum[e] + (c.off[e + 1] - c.off[e] + PM - 1) / PM;
+    }
+  }
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA arrive
+  tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  volatile int* abort_flag = &c.abort;
+  const uint32_t peer_abort = mapa_shared(smem_u32(&c.abort), rank ^ 1u);
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    st_cluster_u32(peer_abort, 1);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int q = 0;
+      bool ok = true;
+      Tile tl;
+      for (int t = cid; ok && decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
+        for (int kb = 0; kb < tl.nkb; ++kb, ++q) {
+          const int s = q % STAGES2;
+          const uint32_t ph = (q / STAGES2) & 1;
+          if (*abort_flag || !mbar_wait(smem_u32(&c.empty[s]), ph ^ 1, p.status, kTimeoutCode)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          // a wgrad K block whose rows run past the expert needs its stale
+          // rows cleared in both CTAs before the MMA (see the relay below)
+          const bool tail = GROUP_K && tl.row_end - (tl.row0 + kb * BK) < BK;
+          const uint32_t own_full = smem_u32(&c.full[s]);
+          uint32_t bar;  // where this CTA's loads complete
+          if (rank == 0) {
+            bar = own_full;
+            if (tail) {
+              mbar_expect_tx(own_full, STAGE2_BYTES);      // + the relay's arrival
+            } else {
+              mbar_expect_tx(own_full, 2 * STAGE2_BYTES);  // both CTAs' bytes
+              mbar_arrive(own_full);
+            }
+          } else if (tail) {
+            bar = own_full;
+            mbar_expect_tx(own_full, STAGE2_BYTES);
+          } else {
+            bar = mapa_shared(own_full, 0);
+          }
+          const bool cross = rank != 0 && !tail;
+          auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+            if (cross)
+              tma_load_2d_pair(dst, m, x, y, bar);
+            else
+              tma_load_2d(dst, m, x, y, bar);
+          };
+          const uint32_t a_dst = smem_u32(smem + s * STAGE2_BYTES);
+          const uint32_t b_dst = a_dst + A2_BYTES;
+          // B columns of this CTA: the second operand for NUM_B = 2 (W3 / dB),
+          // else the upper 128 of the 256
+          const CUtensorMap* bmap = (NUM_B == 2 && rank) ? &maps.b1 : &maps.b0;
+          const int bcol = NUM_B == 2 ? tl.nb * BNB : tl.nb * BN + 128 * static_cast<int>(rank);
+          if (!GROUP_K) {
+            const bool second = p.kconcat == 2 && kb >= p.kblocks;
+            const int kx = (second ? kb - p.kblocks : kb) * BK;
+            load(a_dst, second ? &maps.a1 : &maps.a0, kx, tl.row0 + 128 * static_cast<int>(rank));
+            if (!B_MN) {
+              load(b_dst, second ? &maps.b1 : &maps.b0, kx,
+                   tl.e * p.b_rows + tl.nb * BN + 128 * static_cast<int>(rank));
+            } else {
+#pragma unroll
+              for (int ch = 0; ch < 2; ++ch)
+                load(b_dst + ch * CHUNK_BYTES, bmap, bcol + ch * 64, tl.e * p.b_rows + kx);
+            }
+          } else {
+            const int ky = tl.row0 + kb * BK;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch)
+              load(a_dst + ch * CHUNK_BYTES, &maps.a0,
+                   tl.mb * PM + 128 * static_cast<int>(rank) + ch * 64, ky);
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) load(b_dst + ch * CHUNK_BYTES, bmap, bcol + ch * 64, ky);
+          }
+        }
+      }
+      if (!ok && rank == 0) {
+        // let the loads already issued land before the CTA can exit
+        const int first = q > STAGES2 ? q - STAGES2 : 0;
+        for (int r = first; r < q; ++r)
+          mbar_wait_cluster(smem_u32(&c.full[r % STAGES2]), (r / STAGES2) & 1, p.status,
+                            kTimeoutCode);
+      }
+    }
+  } else if (warp == 1) {
+    if (rank == 0) {
+      // ----------------------------------------------- MMA issuer (even CTA)
+      constexpr uint32_t IDESC = idesc_bf16(PM, BN, A_MN, B_MN);
+      constexpr uint32_t A_LBO = A_MN ? CHUNK_BYTES : 16;
+      constexpr uint32_t B_LBO = B_MN ? CHUNK_BYTES : 16;
+      constexpr uint32_t A_KSTEP = A_MN ? 2048 : 32;
+      constexpr uint32_t B_KSTEP = B_MN ? 2048 : 32;
+      int q = 0, it = 0;
+      bool ok = true;
+      Tile tl;
+      for (int t = cid; ok && decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
+        if (tl.nkb == 0) continue;
+        const int buf = it & 1;
+        const uint32_t u = (it >> 1) & 1;
+        ++it;
+        if (*abort_flag || !mbar_wait(smem_u32(&c.tempty[buf]), u ^ 1, p.status, kTimeoutCode)) {
+          give_up();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem_base + buf * BN;
+        for (int kb = 0; kb < tl.nkb; ++kb, ++q) {
+          const int s = q % STAGES2;
+          const uint32_t ph = (q / STAGES2) & 1;
+          if (*abort_flag || !mbar_wait(smem_u32(&c.full[s]), ph, p.status, kTimeoutCode)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          uint8_t* a_tile = smem + s * STAGE2_BYTES;
+          if (GROUP_K) {
+            const int kv = tl.row_end - (tl.row0 + kb * BK);
+            if (kv < BK) zero_a_tail(a_tile, kv, lane);
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(a_tile);
+            const uint32_t b_base = a_base + A2_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma2_bf16(acc, smem_desc(a_base + kk * A_KSTEP, A_LBO, 1024),
+                         smem_desc(b_base + kk * B_KSTEP, B_LBO, 1024), IDESC, (kb | kk) != 0);
+            umma2_commit_mc(smem_u32(&c.empty[s]), 0x3);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) umma2_commit_mc(smem_u32(&c.tfull[buf]), 0x3);
+        __syncwarp();
+      }
+      if (lane == 0) {
+        umma2_commit(smem_u32(&c.drain));
+        mbar_wait(smem_u32(&c.drain), 0, p.status, kTimeoutCode);
+      }
+      __syncwarp();
+    } else {
+      // ----------------------------------------------- relay (odd CTA)
+      // Only wgrad tiles whose last K block runs into the next expert need it:
+      // that block was loaded against this CTA's own `full` barrier.
+      if (GROUP_K) {
+        int q = 0;
+        uint32_t phase_bits = 0;  // completed phases of each own `full` barrier
+        Tile tl;
+        for (int t = cid; decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
+          if (tl.nkb == 0) continue;
+          const int last = q + tl.nkb - 1;
+          q += tl.nkb;
+          const int kv = tl.row_end - (tl.row0 + (tl.nkb - 1) * BK);
+          if (kv >= BK) continue;
+          const int s = last % STAGES2;
+          const uint32_t ph = (phase_bits >> s) & 1u;
+          phase_bits ^= 1u << s;
+          if (*abort_flag || !mbar_wait(smem_u32(&c.full[s]), ph, p.status, kTimeoutCode)) {
+            give_up();
+            break;
+          }
+          zero_a_tail(smem + s * STAGE2_BYTES, kv, lane);
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&c.full[s]), 0));
+          __syncwarp();
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;             // TMEM lane = row within this CTA's half
+    const int half = 128 * static_cast<int>(rank);
+    int it = 0;
+    Tile tl;
+    for (int t = cid; decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
+      if (*abort_flag) break;
+      const int orow = tl.mb * PM + half + r;       // K-grouped output row
+      if (GROUP_K && tl.nkb == 0) {
+        zero_wgrad_row<NUM_B>(p, tl, orow);
+        continue;
+      }
+      const int buf = it & 1;
+      const uint32_t u = (it >> 1) & 1;
+      ++it;
+      if (!mbar_wait(smem_u32(&c.tfull[buf]), u, p.status, kTimeoutCode)) {
+        give_up();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+      const int grow = tl.row0 + half + r;           // M-grouped row
+      const bool row_ok = GROUP_K ? (orow < p.M) : (grow < tl.row_end);
+#pragma unroll 1
+      for (int ch = 0; ch < BNB / 32; ++ch) {
+        float v0[32];
+        float v1[32];
+        tmem_ld32(tbase + ch * 32, v0);
+        if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
+        const int col = tl.nb * BNB + ch * 32;
+        if (!row_ok || col >= p.N) continue;
+        epilogue_chunk<NUM_B, EPI>(p, tl, grow, orow, col, v0, v1);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&c.tempty[buf]), 0));
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  cluster_sync_all();  // the pair's MMAs and TMEM reads are finished
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, TMEM_COLS);
   }
 }
 
@@ -493,19 +824,72 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Which kernel runs each matmul.  Measured on GB300 (Mixtral-8x7B-shaped
+// layer): the CTA pair is faster for the two dgrads (K-major operands, 5-6%),
+// the one-CTA kernel for the forward and wgrad matmuls (MN-major operands).
+// MOE_GEMM_CTAS=1 or =2 forces one kind for every matmul (for measurement).
+int forced_ctas() {
+  static const int v = [] {
+    const char* e = getenv("MOE_GEMM_CTAS");
+    return (e && (e[0] == '1' || e[0] == '2')) ? e[0] - '0' : 0;
+  }();
+  return v;
+}
+bool pair_for(int epi) {
+  if (forced_ctas()) return forced_ctas() == 2;
+  return epi == EPI_SWIGLU_BWD || epi == EPI_F32;
+}
+
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
-cudaError_t launch(const Params& prm, const Maps& maps, int grid, cudaStream_t s) {
-  auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num_sms,
+                   cudaStream_t s) {
+  if (tiles <= 0) return cudaSuccess;
+  if (!pair_for(EPI)) {
+    auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(prm, maps);
+    return cudaGetLastError();
   }
-  if (grid <= 0) return cudaSuccess;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(prm, maps);
-  return cudaGetLastError();
+  auto kern = gg2_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
+  static bool attr2_set = false;
+  if (!attr2_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+    if (e != cudaSuccess) return e;
+    attr2_set = true;
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM2_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // A persistent grid must fit on the GPU at once: SMs that cannot pair up
+  // inside their GPC host no cluster, so size the grid by what is co-resident.
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
+    max_clusters = n;
+  }
+  g_pair_clusters = max_clusters;
+  const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, prm, maps);
 }
 
 Params base_params(const GemmProblem& g) {
@@ -519,13 +903,23 @@ Params base_params(const GemmProblem& g) {
   return p;
 }
 
+int tile_rows(int epi) { return pair_for(epi) ? PM : BM; }
+
 // Upper bound of an M-grouped tile count without reading the offsets.
-int mgrouped_grid(const GemmProblem& g, int N, int bnb) {
+long long mgrouped_tiles(const GemmProblem& g, int epi, int N, int bnb) {
   const long long nt = (N + bnb - 1) / bnb;
-  const long long mt = (g.rows + BM - 1) / BM + g.E;
-  const long long tiles = nt * mt;
-  return static_cast<int>(tiles < g.num_sms ? tiles : g.num_sms);
+  const long long tm = tile_rows(epi);
+  return nt * ((g.rows + tm - 1) / tm + g.E);
 }
+
+long long kgrouped_tiles(const GemmProblem& g, int epi, int M, int N, int bnb) {
+  const long long tm = tile_rows(epi);
+  return static_cast<long long>(g.E) * ((M + tm - 1) / tm) * ((N + bnb - 1) / bnb);
+}
+
+// Rows of a K-major B box: the whole 256-column tile (one CTA) or this CTA's
+// half of it (pair).
+uint32_t kmajor_b_rows(int epi) { return pair_for(epi) ? 128 : BN; }
 
 }  // namespace
 
@@ -546,7 +940,8 @@ cudaError_t gemm_fc1_fwd(const GemmProblem& g, const void* x_perm, const void* W
   p.out1 = B;
   p.out2 = H;
   p.ldo = g.f;
-  return launch<false, true, 2, EPI_SWIGLU, false>(p, m, mgrouped_grid(g, g.f, BN / 2), s);
+  return launch<false, true, 2, EPI_SWIGLU, false>(p, m, mgrouped_tiles(g, EPI_SWIGLU, g.f, BN / 2),
+                                                    g.num_sms, s);
 }
 
 cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, void* O,
@@ -564,7 +959,8 @@ cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, vo
   p.b_rows = g.f;
   p.out0 = O;
   p.ldo = g.h;
-  return launch<false, true, 1, EPI_BF16, false>(p, m, mgrouped_grid(g, g.h, BN), s);
+  return launch<false, true, 1, EPI_BF16, false>(p, m, mgrouped_tiles(g, EPI_BF16, g.h, BN),
+                                                g.num_sms, s);
 }
 
 cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2, const void* A,
@@ -573,7 +969,7 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   memset(&m, 0, sizeof(m));
   // B operand: W2[e] viewed as [f rows (N), h (K)] -- K-major
   if (!make_map(&m.a0, dO, g.h, g.rows, BK, BM) ||
-      !make_map(&m.b0, W2, g.h, static_cast<uint64_t>(g.E) * g.f, BK, BN))
+      !make_map(&m.b0, W2, g.h, static_cast<uint64_t>(g.E) * g.f, BK, kmajor_b_rows(EPI_SWIGLU_BWD)))
     return cudaErrorInvalidValue;
   m.a1 = m.a0;
   m.b1 = m.b0;
@@ -586,7 +982,8 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.out0 = dA;
   p.out1 = dB;
   p.ldo = g.f;
-  return launch<false, false, 1, EPI_SWIGLU_BWD, false>(p, m, mgrouped_grid(g, g.f, BN), s);
+  return launch<false, false, 1, EPI_SWIGLU_BWD, false>(p, m, mgrouped_tiles(g, EPI_SWIGLU_BWD, g.f, BN),
+                                                         g.num_sms, s);
 }
 
 cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB, const void* W1,
@@ -595,8 +992,8 @@ cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB,
   memset(&m, 0, sizeof(m));
   // B operands: W1[e], W3[e] viewed as [h rows (N), f (K)] -- K-major
   if (!make_map(&m.a0, dA, g.f, g.rows, BK, BM) || !make_map(&m.a1, dB, g.f, g.rows, BK, BM) ||
-      !make_map(&m.b0, W1, g.f, static_cast<uint64_t>(g.E) * g.h, BK, BN) ||
-      !make_map(&m.b1, W3, g.f, static_cast<uint64_t>(g.E) * g.h, BK, BN))
+      !make_map(&m.b0, W1, g.f, static_cast<uint64_t>(g.E) * g.h, BK, kmajor_b_rows(EPI_F32)) ||
+      !make_map(&m.b1, W3, g.f, static_cast<uint64_t>(g.E) * g.h, BK, kmajor_b_rows(EPI_F32)))
     return cudaErrorInvalidValue;
   Params p = base_params(g);
   p.N = g.h;
@@ -605,7 +1002,8 @@ cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB,
   p.b_rows = g.h;
   p.out0 = dX;
   p.ldo = g.h;
-  return launch<false, false, 1, EPI_F32, false>(p, m, mgrouped_grid(g, g.h, BN), s);
+  return launch<false, false, 1, EPI_F32, false>(p, m, mgrouped_tiles(g, EPI_F32, g.h, BN),
+                                                 g.num_sms, s);
 }
 
 cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, float* dW2,
@@ -620,10 +1018,8 @@ cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, 
   p.M = g.f;
   p.N = g.h;
   p.out0 = dW2;
-  const int MT = (g.f + BM - 1) / BM, NT = (g.h + BN - 1) / BN;
-  p.ktiles = g.E * MT * NT;
-  const int grid = p.ktiles < g.num_sms ? p.ktiles : g.num_sms;
-  return launch<true, true, 1, EPI_WGRAD, true>(p, m, grid, s);
+  p.ktiles = static_cast<int>(kgrouped_tiles(g, EPI_WGRAD, g.f, g.h, BN));
+  return launch<true, true, 1, EPI_WGRAD, true>(p, m, p.ktiles, g.num_sms, s);
 }
 
 cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void* dA,
@@ -639,10 +1035,8 @@ cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void*
   p.N = g.f;
   p.out0 = dW1;
   p.out1 = dW3;
-  const int MT = (g.h + BM - 1) / BM, NT = (g.f + BN / 2 - 1) / (BN / 2);
-  p.ktiles = g.E * MT * NT;
-  const int grid = p.ktiles < g.num_sms ? p.ktiles : g.num_sms;
-  return launch<true, true, 2, EPI_WGRAD, true>(p, m, grid, s);
+  p.ktiles = static_cast<int>(kgrouped_tiles(g, EPI_WGRAD, g.h, g.f, BN / 2));
+  return launch<true, true, 2, EPI_WGRAD, true>(p, m, p.ktiles, g.num_sms, s);
 }
 
 }  // namespace moe

@@ -284,36 +284,51 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
-// y[t] = sum_j g[t,j] * O[perm_dst[t*k+j]], fp32 in slot order.
+// y[t] = sum_j g[t,j] * O[perm_dst[t*k+j]], fp32 in slot order.  K = k.
+template <int K>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ O,
                                                       const float* __restrict__ gates,
                                                       const int32_t* __restrict__ perm_dst, int T,
-                                                      int k, int h8, uint4* __restrict__ y) {
+                                                      int h8, uint4* __restrict__ y) {
+  constexpr int k = K;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   for (int t = gw; t < T; t += nw) {
-    long long rows[8];
-    float g[8];
+    long long rows[K];
+    float g[K];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k) {
+    for (int j = 0; j < K; ++j) {
+      {
         const long long r = __ldg(perm_dst + static_cast<size_t>(t) * k + j);
         rows[j] = r < 0 ? 0 : (r >= static_cast<long long>(T) * k ? static_cast<long long>(T) * k - 1 : r);
         g[j] = __ldg(gates + static_cast<size_t>(t) * k + j);
       }
     }
-    for (int c = lane; c < h8; c += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // four 16-byte pieces per lane per step: 4 * k loads in flight
+    for (int c0 = lane; c0 < h8; c0 += 128) {
+      uint4 q[4][K];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= k) break;
-        float v[8];
-        unpack8(__ldg(O + rows[j] * h8 + c), v);
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g[j], v[i], acc[i]);
+        for (int j = 0; j < K; ++j)
+          if (c < h8) q[u][j] = __ldg(O + rows[j] * h8 + c);
       }
-      y[static_cast<size_t>(t) * h8 + c] = pack8(acc);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= h8) break;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          float v[8];
+          unpack8(q[u][j], v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(g[j], v[i], acc[i]);
+        }
+        y[static_cast<size_t>(t) * h8 + c] = pack8(acc);
+      }
     }
   }
 }
@@ -540,8 +555,18 @@ cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t*
                            int k, int h, uint16_t* y, int num_sms, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = grid_for(T, num_sms, 8, 16);
-  combine_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(O), gates, perm_dst, T, k,
-                                      h / 8, reinterpret_cast<uint4*>(y));
+  const uint4* o = reinterpret_cast<const uint4*>(O);
+  uint4* yy = reinterpret_cast<uint4*>(y);
+  switch (k) {
+    case 1: combine_kernel<1><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    case 2: combine_kernel<2><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    case 3: combine_kernel<3><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    case 4: combine_kernel<4><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    case 5: combine_kernel<5><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    case 6: combine_kernel<6><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    case 7: combine_kernel<7><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    default: combine_kernel<8><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+  }
   return cudaGetLastError();
 }
 
