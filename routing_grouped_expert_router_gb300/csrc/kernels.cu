@@ -42,63 +42,86 @@ int grid_for(long long warps_needed, int num_sms, int warps_per_block, int block
 }
 
 // ------------------------------------------------------------------ router
-// A warp owns TOK consecutive tokens.  Lanes split the hidden dimension in
-// 8-element (16-byte) pieces; each lane keeps EP partial logits per token and
-// reuses every router-weight row it loads for all TOK tokens.  A butterfly
-// then gives every lane the full logits; lane j selects for token j.
-template <int EP, int TOK, bool VEC>
-__global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict__ x,
-                                                     const float* __restrict__ Wg,
-                                                     const float* __restrict__ b, int T, int h,
-                                                     int E, int k, int32_t* __restrict__ topk_idx,
-                                                     float* __restrict__ gates) {
+// Block of 8 warps, persistent over tiles of 8 * TOK tokens (TOK per warp).
+// Lanes split the hidden dimension in 8-element slices, so each x load of a
+// warp reads 512 contiguous bytes.  The router weights of a CH-column chunk
+// are staged in shared memory, laid out so that lane l's eight rows of a step
+// are one contiguous block padded by 16 bytes (conflict-free 16-byte loads),
+// and each loaded weight vector serves all TOK tokens of the warp.  While a
+// tile computes, the next tile's rows are prefetched into L2.  A butterfly
+// then gives every lane the full logits; lane u selects for token u.
+template <int EP>
+struct RouterShape {
+  static constexpr int TOK = EP <= 8 ? 8 : 64 / EP;     // tokens per warp
+  static constexpr int CH = EP <= 8 ? 4096 : 32768 / EP;  // columns per staged chunk
+  static constexpr int SLICE = 8 * EP + 4;              // floats per (step, lane) block
+  static constexpr int SMEM = (CH / 8) * SLICE * 4;     // bytes
+};
+
+template <int EP>
+__global__ void __launch_bounds__(256, 1) router_kernel(const uint16_t* __restrict__ x,
+                                                        const float* __restrict__ Wg,
+                                                        const float* __restrict__ b, int T,
+                                                        int h, int E, int k,
+                                                        int32_t* __restrict__ topk_idx,
+                                                        float* __restrict__ gates) {
+  using S = RouterShape<EP>;
+  constexpr int TOK = S::TOK;
+  extern __shared__ float sw[];
   const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  for (int t0 = gw * TOK; t0 < T; t0 += nw * TOK) {
+  const int warp = threadIdx.x >> 5;
+  const int tile = 8 * TOK;
+  for (int t0 = blockIdx.x * tile; t0 < T; t0 += gridDim.x * tile) {
+    // next tile's rows into L2 while this one computes
+    const int tn = t0 + gridDim.x * tile + static_cast<int>(threadIdx.x);
+    if (static_cast<int>(threadIdx.x) < tile && tn < T)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(x + static_cast<size_t>(tn) * h),
+                   "r"(h * 2)
+                   : "memory");
+    const int tw = t0 + warp * TOK;
     float acc[TOK][EP];
 #pragma unroll
     for (int u = 0; u < TOK; ++u)
 #pragma unroll
       for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
 
-    for (int i0 = lane * 8; i0 < h; i0 += 256) {
-      uint4 xq[TOK];
+    for (int c0 = 0; c0 < h; c0 += S::CH) {
+      const int rows = min(S::CH, h - c0);
+      __syncthreads();  // the previous chunk is no longer read
+      for (int q = threadIdx.x; q < rows * EP; q += 256) {
+        const int lr = q / EP;
+        const int e = q - lr * EP;
+        const int slot = (lr >> 3) * S::SLICE + (lr & 7) * EP + e;
+        sw[slot] = (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
+      }
+      __syncthreads();
+      for (int m = 0; m * 256 < rows; ++m) {
+        const int lc = 256 * m + 8 * lane;  // this lane's columns within the chunk
+        if (lc >= rows) break;
+        uint4 xq[TOK];
 #pragma unroll
-      for (int u = 0; u < TOK; ++u)
-        xq[u] = (t0 + u < T)
-                    ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + u) * h + i0))
-                    : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < TOK; ++u)
+          xq[u] = (tw + u < T) ? __ldg(reinterpret_cast<const uint4*>(
+                                     x + static_cast<size_t>(tw + u) * h + c0 + lc))
+                               : make_uint4(0, 0, 0, 0);
+        const float4* wb = reinterpret_cast<const float4*>(sw + (lc >> 3) * S::SLICE);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float xv[TOK];
+        for (int j = 0; j < 8; ++j) {
+          float xv[TOK];
 #pragma unroll
-        for (int u = 0; u < TOK; ++u) {
-          const uint32_t w = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
-          xv[u] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
-        }
-        const float* wrow = Wg + static_cast<size_t>(i0 + j) * E;
-        if (VEC) {
+          for (int u = 0; u < TOK; ++u) {
+            const uint32_t w = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
+            xv[u] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
+          }
 #pragma unroll
           for (int e4 = 0; e4 < EP / 4; ++e4) {
-            if (e4 * 4 < E) {
-              const float4 wv = __ldg(reinterpret_cast<const float4*>(wrow) + e4);
+            const float4 wv = wb[(j * EP) / 4 + e4];
 #pragma unroll
-              for (int u = 0; u < TOK; ++u) {
-                acc[u][4 * e4 + 0] = fmaf(xv[u], wv.x, acc[u][4 * e4 + 0]);
-                acc[u][4 * e4 + 1] = fmaf(xv[u], wv.y, acc[u][4 * e4 + 1]);
-                acc[u][4 * e4 + 2] = fmaf(xv[u], wv.z, acc[u][4 * e4 + 2]);
-                acc[u][4 * e4 + 3] = fmaf(xv[u], wv.w, acc[u][4 * e4 + 3]);
-              }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < EP; ++e) {
-            if (e < E) {
-              const float wv = __ldg(wrow + e);
-#pragma unroll
-              for (int u = 0; u < TOK; ++u) acc[u][e] = fmaf(xv[u], wv, acc[u][e]);
+            for (int u = 0; u < TOK; ++u) {
+              acc[u][4 * e4 + 0] = fmaf(xv[u], wv.x, acc[u][4 * e4 + 0]);
+              acc[u][4 * e4 + 1] = fmaf(xv[u], wv.y, acc[u][4 * e4 + 1]);
+              acc[u][4 * e4 + 2] = fmaf(xv[u], wv.z, acc[u][4 * e4 + 2]);
+              acc[u][4 * e4 + 3] = fmaf(xv[u], wv.w, acc[u][4 * e4 + 3]);
             }
           }
         }
@@ -113,7 +136,7 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict_
 
 #pragma unroll
     for (int u = 0; u < TOK; ++u) {
-      const int t = t0 + u;
+      const int t = tw + u;
       if (lane != u || t >= T) continue;
       float l[EP];
 #pragma unroll
@@ -161,15 +184,20 @@ __global__ void __launch_bounds__(256) router_kernel(const uint16_t* __restrict_
   }
 }
 
-template <int EP, int TOK>
+template <int EP>
 cudaError_t router_launch(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
                           int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
-  const long long warps = (T + TOK - 1) / TOK;
-  const int grid = grid_for(warps, num_sms, 8, 8);
-  if (E % 4 == 0)
-    router_kernel<EP, TOK, true><<<grid, 256, 0, s>>>(x, Wg, b, T, h, E, k, idx, gates);
-  else
-    router_kernel<EP, TOK, false><<<grid, 256, 0, s>>>(x, Wg, b, T, h, E, k, idx, gates);
+  using S = RouterShape<EP>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(router_kernel<EP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int tiles = (T + 8 * S::TOK - 1) / (8 * S::TOK);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  router_kernel<EP><<<grid, 256, S::SMEM, s>>>(x, Wg, b, T, h, E, k, idx, gates);
   return cudaGetLastError();
 }
 
@@ -510,10 +538,10 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, in
 cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
                           int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  if (E <= 8) return router_launch<8, 8>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
-  if (E <= 16) return router_launch<16, 4>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
-  if (E <= 32) return router_launch<32, 2>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
-  return router_launch<64, 1>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+  if (E <= 8) return router_launch<8>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+  if (E <= 16) return router_launch<16>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+  if (E <= 32) return router_launch<32>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+  return router_launch<64>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
 }
 
 cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E, int32_t* blk_counts,
