@@ -107,6 +107,7 @@ struct WsLayout {
   size_t x_perm = 0, dO = 0, dA = 0, dB = 0;  // expert backward
   size_t dX = 0, dg = 0;                     // layer backward
   size_t dl = 0, WgT = 0, partial = 0;       // router backward
+  size_t logits = 0;                         // router partial logits
   size_t total = 0;
 };
 WsLayout ws_layout(const moe_dims& d, int op) {
@@ -115,6 +116,7 @@ WsLayout ws_layout(const moe_dims& d, int op) {
   Carve c;
   WsLayout L;
   L.status = c.take(kAlign);
+  auto route = [&] { L.logits = c.take(moe::router_partial_bytes(d.T, d.h, d.E)); };
   auto dispatch = [&] {
     L.blk_counts = c.take(nblk * d.E * 4);
     L.bases = c.take(nblk * d.E * 4);
@@ -131,12 +133,15 @@ WsLayout ws_layout(const moe_dims& d, int op) {
     L.dB = c.take(R * d.f * 2);
   };
   switch (op) {
-    case MOE_OP_ROUTE: break;
+    case MOE_OP_ROUTE: route(); break;
     case MOE_OP_PERMUTE: dispatch(); break;
     case MOE_OP_EXPERT_FFN_FWD: L.x_perm = c.take(R * d.h * 2); break;
     case MOE_OP_EXPERT_FFN_BWD: expert_bwd(true); break;
     case MOE_OP_ROUTER_BWD: router_bwd(); break;
-    case MOE_OP_LAYER_FWD: dispatch(); break;
+    case MOE_OP_LAYER_FWD:
+      route();
+      dispatch();
+      break;
     case MOE_OP_LAYER_BWD:
       expert_bwd(false);
       L.dX = c.take(R * d.h * 4);
@@ -188,9 +193,9 @@ GemmProblem problem(const moe_dims& d, const int32_t* offsets, void* ws) {
 
 // --------------------------------------------------------- the steps
 moe_status do_route(const moe_dims& d, const uint16_t* x, const float* Wg, const float* b,
-                    int32_t* idx, float* gates, cudaStream_t stream) {
+                    int32_t* idx, float* gates, void* ws, const WsLayout& L, cudaStream_t stream) {
   MOE_RUN(moe::launch_router(x, Wg, d.has_bias ? b : nullptr, d.T, d.h, d.E, d.k, idx, gates,
-                             num_sms(), stream),
+                             at<float>(ws, L.logits), num_sms(), stream),
           "router_topk");
   return MOE_OK;
 }
@@ -340,7 +345,7 @@ moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const float* Wg, c
     return MOE_ERR_INVALID_ARG;
   if ((st = ws_check(d, MOE_OP_ROUTE, ws, ws_bytes)) != MOE_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  return do_route(d, x, Wg, b, topk_idx, gates, stream);
+  return do_route(d, x, Wg, b, topk_idx, gates, ws, ws_layout(d, MOE_OP_ROUTE), stream);
 }
 
 moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const moe_bf16* x,
@@ -486,7 +491,7 @@ moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* W
   int32_t* pdst = at<int32_t>(saved, S.perm_dst);
   uint16_t* xp = at<uint16_t>(saved, S.x_perm);
   uint16_t* O = at<uint16_t>(saved, S.O);
-  if ((st = do_route(d, x, Wg, b, idx, gates, stream)) != MOE_OK) return st;
+  if ((st = do_route(d, x, Wg, b, idx, gates, ws, L, stream)) != MOE_OK) return st;
   if ((st = do_dispatch(d, idx, at<int32_t>(saved, S.counts), offsets, psrc, pdst, ws, L,
                         stream)) != MOE_OK)
     return st;

@@ -42,41 +42,94 @@ int grid_for(long long warps_needed, int num_sms, int warps_per_block, int block
 }
 
 // ------------------------------------------------------------------ router
-// Block of 8 warps, persistent over tiles of 8 * TOK tokens (TOK per warp).
-// Lanes split the hidden dimension in 8-element slices, so each x load of a
-// warp reads 512 contiguous bytes.  The router weights of a CH-column chunk
-// are staged in shared memory, laid out so that lane l's eight rows of a step
-// are one contiguous block padded by 16 bytes (conflict-free 16-byte loads),
-// and each loaded weight vector serves all TOK tokens of the warp.  While a
-// tile computes, the next tile's rows are prefetched into L2.  A butterfly
-// then gives every lane the full logits; lane u selects for token u.
-template <int EP>
-struct RouterShape {
-  static constexpr int TOK = EP <= 8 ? 8 : 64 / EP;     // tokens per warp
-  static constexpr int CH = EP <= 8 ? 4096 : 32768 / EP;  // columns per staged chunk
-  static constexpr int SLICE = 8 * EP + 4;              // floats per (step, lane) block
-  static constexpr int SMEM = (CH / 8) * SLICE * 4;     // bytes
-};
+// The hidden dimension is cut into chunks of CH columns; each block stages one
+// chunk of the router weights in shared memory once and then streams every
+// token tile of its share through it.  With one chunk (E <= 8, h <= 4096) the
+// kernel finishes the routing itself; otherwise it writes fp32 partial logits
+// [chunk][T][EP] and router_select_kernel adds them in chunk order.
 
+// top-k of l[0..E) (descending, ties to the lower id) and renormalised gates
+// exp(l_j - l_top) / sum over the selected.
 template <int EP>
-__global__ void __launch_bounds__(256, 1) router_kernel(const uint16_t* __restrict__ x,
-                                                        const float* __restrict__ Wg,
-                                                        const float* __restrict__ b, int T,
-                                                        int h, int E, int k,
-                                                        int32_t* __restrict__ topk_idx,
-                                                        float* __restrict__ gates) {
-  using S = RouterShape<EP>;
-  constexpr int TOK = S::TOK;
+__device__ __forceinline__ void select_topk(const float (&l)[EP], int E, int k, int32_t* idx_out,
+                                            float* gate_out) {
+  uint64_t taken = 0;
+  float sel_l[8];
+  int sel_e[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= k) break;
+    int best = -1;
+    float bv = 0.f;
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+      if (e < E && !((taken >> e) & 1ull) && (best < 0 || l[e] > bv)) {
+        best = e;
+        bv = l[e];
+      }
+    }
+    if (best < 0) {  // only when logits are NaN: keep the index in range
+      best = 0;
+      while (best < E - 1 && ((taken >> best) & 1ull)) ++best;
+      bv = l[0];
+    }
+    taken |= 1ull << best;
+    sel_e[j] = best;
+    sel_l[j] = bv;
+  }
+  float sj[8];
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= k) break;
+    sj[j] = expf(sel_l[j] - sel_l[0]);
+    sum += sj[j];
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= k) break;
+    idx_out[j] = sel_e[j];
+    gate_out[j] = sj[j] / sum;
+  }
+}
+
+// ---- E <= 8: lanes split the columns (8-element slices, 512-byte coalesced
+// x loads per warp); each lane keeps all 8 partial logits of TOK tokens and
+// reads its rows of the weights as conflict-free 16-byte loads from a padded
+// layout (lane l's eight rows are one block + 16 bytes).  A butterfly gives
+// every lane the full logits.
+constexpr int kRouterATok = 8;
+constexpr int kRouterACh = 4096;
+constexpr int kRouterASlice = 8 * 8 + 4;
+constexpr int kRouterASmem = (kRouterACh / 8) * kRouterASlice * 4;
+
+__global__ void __launch_bounds__(256, 1) router_a_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ Wg, const float* __restrict__ b,
+    int T, int h, int E, int k, int nch, int32_t* __restrict__ topk_idx,
+    float* __restrict__ gates, float* __restrict__ partial) {
+  constexpr int EP = 8, TOK = kRouterATok, CH = kRouterACh, SLICE = kRouterASlice;
   extern __shared__ float sw[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const int c = blockIdx.x % nch;
+  const int sub = blockIdx.x / nch;
+  const int bpc = gridDim.x / nch;
+  const int c0 = c * CH;
+  const int rows = min(CH, h - c0);
+  for (int q = threadIdx.x; q < rows * EP; q += 256) {
+    const int lr = q / EP;
+    const int e = q - lr * EP;
+    sw[(lr >> 3) * SLICE + (lr & 7) * EP + e] =
+        (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
+  }
+  __syncthreads();
   const int tile = 8 * TOK;
-  for (int t0 = blockIdx.x * tile; t0 < T; t0 += gridDim.x * tile) {
-    // next tile's rows into L2 while this one computes
-    const int tn = t0 + gridDim.x * tile + static_cast<int>(threadIdx.x);
+  for (int t0 = sub * tile; t0 < T; t0 += bpc * tile) {
+    const int tn = t0 + bpc * tile + static_cast<int>(threadIdx.x);
     if (static_cast<int>(threadIdx.x) < tile && tn < T)
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(x + static_cast<size_t>(tn) * h),
-                   "r"(h * 2)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       x + static_cast<size_t>(tn) * h + c0),
+                   "r"(rows * 2)
                    : "memory");
     const int tw = t0 + warp * TOK;
     float acc[TOK][EP];
@@ -84,45 +137,31 @@ __global__ void __launch_bounds__(256, 1) router_kernel(const uint16_t* __restri
     for (int u = 0; u < TOK; ++u)
 #pragma unroll
       for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
-
-    for (int c0 = 0; c0 < h; c0 += S::CH) {
-      const int rows = min(S::CH, h - c0);
-      __syncthreads();  // the previous chunk is no longer read
-      for (int q = threadIdx.x; q < rows * EP; q += 256) {
-        const int lr = q / EP;
-        const int e = q - lr * EP;
-        const int slot = (lr >> 3) * S::SLICE + (lr & 7) * EP + e;
-        sw[slot] = (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
-      }
-      __syncthreads();
-      for (int m = 0; m * 256 < rows; ++m) {
-        const int lc = 256 * m + 8 * lane;  // this lane's columns within the chunk
-        if (lc >= rows) break;
-        uint4 xq[TOK];
+    for (int lc = 8 * lane; lc < rows; lc += 256) {
+      uint4 xq[TOK];
 #pragma unroll
-        for (int u = 0; u < TOK; ++u)
-          xq[u] = (tw + u < T) ? __ldg(reinterpret_cast<const uint4*>(
-                                     x + static_cast<size_t>(tw + u) * h + c0 + lc))
-                               : make_uint4(0, 0, 0, 0);
-        const float4* wb = reinterpret_cast<const float4*>(sw + (lc >> 3) * S::SLICE);
+      for (int u = 0; u < TOK; ++u)
+        xq[u] = (tw + u < T) ? __ldg(reinterpret_cast<const uint4*>(
+                                   x + static_cast<size_t>(tw + u) * h + c0 + lc))
+                             : make_uint4(0, 0, 0, 0);
+      const float4* wb = reinterpret_cast<const float4*>(sw + (lc >> 3) * SLICE);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float xv[TOK];
+      for (int j = 0; j < 8; ++j) {
+        float xv[TOK];
+#pragma unroll
+        for (int u = 0; u < TOK; ++u) {
+          const uint32_t w = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
+          xv[u] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
+        }
+#pragma unroll
+        for (int e4 = 0; e4 < EP / 4; ++e4) {
+          const float4 wv = wb[(j * EP) / 4 + e4];
 #pragma unroll
           for (int u = 0; u < TOK; ++u) {
-            const uint32_t w = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
-            xv[u] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
-          }
-#pragma unroll
-          for (int e4 = 0; e4 < EP / 4; ++e4) {
-            const float4 wv = wb[(j * EP) / 4 + e4];
-#pragma unroll
-            for (int u = 0; u < TOK; ++u) {
-              acc[u][4 * e4 + 0] = fmaf(xv[u], wv.x, acc[u][4 * e4 + 0]);
-              acc[u][4 * e4 + 1] = fmaf(xv[u], wv.y, acc[u][4 * e4 + 1]);
-              acc[u][4 * e4 + 2] = fmaf(xv[u], wv.z, acc[u][4 * e4 + 2]);
-              acc[u][4 * e4 + 3] = fmaf(xv[u], wv.w, acc[u][4 * e4 + 3]);
-            }
+            acc[u][4 * e4 + 0] = fmaf(xv[u], wv.x, acc[u][4 * e4 + 0]);
+            acc[u][4 * e4 + 1] = fmaf(xv[u], wv.y, acc[u][4 * e4 + 1]);
+            acc[u][4 * e4 + 2] = fmaf(xv[u], wv.z, acc[u][4 * e4 + 2]);
+            acc[u][4 * e4 + 3] = fmaf(xv[u], wv.w, acc[u][4 * e4 + 3]);
           }
         }
       }
@@ -133,71 +172,190 @@ __global__ void __launch_bounds__(256, 1) router_kernel(const uint16_t* __restri
       for (int e = 0; e < EP; ++e)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc[u][e] += __shfl_xor_sync(kFull, acc[u][e], off);
-
 #pragma unroll
     for (int u = 0; u < TOK; ++u) {
       const int t = tw + u;
       if (lane != u || t >= T) continue;
-      float l[EP];
+      if (nch == 1) {
+        float l[EP];
 #pragma unroll
-      for (int e = 0; e < EP; ++e) l[e] = (e < E) ? acc[u][e] + (b ? __ldg(b + e) : 0.f) : 0.f;
-      uint64_t taken = 0;
-      float sel_l[8];
-      int sel_e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= k) break;
-        int best = -1;
-        float bv = 0.f;
-#pragma unroll
-        for (int e = 0; e < EP; ++e) {
-          if (e < E && !((taken >> e) & 1ull) && (best < 0 || l[e] > bv)) {
-            best = e;
-            bv = l[e];
-          }
-        }
-        if (best < 0) {  // only when logits are NaN: keep the index in range
-          best = 0;
-          while (best < E - 1 && ((taken >> best) & 1ull)) ++best;
-          bv = l[0];
-        }
-        taken |= 1ull << best;
-        sel_e[j] = best;
-        sel_l[j] = bv;
-      }
-      // renormalised gates: exp(l_j - l_top) / sum over the selected
-      float sj[8];
-      float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= k) break;
-        sj[j] = expf(sel_l[j] - sel_l[0]);
-        sum += sj[j];
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= k) break;
-        topk_idx[static_cast<size_t>(t) * k + j] = sel_e[j];
-        gates[static_cast<size_t>(t) * k + j] = sj[j] / sum;
+        for (int e = 0; e < EP; ++e) l[e] = (e < E) ? acc[u][e] + (b ? __ldg(b + e) : 0.f) : 0.f;
+        select_topk<EP>(l, E, k, topk_idx + static_cast<size_t>(t) * k,
+                        gates + static_cast<size_t>(t) * k);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(partial + (static_cast<size_t>(c) * T + t) * EP);
+        dst[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+        dst[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
       }
     }
   }
 }
 
+// ---- E > 8: lanes own experts.  A group of GL = min(32, EP) lanes handles
+// TOK tokens, lane i of a group the experts i, i + 32, ...  Each warp stages
+// its tokens' x slice (XS columns) in shared memory and reads it as
+// broadcasts; every weight value a lane loads from the staged chunk (one
+// conflict-free 4-byte load) then feeds TOK tokens.  No cross-lane reduction.
+constexpr int kRouterBTok = 16;
+constexpr int kRouterBXs = 64;
+constexpr int kRouterBXsp = kRouterBXs + 8;  // padded row (bf16) of a staged x slice
+
 template <int EP>
-cudaError_t router_launch(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
-                          int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
-  using S = RouterShape<EP>;
+struct RouterB {
+  static constexpr int GL = EP >= 32 ? 32 : EP;  // lanes per token group
+  static constexpr int NG = 32 / GL;             // token groups per warp
+  static constexpr int EPL = EP / GL;            // experts per lane
+  static constexpr int CH = 32768 / EP;          // columns per chunk (128 KiB of weights)
+  static constexpr int XROWS = NG * kRouterBTok; // staged token rows per warp
+  static constexpr int SMEM = CH * EP * 4 + 8 * XROWS * kRouterBXsp * 2;
+};
+
+template <int EP>
+__global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __restrict__ x,
+                                                          const float* __restrict__ Wg, int T,
+                                                          int h, int E, int nch,
+                                                          float* __restrict__ partial) {
+  using S = RouterB<EP>;
+  constexpr int TOK = kRouterBTok, XS = kRouterBXs, XSP = kRouterBXsp;
+  extern __shared__ float sw[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sw + S::CH * EP);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane / S::GL;
+  const int el = lane % S::GL;
+  const int c = blockIdx.x % nch;
+  const int sub = blockIdx.x / nch;
+  const int bpc = gridDim.x / nch;
+  const int c0 = c * S::CH;
+  const int rows = min(S::CH, h - c0);
+  for (int q = threadIdx.x; q < rows * EP; q += 256) {
+    const int lr = q / EP;
+    const int e = q - lr * EP;
+    sw[q] = (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
+  }
+  __syncthreads();
+  uint16_t* xw = xs + warp * S::XROWS * XSP;
+  const int btile = 8 * S::XROWS;
+  for (int t0 = sub * btile; t0 < T; t0 += bpc * btile) {
+    const int tw = t0 + warp * S::XROWS;  // this warp's first token
+    float acc[TOK][S::EPL];
+#pragma unroll
+    for (int u = 0; u < TOK; ++u)
+#pragma unroll
+      for (int i = 0; i < S::EPL; ++i) acc[u][i] = 0.f;
+    for (int cs = 0; cs < rows; cs += XS) {
+      // stage x[tw .. tw + XROWS)[c0 + cs .. + XS) (rows of 128 bytes)
+#pragma unroll
+      for (int r = 0; r < S::XROWS * (XS / 8) / 32; ++r) {
+        const int id = r * 32 + lane;
+        const int row = id / (XS / 8);
+        const int c8 = id % (XS / 8);
+        const int t = tw + row;
+        const uint4 v = (t < T) ? __ldg(reinterpret_cast<const uint4*>(
+                                      x + static_cast<size_t>(t) * h + c0 + cs + 8 * c8))
+                                : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(xw + row * XSP + 8 * c8) = v;
+      }
+      __syncwarp();
+#pragma unroll 1
+      for (int c8 = 0; c8 < XS / 8; ++c8) {
+        uint4 xq[TOK];
+#pragma unroll
+        for (int u = 0; u < TOK; ++u)
+          xq[u] = *reinterpret_cast<const uint4*>(xw + (g * TOK + u) * XSP + 8 * c8);
+        const float* wr = sw + (cs + 8 * c8) * EP + el;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float w[S::EPL];
+#pragma unroll
+          for (int i = 0; i < S::EPL; ++i) w[i] = wr[j * EP + S::GL * i];
+#pragma unroll
+          for (int u = 0; u < TOK; ++u) {
+            const uint32_t q = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
+            const float xv = (j & 1) ? bf16_hi(q) : bf16_lo(q);
+#pragma unroll
+            for (int i = 0; i < S::EPL; ++i) acc[u][i] = fmaf(xv, w[i], acc[u][i]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int u = 0; u < TOK; ++u) {
+      const int t = tw + g * TOK + u;
+      if (t >= T) continue;
+      float* dst = partial + (static_cast<size_t>(c) * T + t) * EP + el;
+#pragma unroll
+      for (int i = 0; i < S::EPL; ++i) dst[S::GL * i] = acc[u][i];
+    }
+  }
+}
+
+// Thread per token: logits = sum of the chunks' partials (in chunk order) + b.
+template <int EP>
+__global__ void __launch_bounds__(128) router_select_kernel(const float* __restrict__ partial,
+                                                            int nch, const float* __restrict__ b,
+                                                            int T, int E, int k,
+                                                            int32_t* __restrict__ topk_idx,
+                                                            float* __restrict__ gates) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    float l[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) l[e] = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const float4* src =
+          reinterpret_cast<const float4*>(partial + (static_cast<size_t>(c) * T + t) * EP);
+#pragma unroll
+      for (int e4 = 0; e4 < EP / 4; ++e4) {
+        const float4 v = __ldg(src + e4);
+        l[4 * e4 + 0] += v.x;
+        l[4 * e4 + 1] += v.y;
+        l[4 * e4 + 2] += v.z;
+        l[4 * e4 + 3] += v.w;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e < E && b) l[e] += __ldg(b + e);
+    select_topk<EP>(l, E, k, topk_idx + static_cast<size_t>(t) * k,
+                    gates + static_cast<size_t>(t) * k);
+  }
+}
+
+int router_padded_e(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : 64; }
+
+int router_chunks(int h, int E) {
+  const int ep = router_padded_e(E);
+  const int ch = ep == 8 ? kRouterACh : 32768 / ep;
+  return (h + ch - 1) / ch;
+}
+
+template <int EP>
+cudaError_t router_b_launch(const uint16_t* x, const float* Wg, int T, int h, int E, int nch,
+                            float* partial, int num_sms, cudaStream_t s) {
+  using S = RouterB<EP>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(router_kernel<EP>,
+    cudaError_t e = cudaFuncSetAttribute(router_b_kernel<EP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int tiles = (T + 8 * S::TOK - 1) / (8 * S::TOK);
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  router_kernel<EP><<<grid, 256, S::SMEM, s>>>(x, Wg, b, T, h, E, k, idx, gates);
+  const int tiles = (T + 8 * S::XROWS - 1) / (8 * S::XROWS);
+  int bpc = num_sms / nch;
+  if (bpc < 1) bpc = 1;
+  if (bpc > tiles) bpc = tiles;
+  router_b_kernel<EP><<<nch * bpc, 256, S::SMEM, s>>>(x, Wg, T, h, E, nch, partial);
+  return cudaGetLastError();
+}
+
+template <int EP>
+cudaError_t router_select_launch(const float* partial, int nch, const float* b, int T, int E,
+                                 int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
+  long long blocks = (T + 127) / 128;
+  if (blocks > num_sms * 8) blocks = num_sms * 8;
+  router_select_kernel<EP><<<static_cast<int>(blocks), 128, 0, s>>>(partial, nch, b, T, E, k, idx,
+                                                                   gates);
   return cudaGetLastError();
 }
 
@@ -535,14 +693,46 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, in
 
 }  // namespace
 
-cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
-                          int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
-  if (T == 0) return cudaSuccess;
-  if (E <= 8) return router_launch<8>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
-  if (E <= 16) return router_launch<16>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
-  if (E <= 32) return router_launch<32>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
-  return router_launch<64>(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
+size_t router_partial_bytes(int T, int h, int E) {
+  const int nch = router_chunks(h, E);
+  if (router_padded_e(E) == 8 && nch == 1) return 0;
+  return static_cast<size_t>(nch) * T * router_padded_e(E) * sizeof(float);
 }
+
+cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
+                          int k, int32_t* idx, float* gates, float* partial, int num_sms,
+                          cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int ep = router_padded_e(E);
+  const int nch = router_chunks(h, E);
+  cudaError_t err;
+  if (ep == 8) {
+    static bool attr = false;
+    if (!attr) {
+      err = cudaFuncSetAttribute(router_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kRouterASmem);
+      if (err != cudaSuccess) return err;
+      attr = true;
+    }
+    const int tiles = (T + 8 * kRouterATok - 1) / (8 * kRouterATok);
+    int bpc = num_sms / nch;
+    if (bpc < 1) bpc = 1;
+    if (bpc > tiles) bpc = tiles;
+    router_a_kernel<<<nch * bpc, 256, kRouterASmem, s>>>(x, Wg, b, T, h, E, k, nch, idx, gates,
+                                                        partial);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || nch == 1) return err;
+    return router_select_launch<8>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
+  }
+  if (ep == 16) err = router_b_launch<16>(x, Wg, T, h, E, nch, partial, num_sms, s);
+  else if (ep == 32) err = router_b_launch<32>(x, Wg, T, h, E, nch, partial, num_sms, s);
+  else err = router_b_launch<64>(x, Wg, T, h, E, nch, partial, num_sms, s);
+  if (err != cudaSuccess) return err;
+  if (ep == 16) return router_select_launch<16>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
+  if (ep == 32) return router_select_launch<32>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
+  return router_select_launch<64>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
+}
+
 
 cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E, int32_t* blk_counts,
                                  cudaStream_t s) {

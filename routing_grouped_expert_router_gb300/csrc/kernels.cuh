@@ -14,9 +14,12 @@ inline int dispatch_blocks(long long assignments) {
   return static_cast<int>((assignments + kDispatchChunk - 1) / kDispatchChunk);
 }
 
-// Router + softmax + top-k + renormalisation (warp per token group).
+// Router + softmax + top-k + renormalisation.  `partial` is scratch of
+// router_partial_bytes(T, h, E) bytes (may be NULL when that is 0).
+size_t router_partial_bytes(int T, int h, int E);
 cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, int T, int h, int E,
-                          int k, int32_t* topk_idx, float* gates, int num_sms, cudaStream_t s);
+                          int k, int32_t* topk_idx, float* gates, float* partial, int num_sms,
+                          cudaStream_t s);
 
 // Per-block expert counts [nblk, E] of the assignments.
 cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E, int32_t* blk_counts,
