@@ -51,6 +51,8 @@ def parse():
     # the named workload unchanged)
     p.add_argument("--tokens", type=int, default=0, help="override T")
     p.add_argument("--experts", type=int, default=0, help="override E (k = min(k, E))")
+    # time one step of the path alone (profiling aid; not the bench line)
+    p.add_argument("--stage", default="layer", choices=["layer", "router"])
     return p.parse_args()
 
 
@@ -320,6 +322,39 @@ def blas_threads():
 
 
 # ------------------------------------------------------------------ main ---
+def run_router_stage(args, cfg, peaks):
+    """moe_route alone on the workload's x and router weights (small memory
+    footprint, for profiling the router kernels)."""
+    from routing_grouped_expert_router_gb300 import binding as mb
+    from routing_grouped_expert_router_gb300 import build as mbuild
+    mbuild.build()
+    mb.load()
+    dev = torch.device("cuda", 0)
+    T, h, E, k = cfg.T, cfg.h, cfg.E, cfg.k
+    x = synth.normal(cfg.seed, synth.TID_X, (T, h), 1.0, torch.bfloat16, dev)
+    Wg = synth.normal(cfg.seed, synth.TID_WG, (h, E), h ** -0.5, torch.float32, dev)
+    b = torch.zeros(E, dtype=torch.float32, device=dev)
+    d = mb.dims_of(cfg, has_bias=False)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    gates = torch.empty(T, k, dtype=torch.float32, device=dev)
+    ws = torch.zeros(mb.moe_workspace_bytes(d, mb.OP_ROUTE), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        mb.moe_route(d, x, Wg, b, idx, gates, ws)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(args.steps):
+        mb.moe_route(d, x, Wg, b, idx, gates, ws)
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / args.steps
+    nbytes = metrics.kernel_work(T, h, cfg.f, E, k)["bytes"]["router_topk"]
+    print(json.dumps({"stage": "router", "workload": workload_desc(cfg), "ms": ms,
+                      "gbs": metrics.gbs(nbytes, ms),
+                      "frac_hbm": metrics.gbs(nbytes, ms) / peaks["hbm_gbs"],
+                      "fp32_tflops": 2.0 * T * h * E / (ms * 1e-3) / 1e12}), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -331,6 +366,9 @@ def main():
     peaks, peak_src = load_peaks()
     workload = workload_desc(cfg)
     n = max(args.gpus, world)
+    if args.stage == "router":
+        run_router_stage(args, cfg, peaks)
+        return
 
     if args.impl == "reference":
         if rank != 0:

@@ -34,6 +34,10 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
   return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
 }
 
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 int grid_for(long long warps_needed, int num_sms, int warps_per_block, int blocks_per_sm) {
   long long blocks = (warps_needed + warps_per_block - 1) / warps_per_block;
   long long cap = static_cast<long long>(num_sms) * blocks_per_sm;
@@ -93,22 +97,44 @@ __device__ __forceinline__ void select_topk(const float (&l)[EP], int E, int k, 
   }
 }
 
-// ---- E <= 8: lanes split the columns (8-element slices, 512-byte coalesced
-// x loads per warp); each lane keeps all 8 partial logits of TOK tokens and
-// reads its rows of the weights as conflict-free 16-byte loads from a padded
-// layout (lane l's eight rows are one block + 16 bytes).  A butterfly gives
-// every lane the full logits.
-constexpr int kRouterATok = 8;
-constexpr int kRouterACh = 4096;
+// ---- E <= 8: lanes split the columns (8-element slices); each lane keeps
+// all 8 partial logits of TOK tokens and reads its rows of the weights as
+// conflict-free 16-byte loads from a padded layout (lane l's eight rows are
+// one block + 16 bytes).  x streams through a ring of NSTAGE shared-memory
+// stages filled with cp.async (256 columns of the block's 64 tokens each), so
+// several steps of loads are in flight without holding registers.  A
+// butterfly gives every lane the full logits.
+constexpr int kRouterAThreads = 512;
+constexpr int kRouterATok = 4;                      // tokens per warp
+constexpr int kRouterATile = kRouterAThreads / 32 * kRouterATok;  // tokens per block tile
+constexpr int kRouterACh = 2048;                    // columns per weight chunk
 constexpr int kRouterASlice = 8 * 8 + 4;
-constexpr int kRouterASmem = (kRouterACh / 8) * kRouterASlice * 4;
+constexpr int kRouterAStage = kRouterATile * 256;   // bf16 per x stage (32 KiB)
+constexpr int kRouterANStage = 3;
+constexpr int kRouterASmem =
+    (kRouterACh / 8) * kRouterASlice * 4 + kRouterANStage * kRouterAStage * 2;
 
-__global__ void __launch_bounds__(256, 1) router_a_kernel(
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ Wg, const float* __restrict__ b,
     int T, int h, int E, int k, int nch, int32_t* __restrict__ topk_idx,
     float* __restrict__ gates, float* __restrict__ partial) {
-  constexpr int EP = 8, TOK = kRouterATok, CH = kRouterACh, SLICE = kRouterASlice;
+  constexpr int EP = 8, TOK = kRouterATok, TILE = kRouterATile, CH = kRouterACh;
+  constexpr int SLICE = kRouterASlice, NST = kRouterANStage;
   extern __shared__ float sw[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sw + (CH / 8) * SLICE);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int c = blockIdx.x % nch;
@@ -116,34 +142,57 @@ __global__ void __launch_bounds__(256, 1) router_a_kernel(
   const int bpc = gridDim.x / nch;
   const int c0 = c * CH;
   const int rows = min(CH, h - c0);
-  for (int q = threadIdx.x; q < rows * EP; q += 256) {
+  const int nsteps = (rows + 255) / 256;  // 256-column steps of a tile
+  for (int q = threadIdx.x; q < rows * EP; q += kRouterAThreads) {
     const int lr = q / EP;
     const int e = q - lr * EP;
     sw[(lr >> 3) * SLICE + (lr & 7) * EP + e] =
         (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
   }
-  __syncthreads();
-  const int tile = 8 * TOK;
-  for (int t0 = sub * tile; t0 < T; t0 += bpc * tile) {
-    const int tn = t0 + bpc * tile + static_cast<int>(threadIdx.x);
-    if (static_cast<int>(threadIdx.x) < tile && tn < T)
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                       x + static_cast<size_t>(tn) * h + c0),
-                   "r"(rows * 2)
-                   : "memory");
-    const int tw = t0 + warp * TOK;
-    float acc[TOK][EP];
+  // this block's tiles, flattened with their steps into one stream of stages
+  const int ntiles = (T + TILE - 1) / TILE;
+  const int my_tiles = sub < ntiles ? (ntiles - sub + bpc - 1) / bpc : 0;
+  const int total = my_tiles * nsteps;
+  auto issue = [&](int g) {  // stage g -> ring slot g % NST
+    if (g < total) {
+      const int t0 = (sub + (g / nsteps) * bpc) * TILE;
+      const int cs = (g % nsteps) * 256;
+      const uint32_t base = smem_addr(xs + (g % NST) * kRouterAStage);
 #pragma unroll
-    for (int u = 0; u < TOK; ++u)
+      for (int i = 0; i < TILE * 32 / kRouterAThreads; ++i) {
+        const int id = i * kRouterAThreads + threadIdx.x;
+        const int tok = id >> 5;
+        const int c16 = id & 31;
+        const int t = t0 + tok;
+        const bool ok = t < T && cs + 8 * c16 < rows;
+        const uint16_t* src = ok ? x + static_cast<size_t>(t) * h + c0 + cs + 8 * c16 : x;
+        cp_async16(base + (tok * 256 + 8 * c16) * 2, src, ok);
+      }
+    }
+    cp_async_commit();  // an empty group keeps the group count uniform
+  };
 #pragma unroll
-      for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
-    for (int lc = 8 * lane; lc < rows; lc += 256) {
-      uint4 xq[TOK];
+  for (int g = 0; g < NST - 1; ++g) issue(g);
+  __syncthreads();  // weights staged
+
+  float acc[TOK][EP];
+  for (int g = 0; g < total; ++g) {
+    issue(g + NST - 1);
+    cp_async_wait<NST - 1>();
+    __syncthreads();  // stage g landed for every thread's copies
+    const int step = g % nsteps;
+    if (step == 0) {
 #pragma unroll
       for (int u = 0; u < TOK; ++u)
-        xq[u] = (tw + u < T) ? __ldg(reinterpret_cast<const uint4*>(
-                                   x + static_cast<size_t>(tw + u) * h + c0 + lc))
-                             : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
+    }
+    const int lc = step * 256 + 8 * lane;
+    if (lc < rows) {
+      const uint16_t* xt = xs + (g % NST) * kRouterAStage + (warp * TOK) * 256 + 8 * lane;
+      uint4 xq[TOK];
+#pragma unroll
+      for (int u = 0; u < TOK; ++u) xq[u] = *reinterpret_cast<const uint4*>(xt + u * 256);
       const float4* wb = reinterpret_cast<const float4*>(sw + (lc >> 3) * SLICE);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -166,29 +215,35 @@ __global__ void __launch_bounds__(256, 1) router_a_kernel(
         }
       }
     }
+    __syncthreads();  // stage g's slot may be refilled from the next iteration on
+    if (step == nsteps - 1) {
 #pragma unroll
-    for (int u = 0; u < TOK; ++u)
+      for (int u = 0; u < TOK; ++u)
 #pragma unroll
-      for (int e = 0; e < EP; ++e)
+        for (int e = 0; e < EP; ++e)
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc[u][e] += __shfl_xor_sync(kFull, acc[u][e], off);
+          for (int off = 16; off > 0; off >>= 1)
+            acc[u][e] += __shfl_xor_sync(kFull, acc[u][e], off);
+      const int tw = (sub + (g / nsteps) * bpc) * TILE + warp * TOK;
 #pragma unroll
-    for (int u = 0; u < TOK; ++u) {
-      const int t = tw + u;
-      if (lane != u || t >= T) continue;
-      if (nch == 1) {
-        float l[EP];
+      for (int u = 0; u < TOK; ++u) {
+        const int t = tw + u;
+        if (lane != u || t >= T) continue;
+        if (nch == 1) {
+          float l[EP];
 #pragma unroll
-        for (int e = 0; e < EP; ++e) l[e] = (e < E) ? acc[u][e] + (b ? __ldg(b + e) : 0.f) : 0.f;
-        select_topk<EP>(l, E, k, topk_idx + static_cast<size_t>(t) * k,
-                        gates + static_cast<size_t>(t) * k);
-      } else {
-        float4* dst = reinterpret_cast<float4*>(partial + (static_cast<size_t>(c) * T + t) * EP);
-        dst[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
-        dst[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
+          for (int e = 0; e < EP; ++e) l[e] = (e < E) ? acc[u][e] + (b ? __ldg(b + e) : 0.f) : 0.f;
+          select_topk<EP>(l, E, k, topk_idx + static_cast<size_t>(t) * k,
+                          gates + static_cast<size_t>(t) * k);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(partial + (static_cast<size_t>(c) * T + t) * EP);
+          dst[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+          dst[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
+        }
       }
     }
   }
+  cp_async_wait<0>();
 }
 
 // ---- E > 8: lanes own experts.  A group of GL = min(32, EP) lanes handles
@@ -565,95 +620,120 @@ __global__ void transpose_wg_kernel(const float* __restrict__ Wg, int h, int E,
   }
 }
 
-// Router backward per token + dx.
+// Router backward per token + dx, warp per token (K = k).  U 16-byte pieces of
+// the row per lane per step keep 2 * U * K fp32 loads of dX_perm in flight.
+template <int K>
 __global__ void __launch_bounds__(256) token_grad_kernel(
     const float4* __restrict__ dX, const int32_t* __restrict__ perm_dst,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ gates,
-    const float* __restrict__ dg, const float4* __restrict__ WgT, int T, int k, int h8, int E,
+    const float* __restrict__ dg, const float4* __restrict__ WgT, int T, int h8, int E,
     float* __restrict__ dl, uint4* __restrict__ dx) {
+  constexpr int U = K <= 2 ? 2 : 1;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
+  const long long R = static_cast<long long>(T) * K;
   for (int t = gw; t < T; t += nw) {
-    long long rows[8];
-    int ex[8];
-    float g[8], d[8];
+    long long rows[K];
+    int ex[K];
+    float g[K], d[K];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j < k) {
-        const size_t a = static_cast<size_t>(t) * k + j;
-        const long long r = __ldg(perm_dst + a);
-        rows[j] = r < 0 ? 0 : (r >= static_cast<long long>(T) * k ? static_cast<long long>(T) * k - 1 : r);
-        const int e = __ldg(topk_idx + a);
-        ex[j] = e < 0 ? 0 : (e >= E ? E - 1 : e);
-        g[j] = __ldg(gates + a);
-        d[j] = __ldg(dg + a);
-      }
+    for (int j = 0; j < K; ++j) {
+      const size_t a = static_cast<size_t>(t) * K + j;
+      const long long r = __ldg(perm_dst + a);
+      rows[j] = r < 0 ? 0 : (r >= R ? R - 1 : r);
+      const int e = __ldg(topk_idx + a);
+      ex[j] = e < 0 ? 0 : (e >= E ? E - 1 : e);
+      g[j] = __ldg(gates + a);
+      d[j] = __ldg(dg + a);
     }
     // dl_j = g_j (dg_j - sum_i g_i dg_i), evaluated as g_j sum_i g_i (dg_j - dg_i)
     // (sum_i g_i = 1): no cancellation when one gate is close to 1, and
     // exactly 0 for k = 1.
-    float dlj[8];
+    float dlj[K];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j >= k) break;
+    for (int j = 0; j < K; ++j) {
       float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i < k && i != j) acc = fmaf(g[i], d[j] - d[i], acc);
+      for (int i = 0; i < K; ++i)
+        if (i != j) acc = fmaf(g[i], d[j] - d[i], acc);
       dlj[j] = g[j] * acc;
     }
     for (int e = lane; e < E; e += 32) {
       float v = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < k && ex[j] == e) v = dlj[j];
+      for (int j = 0; j < K; ++j)
+        if (ex[j] == e) v = dlj[j];
       dl[static_cast<size_t>(t) * E + e] = v;
     }
-    for (int c = lane; c < h8; c += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c0 = lane; c0 < h8; c0 += 32 * U) {
+      float4 q[U][K][2];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= k) break;
-        const float4 u0 = __ldg(dX + (rows[j] * h8 + c) * 2);
-        const float4 u1 = __ldg(dX + (rows[j] * h8 + c) * 2 + 1);
-        acc[0] += u0.x; acc[1] += u0.y; acc[2] += u0.z; acc[3] += u0.w;
-        acc[4] += u1.x; acc[5] += u1.y; acc[6] += u1.z; acc[7] += u1.w;
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          if (c < h8) {
+            q[u][j][0] = __ldg(dX + (rows[j] * h8 + c) * 2);
+            q[u][j][1] = __ldg(dX + (rows[j] * h8 + c) * 2 + 1);
+          }
+        }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= k) break;
-        const size_t wo = (static_cast<size_t>(ex[j]) * h8 + c) * 2;
-        const float4 w0 = __ldg(WgT + wo);
-        const float4 w1 = __ldg(WgT + wo + 1);
-        acc[0] = fmaf(dlj[j], w0.x, acc[0]); acc[1] = fmaf(dlj[j], w0.y, acc[1]);
-        acc[2] = fmaf(dlj[j], w0.z, acc[2]); acc[3] = fmaf(dlj[j], w0.w, acc[3]);
-        acc[4] = fmaf(dlj[j], w1.x, acc[4]); acc[5] = fmaf(dlj[j], w1.y, acc[5]);
-        acc[6] = fmaf(dlj[j], w1.z, acc[6]); acc[7] = fmaf(dlj[j], w1.w, acc[7]);
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= h8) break;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          acc[0] += q[u][j][0].x; acc[1] += q[u][j][0].y; acc[2] += q[u][j][0].z; acc[3] += q[u][j][0].w;
+          acc[4] += q[u][j][1].x; acc[5] += q[u][j][1].y; acc[6] += q[u][j][1].z; acc[7] += q[u][j][1].w;
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          const size_t wo = (static_cast<size_t>(ex[j]) * h8 + c) * 2;
+          const float4 w0 = __ldg(WgT + wo);
+          const float4 w1 = __ldg(WgT + wo + 1);
+          acc[0] = fmaf(dlj[j], w0.x, acc[0]); acc[1] = fmaf(dlj[j], w0.y, acc[1]);
+          acc[2] = fmaf(dlj[j], w0.z, acc[2]); acc[3] = fmaf(dlj[j], w0.w, acc[3]);
+          acc[4] = fmaf(dlj[j], w1.x, acc[4]); acc[5] = fmaf(dlj[j], w1.y, acc[5]);
+          acc[6] = fmaf(dlj[j], w1.z, acc[6]); acc[7] = fmaf(dlj[j], w1.w, acc[7]);
+        }
+        dx[static_cast<size_t>(t) * h8 + c] = pack8(acc);
       }
-      dx[static_cast<size_t>(t) * h8 + c] = pack8(acc);
     }
   }
 }
 
-// dWg partials: block (i-tile of 256, token chunk of kWgChunk); thread owns one i
-// and EP experts; dl rows of the chunk are staged in shared memory.
+// dWg partials: block = (column tile, token chunk of kWgChunk); thread owns
+// CPT consecutive columns (2 for E <= 8, so a warp's x loads are whole
+// 128-byte lines) and EP experts; dl rows of the chunk are staged in shared
+// memory.
 constexpr int kWgChunk = 256;
 constexpr int kWgStage = 32;
+
+template <int EP>
+struct WgShape {
+  static constexpr int CPT = EP <= 8 ? 2 : 16 / EP >= 1 ? 16 / EP : 1;  // columns per thread
+  static constexpr int COLS = 256 * CPT;             // columns per block
+};
 
 template <int EP>
 __global__ void __launch_bounds__(256) router_wgrad_kernel(const uint16_t* __restrict__ x,
                                                            const float* __restrict__ dl, int T,
                                                            int h, int E,
                                                            float* __restrict__ partial) {
+  constexpr int CPT = WgShape<EP>::CPT;
   __shared__ float sdl[kWgStage][EP];
-  const int i = blockIdx.x * 256 + threadIdx.x;
+  const int i0 = blockIdx.x * WgShape<EP>::COLS + threadIdx.x * CPT;  // first column
   const int chunk = blockIdx.y;
   const int t0 = chunk * kWgChunk;
   const int t1 = min(T, t0 + kWgChunk);
-  float acc[EP];
+  float acc[CPT][EP];
 #pragma unroll
-  for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+  for (int c = 0; c < CPT; ++c)
+#pragma unroll
+    for (int e = 0; e < EP; ++e) acc[c][e] = 0.f;
   for (int ts = t0; ts < t1; ts += kWgStage) {
     __syncthreads();
     for (int q = threadIdx.x; q < kWgStage * EP; q += 256) {
@@ -662,21 +742,41 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(const uint16_t* __res
       sdl[q / EP][e] = (tt < t1 && e < E) ? dl[static_cast<size_t>(tt) * E + e] : 0.f;
     }
     __syncthreads();
-    if (i < h) {
+    if (i0 < h) {
       const int n = min(kWgStage, t1 - ts);
       for (int u = 0; u < n; ++u) {
-        const float xv = __uint_as_float(static_cast<uint32_t>(x[static_cast<size_t>(ts + u) * h + i])
-                                         << 16);
+        const uint16_t* xr = x + static_cast<size_t>(ts + u) * h + i0;
+        float xv[CPT];
+        if constexpr (CPT == 8) {
+          unpack8(__ldg(reinterpret_cast<const uint4*>(xr)), xv);
+        } else if constexpr (CPT == 4) {
+          const uint2 q = __ldg(reinterpret_cast<const uint2*>(xr));
+          xv[0] = bf16_lo(q.x);
+          xv[1] = bf16_hi(q.x);
+          xv[2] = bf16_lo(q.y);
+          xv[3] = bf16_hi(q.y);
+        } else if constexpr (CPT == 2) {
+          const uint32_t q = __ldg(reinterpret_cast<const uint32_t*>(xr));
+          xv[0] = bf16_lo(q);
+          xv[1] = bf16_hi(q);
+        } else {
+          xv[0] = __uint_as_float(static_cast<uint32_t>(__ldg(xr)) << 16);
+        }
 #pragma unroll
-        for (int e = 0; e < EP; ++e) acc[e] = fmaf(xv, sdl[u][e], acc[e]);
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+          for (int e = 0; e < EP; ++e) acc[c][e] = fmaf(xv[c], sdl[u][e], acc[c][e]);
       }
     }
   }
-  if (i < h) {
-    float* dst = partial + (static_cast<size_t>(chunk) * h + i) * E;
+  if (i0 < h) {
 #pragma unroll
-    for (int e = 0; e < EP; ++e)
-      if (e < E) dst[e] = acc[e];
+    for (int c = 0; c < CPT; ++c) {
+      float* dst = partial + (static_cast<size_t>(chunk) * h + i0 + c) * E;
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (e < E) dst[e] = acc[c][e];
+    }
   }
 }
 
@@ -714,11 +814,11 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
       if (err != cudaSuccess) return err;
       attr = true;
     }
-    const int tiles = (T + 8 * kRouterATok - 1) / (8 * kRouterATok);
+    const int tiles = (T + kRouterATile - 1) / kRouterATile;
     int bpc = num_sms / nch;
     if (bpc < 1) bpc = 1;
     if (bpc > tiles) bpc = tiles;
-    router_a_kernel<<<nch * bpc, 256, kRouterASmem, s>>>(x, Wg, b, T, h, E, k, nch, idx, gates,
+    router_a_kernel<<<nch * bpc, kRouterAThreads, kRouterASmem, s>>>(x, Wg, b, T, h, E, k, nch, idx, gates,
                                                         partial);
     err = cudaGetLastError();
     if (err != cudaSuccess || nch == 1) return err;
@@ -813,10 +913,20 @@ cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
                               uint16_t* dx, int num_sms, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = grid_for(T, num_sms, 8, 16);
-  token_grad_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(dX_perm), perm_dst,
-                                         topk_idx, gates, dg,
-                                         reinterpret_cast<const float4*>(WgT), T, k, h / 8, E, dl,
-                                         reinterpret_cast<uint4*>(dx));
+  const float4* d4 = reinterpret_cast<const float4*>(dX_perm);
+  const float4* w4 = reinterpret_cast<const float4*>(WgT);
+  uint4* o = reinterpret_cast<uint4*>(dx);
+  const int h8 = h / 8;
+  switch (k) {
+    case 1: token_grad_kernel<1><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    case 2: token_grad_kernel<2><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    case 3: token_grad_kernel<3><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    case 4: token_grad_kernel<4><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    case 5: token_grad_kernel<5><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    case 6: token_grad_kernel<6><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    case 7: token_grad_kernel<7><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    default: token_grad_kernel<8><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+  }
   return cudaGetLastError();
 }
 
@@ -826,15 +936,15 @@ cudaError_t launch_router_wgrad(const uint16_t* x, const float* dl, int T, int h
                                 float* partial, float* dWg, cudaStream_t s) {
   const int nchunks = wgrad_router_chunks(T);
   if (nchunks > 0) {
-    dim3 grid((h + 255) / 256, nchunks);
+    auto cols = [&](int c) { return dim3((h + c - 1) / c, nchunks); };
     if (E <= 8)
-      router_wgrad_kernel<8><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+      router_wgrad_kernel<8><<<cols(WgShape<8>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
     else if (E <= 16)
-      router_wgrad_kernel<16><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+      router_wgrad_kernel<16><<<cols(WgShape<16>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
     else if (E <= 32)
-      router_wgrad_kernel<32><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+      router_wgrad_kernel<32><<<cols(WgShape<32>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
     else
-      router_wgrad_kernel<64><<<grid, 256, 0, s>>>(x, dl, T, h, E, partial);
+      router_wgrad_kernel<64><<<cols(WgShape<64>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
