@@ -1,4 +1,5 @@
-"""CPU oracle for one dropless top-k MoE FFN layer with SwiGLU experts.
+"""CPU oracle for one top-k MoE FFN layer with SwiGLU experts (dropless by
+default; optional per-expert capacity and local expert range in dispatch).
 
 TEST INFRASTRUCTURE.  Only the test suite, the package's smoke check and the
 benchmark's CPU-baseline leg may import or run this module.  The CUDA library
@@ -146,21 +147,47 @@ def condition_router_margins(x, Wg, b, k, fresh_rows, margin=1e-3, max_attempts=
 
 # --------------------------------------------------------------- dispatch ---
 
-def dispatch(topk_idx, E):
+def dispatch(topk_idx, E, capacity=None, experts=None):
     """Counts, offsets and the stable expert-major permutation.
 
-    counts[e] = #{a : topk_idx[a] = e};  offsets = exclusive scan, offsets[E] =
-    T*k;  perm_src[p] = the assignment a placed at permuted row p, ordered by
-    expert then by a (so by token);  perm_dst = inverse of perm_src.
-    MegaScale-MoE digest §3.3 (tokens sorted by expert, then by source).
+    Dropless (the defaults): counts[e] = #{a : topk_idx[a] = e};  offsets =
+    exclusive scan, offsets[E] = T*k;  perm_src[p] = the assignment a placed at
+    permuted row p, ordered by expert then by a (so by token);  perm_dst =
+    inverse of perm_src.  MegaScale-MoE digest §3.3 (tokens sorted by expert,
+    then by source).
+
+    experts = (e_lo, e_hi): only assignments to experts e_lo <= e < e_hi are
+    placed, the others are dropped -- the local "scatter & drop" that follows
+    the all-gather of every token (digest §3.2, Diagram B; review §四
+    自适应EP通信策略详解, step 2).  counts and offsets then cover the e_hi - e_lo
+    local experts.
+
+    capacity = C: each expert takes at most C assignments, the first C in
+    assignment order a = t*k + j (earlier tokens first, then slot order); the
+    rest are dropped -- the token dropping used for load balance (digest §3.2,
+    the paragraph after Figure 7; the pages give no drop order, this one is the
+    plainest deterministic choice).  Gates are not renormalised after a drop.
+
+    Returns counts [EL], offsets [EL+1], perm_src [offsets[EL]] (placed rows
+    only) and perm_dst [T*k] with -1 for every dropped assignment.
     """
     flat = np.asarray(topk_idx, dtype=np.int64).ravel()
-    counts = np.bincount(flat, minlength=E).astype(np.int32)
-    offsets = np.zeros(E + 1, dtype=np.int32)
+    e_lo, e_hi = (0, E) if experts is None else (int(experts[0]), int(experts[1]))
+    EL = e_hi - e_lo
+    cap = flat.size if capacity is None else int(capacity)
+    # stable sort by expert: within an expert, ascending a
+    order = np.argsort(flat, kind="stable")
+    full = np.bincount(flat, minlength=E)
+    start = np.zeros(E + 1, dtype=np.int64)
+    start[1:] = np.cumsum(full)
+    counts = np.minimum(full[e_lo:e_hi], cap).astype(np.int32)
+    offsets = np.zeros(EL + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
-    perm_src = np.argsort(flat, kind="stable").astype(np.int32)
-    perm_dst = np.empty_like(perm_src)
-    perm_dst[perm_src] = np.arange(flat.size, dtype=np.int32)
+    perm_src = np.concatenate(
+        [order[start[e]:start[e] + counts[e - e_lo]] for e in range(e_lo, e_hi)]
+        + [np.zeros(0, dtype=np.int64)]).astype(np.int32)
+    perm_dst = np.full(flat.size, -1, dtype=np.int32)
+    perm_dst[perm_src] = np.arange(perm_src.size, dtype=np.int32)
     return counts, offsets, perm_src, perm_dst
 
 
@@ -170,8 +197,14 @@ def permute_rows(x, perm_src, k):
 
 
 def unpermute_rows(rows_perm, perm_dst):
-    """rows_assign[a] = rows_perm[perm_dst[a]] (assignment order a = t*k+j)."""
-    return np.asarray(rows_perm)[np.asarray(perm_dst, dtype=np.int64)]
+    """rows_assign[a] = rows_perm[perm_dst[a]] (assignment order a = t*k+j);
+    a zero row where perm_dst[a] = -1 (a dropped assignment)."""
+    rows_perm = np.asarray(rows_perm)
+    dst = np.asarray(perm_dst, dtype=np.int64)
+    out = np.zeros((dst.size,) + rows_perm.shape[1:], dtype=rows_perm.dtype)
+    kept = dst >= 0
+    out[kept] = rows_perm[dst[kept]]
+    return out
 
 
 # ---------------------------------------------------------------- experts ---
@@ -224,26 +257,29 @@ def expert_ffn_fwd(x_perm, offsets, W1, W3, W2, counter=None):
 
 
 def combine(O, gates, perm_dst, T, k):
-    """y[t] = sum_{j<k} g[t,j] * O[perm_dst[t*k+j]], summed in slot order.
+    """y[t] = sum_{j<k} g[t,j] * O[perm_dst[t*k+j]], summed in slot order; a
+    dropped slot (perm_dst = -1) adds nothing.
     DisagMoE §2.1 (outputs reduced by a weighted sum)."""
     O = np.asarray(O)
     idx = np.asarray(perm_dst, dtype=np.int64).reshape(T, k)
     g = np.asarray(gates, dtype=np.float64).reshape(T, k)
     y = np.zeros((T, O.shape[1]))
     for j in range(k):
-        y += g[:, j:j + 1] * O[idx[:, j]]
+        kept = idx[:, j] >= 0
+        y[kept] += g[kept, j:j + 1] * O[idx[kept, j]]
     return y
 
 
-def layer_fwd(x, Wg, b, W1, W3, W2, k, counter=None):
+def layer_fwd(x, Wg, b, W1, W3, W2, k, counter=None, capacity=None):
     """route -> dispatch -> permute -> expert FFN -> combine.
 
-    Returns y (float64 [T,h]) and a context dict with every intermediate.
+    capacity: see dispatch (None = dropless).  Returns y (float64 [T,h]) and a
+    context dict with every intermediate.
     """
     T = x.shape[0]
     E = Wg.shape[1]
     topk_idx, gates, l64 = route(x, Wg, b, k)
-    counts, offsets, perm_src, perm_dst = dispatch(topk_idx, E)
+    counts, offsets, perm_src, perm_dst = dispatch(topk_idx, E, capacity)
     x64 = as_f64(x)
     x_perm = permute_rows(x64, perm_src, k)
     A, B, H, O = expert_ffn_fwd(x_perm, offsets, W1, W3, W2, counter)
@@ -305,8 +341,9 @@ def router_bwd(gates, dg):
 def layer_bwd(dy, x, Wg, W1, W3, W2, ctx, counter=None):
     """Gradients of L = <dy, y> with respect to x, Wg, W1, W3, W2, plus dg.
 
-    dO[p] = g[a] dy[t];  dg[a] = <dy[t], O[p]>;  expert backward;
-    dx[t] = sum_j dX_perm[perm_dst[t*k+j]] + sum_j dl[t,j] Wg[:, e_j];
+    dO[p] = g[a] dy[t];  dg[a] = <dy[t], O[p]> (0 for a dropped a);  expert
+    backward;  dx[t] = sum_j dX_perm[perm_dst[t*k+j]] (kept slots) +
+    sum_j dl[t,j] Wg[:, e_j];
     dWg = x^T dl  (dl is zero outside each token's k selected experts).
     """
     k = ctx["k"]
@@ -320,7 +357,7 @@ def layer_bwd(dy, x, Wg, W1, W3, W2, ctx, counter=None):
     tok = perm_src // k
     dO = g_flat[perm_src][:, None] * dy64[tok]
     dg_perm = np.einsum("ph,ph->p", dy64[tok], ctx["O"])
-    dg = np.empty(T * k)
+    dg = np.zeros(T * k)          # a dropped slot has no output: dg = 0
     dg[perm_src] = dg_perm
     dg = dg.reshape(T, k)
     ex = expert_ffn_bwd(dO, ctx["x_perm"], ctx["offsets"], W1, W3, W2,
