@@ -1,6 +1,9 @@
 /*
- * moe.h -- C ABI of libmoe_gb300: one dropless top-k Mixture-of-Experts FFN
- * layer with SwiGLU experts, forward and backward, on one GB300 (sm_103a).
+ * moe.h -- C ABI of libmoe_gb300: one top-k Mixture-of-Experts FFN layer with
+ * SwiGLU experts, forward and backward, on one GB300 (sm_103a).  Dropless by
+ * default; optionally with a per-expert capacity (token dropping) and, for the
+ * dispatch step alone, a local expert range (the "scatter & drop" that follows
+ * an all-gather of every token).
  *
  * The layer (sources named by page title and section):
  *   - a trainable gate scores every expert per token; the k experts with the
@@ -11,7 +14,11 @@
  *   - the experts are SwiGLU FFNs run together as one GroupedGEMM, "one kernel
  *     for the matrix products of several experts" (digest, glossary; MegaScale-
  *     MoE paper review, §三 核心公式 and 训练流程);
- *   - forward and backward are explicit operators, not autograd (digest §3.3).
+ *   - forward and backward are explicit operators, not autograd (digest §3.3);
+ *   - load balance may drop tokens per GPU (digest §3.2, the paragraph after
+ *     Figure 7), and the all-gather path of adaptive EP drops, locally, the
+ *     tokens that no local expert takes (digest §3.2, Diagram B; review §四
+ *     自适应EP通信策略详解, step 2).
  *
  * Conventions shared by every entry point
  *   - Pointers named x, Wg, W1 ... and every output are DEVICE pointers owned by
@@ -30,6 +37,13 @@
  *     An assignment a = t*k + j is token t's j-th chosen expert.  A permuted
  *     row p indexes the expert-major order: rows offsets[e] .. offsets[e+1]-1
  *     belong to expert e, in ascending a.
+ *   - Token dropping (dims.capacity = C > 0): expert e takes only its first C
+ *     assignments in ascending a; every other assignment is dropped.  A
+ *     dropped assignment has perm_dst[a] = -1, adds nothing to y and gets no
+ *     gradient through the experts (its gate gradient is 0); the gates are
+ *     not renormalised.  Only the offsets[E] <= T*k placed rows exist: rows
+ *     p >= offsets[E] of the permuted buffers are neither written nor read.
+ *     C = 0 is dropless (offsets[E] = T*k).
  *   - Gradients are written, not accumulated.  An expert that receives no
  *     token gets zero weight gradients.
  *   - Argument errors are found on the host before any launch and returned as
@@ -37,8 +51,10 @@
  *     MOE_ERR_CUDA.  Device code never traps or prints: a kernel whose bounded
  *     wait runs out records MOE_ERR_DEVICE_TIMEOUT in the status word at the
  *     start of `ws` and returns; moe_read_device_status() reports it.
- *   - Supported shapes: 1 <= k <= 8, k <= E <= 64, T*k < 2^31, h and f
- *     multiples of 64 (the GEMMs' K blocks are 64 wide).
+ *   - Supported shapes: 1 <= k <= 8, E <= 64, T*k < 2^31, h and f multiples
+ *     of 64 (the GEMMs' K blocks are 64 wide).  Calls that choose experts
+ *     (moe_route, moe_layer_fwd/bwd, moe_saved_bytes) also need k <= E; the
+ *     others may run on a subset of the experts (E = a local expert count).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -70,6 +86,7 @@ typedef struct {
   int32_t E;         /* experts */
   int32_t k;         /* experts per token */
   int32_t has_bias;  /* 1: router bias b[E] is added to the logits */
+  int32_t capacity;  /* 0: dropless; C > 0: at most C assignments per expert */
 } moe_dims;
 
 typedef enum {
@@ -107,10 +124,11 @@ moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const float* Wg,
  * the scatter that makes each expert's tokens contiguous).  Deterministic,
  * no atomics.
  * In: topk_idx [T,k]; x [T,h] bf16 or NULL.
- * Out: counts [E], offsets [E+1] (offsets[E] = T*k), perm_src [T*k]
- * (permuted row -> assignment), perm_dst [T*k] (assignment -> permuted row),
- * and, when x and x_perm are both non-NULL, x_perm [T*k,h] with
- * x_perm[p] = x[perm_src[p] / k]. */
+ * Out: counts [E], offsets [E+1] (offsets[E] = T*k when dropless), perm_src
+ * [T*k] (permuted row -> assignment; the first offsets[E] entries are
+ * written), perm_dst [T*k] (assignment -> permuted row, -1 if dropped), and,
+ * when x and x_perm are both non-NULL, x_perm [T*k,h] with
+ * x_perm[p] = x[perm_src[p] / k] for p < offsets[E]. */
 moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx,
                        const moe_bf16* x, int32_t* counts, int32_t* offsets,
                        int32_t* perm_src, int32_t* perm_dst, moe_bf16* x_perm,
@@ -132,8 +150,27 @@ moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* topk_idx,
                                int32_t* perm_dst, moe_bf16* x_perm,
                                moe_stream_t stream);
 
-/* Inverse row move: rows_assign[a] = rows_perm[perm_dst[a]] for a < T*k.
- * rows_perm, rows_assign: [T*k, h] bf16. */
+/* The all-gather path's local "scatter & drop" (digest §3.2, Diagram B; review
+ * §四 自适应EP通信策略详解, step 2): given every token's routing, place only the
+ * assignments to the local experts e_lo <= e < e_hi (0 <= e_lo < e_hi <= E),
+ * each expert taking at most dims.capacity of them when that is non-zero.
+ * Same outputs as moe_permute over the EL = e_hi - e_lo local experts:
+ * counts [EL], offsets [EL+1] (local expert i = global e_lo + i), perm_src
+ * [T*k] (first offsets[EL] entries), perm_dst [T*k] (-1 for every assignment
+ * not placed here), x_perm rows p < offsets[EL] when x and x_perm are given.
+ * The local rows then run through moe_expert_ffn_fwd/bwd with dims.E = EL and
+ * the local experts' weights; moe_combine with this perm_dst gives the local
+ * experts' share of y (the partial sum the reduce-scatter adds up).
+ * Workspace: moe_workspace_bytes(dims, MOE_OP_PERMUTE). */
+moe_status moe_permute_local(const moe_dims* dims, const int32_t* topk_idx,
+                             int32_t e_lo, int32_t e_hi, const moe_bf16* x,
+                             int32_t* counts, int32_t* offsets,
+                             int32_t* perm_src, int32_t* perm_dst,
+                             moe_bf16* x_perm, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/* Inverse row move: rows_assign[a] = rows_perm[perm_dst[a]] for a < T*k, a
+ * zero row where perm_dst[a] = -1.  rows_perm, rows_assign: [T*k, h] bf16. */
 moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst,
                          const moe_bf16* rows_perm, moe_bf16* rows_assign,
                          moe_stream_t stream);
@@ -143,7 +180,8 @@ moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst,
  *   A = X W1[e],  B = X W3[e],  H = silu(A) * B,  O = H W2[e]
  * (review §三 核心公式: SwiGLU with MoE, 3k*bsh*h_ffn multiply-adds).
  * bf16 operands, fp32 accumulation in tensor memory; A, B, H, O stored bf16
- * [T*k, f] / [T*k, h].  offsets is read on the device only. */
+ * [T*k, f] / [T*k, h], rows p < offsets[E] only.  offsets is read on the
+ * device only. */
 moe_status moe_expert_ffn_fwd(const moe_dims* dims, const moe_bf16* x,
                               const int32_t* perm_src, const int32_t* offsets,
                               const moe_bf16* W1, const moe_bf16* W3,
@@ -152,8 +190,9 @@ moe_status moe_expert_ffn_fwd(const moe_dims* dims, const moe_bf16* x,
                               void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Gate-weighted combine: y[t] = sum_{j<k} gates[t,j] * O[perm_dst[t*k+j]],
- * summed in fp32 in slot order, rounded once to bf16.  Deterministic (a
- * gather, no scatter-add).  DisagMoE §2.1 (weighted sum). */
+ * summed in fp32 in slot order, rounded once to bf16; slots with
+ * perm_dst = -1 are skipped.  Deterministic (a gather, no scatter-add).
+ * DisagMoE §2.1 (weighted sum). */
 moe_status moe_combine(const moe_dims* dims, const moe_bf16* O,
                        const float* gates, const int32_t* perm_dst,
                        moe_bf16* y, moe_stream_t stream);
@@ -166,7 +205,9 @@ moe_status moe_combine(const moe_dims* dims, const moe_bf16* O,
  *   dW2[e] = H_e^T dO_e ; dW1[e] = X_e^T dA_e ; dW3[e] = X_e^T dB_e
  *   dX_perm = dA W1[e]^T + dB W3[e]^T          (fp32 [T*k, h])
  * FC2's gradients take fc2_in = H and the gradient of fc2_out (review
- * 选择性激活重计算).  A, B, H, O are moe_expert_ffn_fwd's outputs. */
+ * 选择性激活重计算).  A, B, H, O are moe_expert_ffn_fwd's outputs.  Rows
+ * p < offsets[E] only: dg[a] is written for the placed assignments
+ * a = perm_src[p] alone, and so are the dX_perm rows. */
 moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x,
                               const moe_bf16* dy, const float* gates,
                               const int32_t* perm_src, const int32_t* offsets,
@@ -183,7 +224,8 @@ moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x,
  *   dx[t]   = sum_j dX_perm[perm_dst[t*k+j]] + sum_j dl[t,j] Wg[:, e_j]  (bf16)
  *   dWg     = x^T dl (fp32 [h,E]; a fixed-order two-level reduction)
  * In: x, Wg, topk_idx, gates, dg [T*k], dX_perm [T*k,h] fp32, perm_src,
- * perm_dst, offsets. */
+ * perm_dst, offsets.  A slot with perm_dst = -1 counts with dg = 0 and adds
+ * no dX_perm row. */
 moe_status moe_router_bwd(const moe_dims* dims, const moe_bf16* x,
                           const float* Wg, const int32_t* topk_idx,
                           const float* gates, const float* dg,

@@ -9,6 +9,7 @@ library is absent: there is no fallback path.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import re
 
@@ -35,16 +36,23 @@ class MoeError(RuntimeError):
 
 class moe_dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("h", ctypes.c_int32), ("f", ctypes.c_int32),
-                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("has_bias", ctypes.c_int32)]
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("has_bias", ctypes.c_int32),
+                ("capacity", ctypes.c_int32)]
 
 
-def dims(T, h, f, E, k, has_bias=False) -> moe_dims:
-    return moe_dims(int(T), int(h), int(f), int(E), int(k), int(bool(has_bias)))
+def dims(T, h, f, E, k, has_bias=False, capacity=0) -> moe_dims:
+    return moe_dims(int(T), int(h), int(f), int(E), int(k), int(bool(has_bias)), int(capacity))
 
 
-def dims_of(cfg, has_bias=None) -> moe_dims:
+def dims_of(cfg, has_bias=None, capacity=0) -> moe_dims:
     hb = cfg.zipf_s > 0 if has_bias is None else has_bias
-    return dims(cfg.T, cfg.h, cfg.f, cfg.E, cfg.k, hb)
+    return dims(cfg.T, cfg.h, cfg.f, cfg.E, cfg.k, hb, capacity)
+
+
+def capacity_for(T, k, E, factor: float) -> int:
+    """Per-expert capacity ceil(factor * T * k / E): factor 1.0 is the share an
+    expert gets under perfect balance."""
+    return int(math.ceil(factor * T * k / E))
 
 
 _LIB = None
@@ -59,6 +67,8 @@ _SIGS = {
     "moe_route": (_I, [_D, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_permute_local": (_I, [_D, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
+                               _P, _SZ, _P]),
     "moe_unpermute": (_I, [_D, _P, _P, _P, _P]),
     "moe_expert_ffn_fwd": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_D, _P, _P, _P, _P, _P]),
@@ -167,6 +177,15 @@ def moe_permute_noalloc(d, topk_idx, x, counts, offsets, perm_src, perm_dst, x_p
     _check(load().moe_permute_noalloc(ctypes.byref(d), _addr(topk_idx), _addr(x), _addr(counts),
                                       _addr(offsets), _addr(perm_src), _addr(perm_dst),
                                       _addr(x_perm), _stream(stream)), "moe_permute_noalloc")
+
+
+def moe_permute_local(d, topk_idx, e_lo, e_hi, x, counts, offsets, perm_src, perm_dst, x_perm,
+                      ws, ws_bytes=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_permute_local(ctypes.byref(d), _addr(topk_idx), int(e_lo), int(e_hi),
+                                    _addr(x), _addr(counts), _addr(offsets), _addr(perm_src),
+                                    _addr(perm_dst), _addr(x_perm), _addr(ws), ws_bytes,
+                                    _stream(stream)), "moe_permute_local")
 
 
 def moe_unpermute(d, perm_dst, rows_perm, rows_assign, stream=None):

@@ -6,6 +6,7 @@
 // synchronises except moe_read_device_status.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 #include <cstring>
 
@@ -44,14 +45,21 @@ bool buf_ok(const void* p, size_t bytes) {
   return bytes == 0 ? (p == nullptr || aligned(p, 16)) : ptr_ok(p);
 }
 
-moe_status check_dims(const moe_dims* d) {
+// `routed`: the call selects k distinct experts per token, so k <= E.  Calls
+// that only move or transform already-routed rows also take a subset of the
+// experts (E = the local experts of moe_permute_local), where k may exceed E.
+moe_status check_dims(const moe_dims* d, bool routed) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->T < 0 || d->h <= 0 || d->f <= 0 || d->E <= 0 || d->k <= 0) return MOE_ERR_INVALID_ARG;
-  if (d->k > d->E) return MOE_ERR_INVALID_ARG;
+  if ((routed && d->k > d->E) || d->capacity < 0) return MOE_ERR_INVALID_ARG;
   if (d->k > 8 || d->E > moe::kRouterMaxE) return MOE_ERR_UNSUPPORTED;
   if (d->h % 64 != 0 || d->f % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(d->T) * d->k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+bool routed_op(int op) {
+  return op == MOE_OP_ROUTE || op == MOE_OP_LAYER_FWD || op == MOE_OP_LAYER_BWD;
 }
 
 int num_sms() {
@@ -200,17 +208,23 @@ moe_status do_route(const moe_dims& d, const uint16_t* x, const float* Wg, const
   return MOE_OK;
 }
 
-moe_status do_dispatch(const moe_dims& d, const int32_t* idx, int32_t* counts, int32_t* offsets,
-                       int32_t* psrc, int32_t* pdst, void* ws, const WsLayout& L,
-                       cudaStream_t stream) {
+// Experts [e_lo, e_hi) of the layer, each taking at most d.capacity
+// assignments (all of them when capacity is 0).
+moe::DispatchSel selection(const moe_dims& d, int e_lo, int e_hi) {
+  return moe::DispatchSel{e_lo, e_hi - e_lo, d.capacity > 0 ? d.capacity : INT_MAX};
+}
+
+moe_status do_dispatch(const moe_dims& d, const moe::DispatchSel& sel, const int32_t* idx,
+                       int32_t* counts, int32_t* offsets, int32_t* psrc, int32_t* pdst, void* ws,
+                       const WsLayout& L, cudaStream_t stream) {
   const long long R = static_cast<long long>(rows_of(d));
   const int nblk = moe::dispatch_blocks(R);
   int32_t* blk = at<int32_t>(ws, L.blk_counts);
   int32_t* bases = at<int32_t>(ws, L.bases);
-  MOE_RUN(moe::launch_dispatch_hist(idx, R, d.E, blk, stream), "dispatch_hist");
-  MOE_RUN(moe::launch_dispatch_scan(blk, nblk, d.E, counts, offsets, bases, stream),
+  MOE_RUN(moe::launch_dispatch_hist(idx, R, d.E, sel, blk, stream), "dispatch_hist");
+  MOE_RUN(moe::launch_dispatch_scan(blk, nblk, sel, counts, offsets, bases, stream),
           "dispatch_scan");
-  MOE_RUN(moe::launch_dispatch_scatter(idx, R, d.E, bases, psrc, pdst, stream),
+  MOE_RUN(moe::launch_dispatch_scatter(idx, R, d.E, sel, bases, offsets, psrc, pdst, stream),
           "dispatch_scatter");
   return MOE_OK;
 }
@@ -280,17 +294,17 @@ const char* moe_status_string(moe_status s) {
 const char* moe_version(void) { return "libmoe_gb300 0.1 (sm_103a, tcgen05 GroupedGEMM)"; }
 
 size_t moe_workspace_bytes(const moe_dims* dims, int op) {
-  if (check_dims(dims) != MOE_OK) return 0;
+  if (check_dims(dims, routed_op(op)) != MOE_OK) return 0;
   return ws_layout(*dims, op).total;
 }
 
 size_t moe_saved_bytes(const moe_dims* dims) {
-  if (check_dims(dims) != MOE_OK) return 0;
+  if (check_dims(dims, true) != MOE_OK) return 0;
   return saved_layout(*dims).total;
 }
 
 void* moe_saved_view(const moe_dims* dims, void* saved, const char* name) {
-  if (check_dims(dims) != MOE_OK || !saved || !name) return nullptr;
+  if (check_dims(dims, true) != MOE_OK || !saved || !name) return nullptr;
   const SavedLayout L = saved_layout(*dims);
   struct {
     const char* n;
@@ -336,7 +350,7 @@ moe_status moe_clear_device_status(void* ws, moe_stream_t stream) {
 moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const float* Wg, const float* b,
                      int32_t* topk_idx, float* gates, void* ws, size_t ws_bytes,
                      moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, true);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t T = d.T, R = rows_of(d);
@@ -351,7 +365,7 @@ moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const float* Wg, c
 moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const moe_bf16* x,
                        int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* perm_dst,
                        moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, false);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t R = rows_of(d);
@@ -362,18 +376,45 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const moe_
   if ((st = ws_check(d, MOE_OP_PERMUTE, ws, ws_bytes)) != MOE_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const WsLayout L = ws_layout(d, MOE_OP_PERMUTE);
-  if ((st = do_dispatch(d, topk_idx, counts, offsets, perm_src, perm_dst, ws, L, stream)) != MOE_OK)
+  if ((st = do_dispatch(d, selection(d, 0, d.E), topk_idx, counts, offsets, perm_src, perm_dst,
+                        ws, L, stream)) != MOE_OK)
     return st;
   if (x && x_perm)
     MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(rows_of(d)), d.T,
-                                    d.h, x_perm, num_sms(), stream),
+                                    d.h, x_perm, num_sms(), stream, offsets + d.E),
+            "permute_rows");
+  return MOE_OK;
+}
+
+moe_status moe_permute_local(const moe_dims* dims, const int32_t* topk_idx, int32_t e_lo,
+                             int32_t e_hi, const moe_bf16* x, int32_t* counts, int32_t* offsets,
+                             int32_t* perm_src, int32_t* perm_dst, moe_bf16* x_perm, void* ws,
+                             size_t ws_bytes, moe_stream_t stream_) {
+  moe_status st = check_dims(dims, false);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (e_lo < 0 || e_hi <= e_lo || e_hi > d.E) return MOE_ERR_INVALID_ARG;
+  const size_t R = rows_of(d);
+  if (!buf_ok(topk_idx, R) || !ptr_ok(counts) || !ptr_ok(offsets) || !buf_ok(perm_src, R) ||
+      !buf_ok(perm_dst, R))
+    return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned(x, 16)) || (x_perm && !aligned(x_perm, 16))) return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_PERMUTE, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_PERMUTE);
+  if ((st = do_dispatch(d, selection(d, e_lo, e_hi), topk_idx, counts, offsets, perm_src,
+                        perm_dst, ws, L, stream)) != MOE_OK)
+    return st;
+  if (x && x_perm)
+    MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(R), d.T, d.h, x_perm,
+                                    num_sms(), stream, offsets + (e_hi - e_lo)),
             "permute_rows");
   return MOE_OK;
 }
 
 moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst, const moe_bf16* rows_perm,
                          moe_bf16* rows_assign, moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, false);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t R = rows_of(d);
@@ -391,7 +432,7 @@ moe_status moe_expert_ffn_fwd(const moe_dims* dims, const moe_bf16* x, const int
                               const int32_t* offsets, const moe_bf16* W1, const moe_bf16* W3,
                               const moe_bf16* W2, moe_bf16* A, moe_bf16* B, moe_bf16* H,
                               moe_bf16* O, void* ws, size_t ws_bytes, moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, false);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t T = d.T, R = rows_of(d);
@@ -403,14 +444,14 @@ moe_status moe_expert_ffn_fwd(const moe_dims* dims, const moe_bf16* x, const int
   const WsLayout L = ws_layout(d, MOE_OP_EXPERT_FFN_FWD);
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
   MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(rows_of(d)), d.T, d.h,
-                                  xp, num_sms(), stream),
+                                  xp, num_sms(), stream, offsets + d.E),
           "permute_rows");
   return do_ffn_fwd(d, xp, offsets, W1, W3, W2, A, B, H, O, ws, stream);
 }
 
 moe_status moe_combine(const moe_dims* dims, const moe_bf16* O, const float* gates,
                        const int32_t* perm_dst, moe_bf16* y, moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, false);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t T = d.T, R = rows_of(d);
@@ -428,7 +469,7 @@ moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x, const moe
                               const moe_bf16* O, float* dX_perm, float* dg, float* dW1,
                               float* dW3, float* dW2, void* ws, size_t ws_bytes,
                               moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, false);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t T = d.T, R = rows_of(d);
@@ -443,9 +484,11 @@ moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x, const moe
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
   uint16_t* dO = at<uint16_t>(ws, L.dO);
   const long long nrows = static_cast<long long>(R);
-  MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, nrows, d.T, d.h, xp, num_sms(), stream),
+  MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, nrows, d.T, d.h, xp, num_sms(), stream,
+                                  offsets + d.E),
           "permute_rows");
-  MOE_RUN(moe::launch_bwd_prep(dy, O, gates, perm_src, nrows, d.k, d.h, dO, dg, num_sms(), stream),
+  MOE_RUN(moe::launch_bwd_prep(dy, O, gates, perm_src, nrows, d.k, d.h, dO, dg, num_sms(), stream,
+                               offsets + d.E),
           "bwd_prep");
   return do_ffn_bwd(d, xp, dO, offsets, W1, W3, W2, A, B, H, at<uint16_t>(ws, L.dA),
                     at<uint16_t>(ws, L.dB), dX_perm, dW1, dW3, dW2, ws, stream);
@@ -456,7 +499,7 @@ moe_status moe_router_bwd(const moe_dims* dims, const moe_bf16* x, const float* 
                           const float* dX_perm, const int32_t* perm_src, const int32_t* perm_dst,
                           const int32_t* offsets, moe_bf16* dx, float* dWg, void* ws,
                           size_t ws_bytes, moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, false);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t T = d.T, R = rows_of(d);
@@ -473,7 +516,7 @@ moe_status moe_router_bwd(const moe_dims* dims, const moe_bf16* x, const float* 
 moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* Wg, const float* b,
                          const moe_bf16* W1, const moe_bf16* W3, const moe_bf16* W2, moe_bf16* y,
                          void* saved, void* ws, size_t ws_bytes, moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, true);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t T = d.T;
@@ -492,11 +535,11 @@ moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* W
   uint16_t* xp = at<uint16_t>(saved, S.x_perm);
   uint16_t* O = at<uint16_t>(saved, S.O);
   if ((st = do_route(d, x, Wg, b, idx, gates, ws, L, stream)) != MOE_OK) return st;
-  if ((st = do_dispatch(d, idx, at<int32_t>(saved, S.counts), offsets, psrc, pdst, ws, L,
-                        stream)) != MOE_OK)
+  if ((st = do_dispatch(d, selection(d, 0, d.E), idx, at<int32_t>(saved, S.counts), offsets, psrc,
+                        pdst, ws, L, stream)) != MOE_OK)
     return st;
   MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, static_cast<long long>(rows_of(d)), d.T, d.h, xp,
-                                  num_sms(), stream),
+                                  num_sms(), stream, offsets + d.E),
           "permute_rows");
   if ((st = do_ffn_fwd(d, xp, offsets, W1, W3, W2, at<uint16_t>(saved, S.A),
                        at<uint16_t>(saved, S.B), at<uint16_t>(saved, S.H), O, ws, stream)) != MOE_OK)
@@ -510,7 +553,7 @@ moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16
                          const moe_bf16* W2, const void* saved, moe_bf16* dx, float* dWg,
                          float* dW1, float* dW3, float* dW2, void* ws, size_t ws_bytes,
                          moe_stream_t stream_) {
-  moe_status st = check_dims(dims);
+  moe_status st = check_dims(dims, true);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   const size_t T = d.T;
@@ -532,7 +575,7 @@ moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16
   float* dg = at<float>(ws, L.dg);
   const long long R = static_cast<long long>(rows_of(d));
   MOE_RUN(moe::launch_bwd_prep(dy, at<uint16_t>(saved, S.O), gates, psrc, R, d.k, d.h, dO, dg,
-                               num_sms(), stream),
+                               num_sms(), stream, offsets + d.E),
           "bwd_prep");
   if ((st = do_ffn_bwd(d, at<uint16_t>(saved, S.x_perm), dO, offsets, W1, W3, W2,
                        at<uint16_t>(saved, S.A), at<uint16_t>(saved, S.B),

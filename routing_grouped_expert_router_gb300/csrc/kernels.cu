@@ -418,17 +418,21 @@ cudaError_t router_select_launch(const float* partial, int nch, const float* b, 
 // A block takes kDispatchChunk consecutive assignments in four rounds of 256.
 // Within a round a warp groups equal experts with __match_any_sync; the
 // group's lowest lane records the group size.  The stable rank of an
-// assignment inside its block is then
-//   running[e] (earlier rounds) + sizes of earlier warps (this round)
-//   + lanes below it in its own group.
+// assignment among its expert's assignments is then
+//   bases[block][e] (earlier blocks) + running[e] (earlier rounds)
+//   + sizes of earlier warps (this round) + lanes below it in its own group.
+// An assignment is kept when its expert lies in the local range
+// [e_lo, e_lo + EL) and its rank is below `cap`; kept ones go to permuted row
+// offsets[e] + rank, the others get perm_dst = -1.
 constexpr int kDispThreads = 256;
 constexpr int kDispWarps = kDispThreads / 32;
 constexpr int kDispMaxE = 256;
 
 template <bool WRITE>
 __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
-    const int32_t* __restrict__ topk_idx, long long n, int E, int32_t* __restrict__ blk_counts,
-    const int32_t* __restrict__ bases, int32_t* __restrict__ perm_src,
+    const int32_t* __restrict__ topk_idx, long long n, int E, int e_lo, int EL, int cap,
+    int32_t* __restrict__ blk_counts, const int32_t* __restrict__ bases,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
     int32_t* __restrict__ perm_dst) {
   __shared__ int running[kDispMaxE];
   __shared__ int wc[kDispWarps][kDispMaxE];
@@ -436,31 +440,35 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const long long base = static_cast<long long>(blockIdx.x) * kDispatchChunk;
-  for (int e = tid; e < E; e += kDispThreads) running[e] = 0;
+  for (int e = tid; e < EL; e += kDispThreads) running[e] = 0;
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int r = 0; r < kDispatchChunk / kDispThreads; ++r) {
-    for (int i = tid; i < kDispWarps * E; i += kDispThreads) wc[i / E][i % E] = 0;
+    for (int i = tid; i < kDispWarps * EL; i += kDispThreads) wc[i / EL][i % EL] = 0;
     __syncthreads();
     const long long a = base + r * kDispThreads + tid;
     const bool valid = a < n;
-    int e = -1;
+    int le = -1;  // local expert, -1 = not placed
     if (valid) {
-      e = __ldg(topk_idx + a);
+      int e = __ldg(topk_idx + a);
       e = e < 0 ? 0 : (e >= E ? E - 1 : e);  // keep every index in range
+      le = (e >= e_lo && e < e_lo + EL) ? e - e_lo : -1;
     }
-    const unsigned grp = __match_any_sync(kFull, e);
+    const unsigned grp = __match_any_sync(kFull, le);
     const int lrank = __popc(grp & lt_mask);
-    if (valid && lrank == 0) wc[warp][e] = __popc(grp);
+    if (le >= 0 && lrank == 0) wc[warp][le] = __popc(grp);
     __syncthreads();
     if (valid && WRITE) {
-      int rank = running[e] + lrank;
-      for (int w = 0; w < warp; ++w) rank += wc[w][e];
-      const int dst = __ldg(bases + static_cast<size_t>(blockIdx.x) * E + e) + rank;
+      int dst = -1;
+      if (le >= 0) {
+        int rank = __ldg(bases + static_cast<size_t>(blockIdx.x) * EL + le) + running[le] + lrank;
+        for (int w = 0; w < warp; ++w) rank += wc[w][le];
+        if (rank < cap) dst = __ldg(offsets + le) + rank;
+      }
       perm_dst[a] = dst;
-      perm_src[dst] = static_cast<int32_t>(a);
+      if (dst >= 0) perm_src[dst] = static_cast<int32_t>(a);
     }
     __syncthreads();
-    for (int ee = tid; ee < E; ee += kDispThreads) {
+    for (int ee = tid; ee < EL; ee += kDispThreads) {
       int add = 0;
       for (int w = 0; w < kDispWarps; ++w) add += wc[w][ee];
       running[ee] += add;
@@ -468,58 +476,66 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
   }
   if (!WRITE) {
     __syncthreads();
-    for (int e = tid; e < E; e += kDispThreads)
-      blk_counts[static_cast<size_t>(blockIdx.x) * E + e] = running[e];
+    for (int e = tid; e < EL; e += kDispThreads)
+      blk_counts[static_cast<size_t>(blockIdx.x) * EL + e] = running[e];
   }
 }
 
+// counts[e] = min(assignments of e, cap); offsets = exclusive scan of counts;
+// bases[b][e] = assignments of e in blocks before b (ranks, not rows).
 __global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t* __restrict__ blk_counts,
-                                                            int nblk, int E,
+                                                            int nblk, int EL, int cap,
                                                             int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ bases) {
   __shared__ int tot[kDispMaxE + 1];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  for (int e = threadIdx.x; e < EL; e += blockDim.x) {
     int s = 0;
-    for (int bk = 0; bk < nblk; ++bk) s += blk_counts[static_cast<size_t>(bk) * E + e];
+    for (int bk = 0; bk < nblk; ++bk) {
+      bases[static_cast<size_t>(bk) * EL + e] = s;
+      s += blk_counts[static_cast<size_t>(bk) * EL + e];
+    }
+    s = s < cap ? s : cap;
     tot[e] = s;
     counts[e] = s;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int run = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = tot[e];
-      tot[e] = run;
+    for (int e = 0; e < EL; ++e) {
       offsets[e] = run;
-      run += c;
+      run += tot[e];
     }
-    offsets[E] = run;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = tot[e];
-    for (int bk = 0; bk < nblk; ++bk) {
-      bases[static_cast<size_t>(bk) * E + e] = run;
-      run += blk_counts[static_cast<size_t>(bk) * E + e];
-    }
+    offsets[EL] = run;
   }
 }
 
 // --------------------------------------------------------------- row moves
 // Warp per row, 16-byte pieces.
+// Rows p < *nvalid (all `rows` when nvalid is NULL); a negative index gives a
+// zero row.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ in,
                                                           const int32_t* __restrict__ idx, int div,
                                                           long long rows, long long src_rows,
+                                                          const int32_t* __restrict__ nvalid,
                                                           int h8, uint4* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  if (nvalid) {
+    const long long nv = __ldg(nvalid);
+    rows = nv < rows ? (nv < 0 ? 0 : nv) : rows;
+  }
   for (long long p = gw; p < rows; p += nw) {
-    long long src = __ldg(idx + p) / div;
-    src = src < 0 ? 0 : (src >= src_rows ? src_rows - 1 : src);  // stay inside `in`
-    const uint4* s = in + src * h8;
+    const long long i = __ldg(idx + p);
     uint4* d = out + p * h8;
+    if (i < 0) {
+      for (int c = lane; c < h8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    long long src = i / div;
+    src = src >= src_rows ? src_rows - 1 : src;  // stay inside `in`
+    const uint4* s = in + src * h8;
 #pragma unroll 4
     for (int c = lane; c < h8; c += 32) d[c] = __ldg(s + c);
   }
@@ -537,13 +553,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   const int nw = (gridDim.x * blockDim.x) >> 5;
   for (int t = gw; t < T; t += nw) {
     long long rows[K];
+    bool kept[K];
     float g[K];
 #pragma unroll
     for (int j = 0; j < K; ++j) {
       {
         const long long r = __ldg(perm_dst + static_cast<size_t>(t) * k + j);
+        // a dropped slot (r < 0) adds nothing and reads no row
+        kept[j] = r >= 0;
         rows[j] = r < 0 ? 0 : (r >= static_cast<long long>(T) * k ? static_cast<long long>(T) * k - 1 : r);
-        g[j] = __ldg(gates + static_cast<size_t>(t) * k + j);
+        g[j] = r < 0 ? 0.f : __ldg(gates + static_cast<size_t>(t) * k + j);
       }
     }
     // four 16-byte pieces per lane per step: 4 * k loads in flight
@@ -554,7 +573,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         const int c = c0 + 32 * u;
 #pragma unroll
         for (int j = 0; j < K; ++j)
-          if (c < h8) q[u][j] = __ldg(O + rows[j] * h8 + c);
+          q[u][j] = (c < h8 && kept[j]) ? __ldg(O + rows[j] * h8 + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -579,15 +598,21 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
                                                        const uint4* __restrict__ O,
                                                        const float* __restrict__ gates,
                                                        const int32_t* __restrict__ perm_src,
-                                                       long long rows, int k, int h8,
-                                                       uint4* __restrict__ dO,
+                                                       long long rows,
+                                                       const int32_t* __restrict__ nvalid, int k,
+                                                       int h8, uint4* __restrict__ dO,
                                                        float* __restrict__ dg) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const long long total = rows;
+  if (nvalid) {
+    const long long nv = __ldg(nvalid);
+    rows = nv < rows ? (nv < 0 ? 0 : nv) : rows;
+  }
   for (long long p = gw; p < rows; p += nw) {
     int a = __ldg(perm_src + p);
-    a = a < 0 ? 0 : (a >= rows ? static_cast<int>(rows - 1) : a);
+    a = a < 0 ? 0 : (a >= total ? static_cast<int>(total - 1) : a);
     const long long t = a / k;
     const float g = __ldg(gates + a);
     float dot = 0.f;
@@ -636,16 +661,18 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
   for (int t = gw; t < T; t += nw) {
     long long rows[K];
     int ex[K];
+    bool kept[K];
     float g[K], d[K];
 #pragma unroll
     for (int j = 0; j < K; ++j) {
       const size_t a = static_cast<size_t>(t) * K + j;
       const long long r = __ldg(perm_dst + a);
+      kept[j] = r >= 0;  // a dropped slot has no expert output: dg = 0, no dX
       rows[j] = r < 0 ? 0 : (r >= R ? R - 1 : r);
       const int e = __ldg(topk_idx + a);
       ex[j] = e < 0 ? 0 : (e >= E ? E - 1 : e);
       g[j] = __ldg(gates + a);
-      d[j] = __ldg(dg + a);
+      d[j] = kept[j] ? __ldg(dg + a) : 0.f;
     }
     // dl_j = g_j (dg_j - sum_i g_i dg_i), evaluated as g_j sum_i g_i (dg_j - dg_i)
     // (sum_i g_i = 1): no cancellation when one gate is close to 1, and
@@ -673,9 +700,12 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
         const int c = c0 + 32 * u;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
-          if (c < h8) {
+          if (c < h8 && kept[j]) {
             q[u][j][0] = __ldg(dX + (rows[j] * h8 + c) * 2);
             q[u][j][1] = __ldg(dX + (rows[j] * h8 + c) * 2 + 1);
+          } else {
+            q[u][j][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            q[u][j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
       }
@@ -834,38 +864,43 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
 }
 
 
-cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E, int32_t* blk_counts,
-                                 cudaStream_t s) {
+cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E,
+                                 const DispatchSel& sel, int32_t* blk_counts, cudaStream_t s) {
   const int nblk = dispatch_blocks(n);
   if (nblk == 0) return cudaSuccess;
-  dispatch_kernel<false><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, blk_counts, nullptr,
+  dispatch_kernel<false><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, sel.e_lo, sel.count,
+                                                        sel.capacity, blk_counts, nullptr, nullptr,
                                                         nullptr, nullptr);
   return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* counts,
-                                 int32_t* offsets, int32_t* bases, cudaStream_t s) {
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(blk_counts, nblk, E, counts, offsets, bases);
+cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, const DispatchSel& sel,
+                                 int32_t* counts, int32_t* offsets, int32_t* bases,
+                                 cudaStream_t s) {
+  dispatch_scan_kernel<<<1, 256, 0, s>>>(blk_counts, nblk, sel.count, sel.capacity, counts,
+                                         offsets, bases);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
-                                    const int32_t* bases, int32_t* perm_src, int32_t* perm_dst,
+                                    const DispatchSel& sel, const int32_t* bases,
+                                    const int32_t* offsets, int32_t* perm_src, int32_t* perm_dst,
                                     cudaStream_t s) {
   const int nblk = dispatch_blocks(n);
   if (nblk == 0) return cudaSuccess;
-  dispatch_kernel<true><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, nullptr, bases, perm_src,
-                                                       perm_dst);
+  dispatch_kernel<true><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, sel.e_lo, sel.count,
+                                                       sel.capacity, nullptr, bases, offsets,
+                                                       perm_src, perm_dst);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                                long long src_rows, int h, uint16_t* out, int num_sms,
-                               cudaStream_t s) {
+                               cudaStream_t s, const int32_t* nvalid) {
   if (rows == 0 || src_rows == 0) return cudaSuccess;
   const int grid = grid_for(rows, num_sms, 8, 16);
   gather_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(in), idx, div, rows,
-                                          src_rows, h / 8, reinterpret_cast<uint4*>(out));
+                                          src_rows, nvalid, h / 8, reinterpret_cast<uint4*>(out));
   return cudaGetLastError();
 }
 
@@ -890,12 +925,12 @@ cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t*
 
 cudaError_t launch_bwd_prep(const uint16_t* dy, const uint16_t* O, const float* gates,
                             const int32_t* perm_src, long long rows, int k, int h, uint16_t* dO,
-                            float* dg, int num_sms, cudaStream_t s) {
+                            float* dg, int num_sms, cudaStream_t s, const int32_t* nvalid) {
   if (rows == 0) return cudaSuccess;
   const int grid = grid_for(rows, num_sms, 8, 16);
   bwd_prep_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(dy),
-                                       reinterpret_cast<const uint4*>(O), gates, perm_src, rows, k,
-                                       h / 8, reinterpret_cast<uint4*>(dO), dg);
+                                       reinterpret_cast<const uint4*>(O), gates, perm_src, rows,
+                                       nvalid, k, h / 8, reinterpret_cast<uint4*>(dO), dg);
   return cudaGetLastError();
 }
 

@@ -21,22 +21,33 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
                           int k, int32_t* topk_idx, float* gates, float* partial, int num_sms,
                           cudaStream_t s);
 
-// Per-block expert counts [nblk, E] of the assignments.
-cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E, int32_t* blk_counts,
+// Which assignments dispatch keeps: experts [e_lo, e_lo + count) and at most
+// `capacity` per expert (in assignment order).  Dropless: {0, E, INT_MAX}.
+struct DispatchSel {
+  int e_lo;
+  int count;
+  int capacity;
+};
+
+// Per-block expert counts [nblk, count] of the assignments.
+cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E,
+                                 const DispatchSel& sel, int32_t* blk_counts, cudaStream_t s);
+// counts [count] (kept), offsets [count + 1] and block rank bases [nblk, count].
+cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, const DispatchSel& sel,
+                                 int32_t* counts, int32_t* offsets, int32_t* bases,
                                  cudaStream_t s);
-// counts [E], offsets [E+1] and block bases [nblk, E].
-cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, int E, int32_t* counts,
-                                 int32_t* offsets, int32_t* bases, cudaStream_t s);
-// perm_dst[a], perm_src[p] from block bases and in-block stable ranks.
+// perm_dst[a] (-1 when dropped), perm_src[p] from bases, offsets and in-block ranks.
 cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
-                                    const int32_t* bases, int32_t* perm_src, int32_t* perm_dst,
+                                    const DispatchSel& sel, const int32_t* bases,
+                                    const int32_t* offsets, int32_t* perm_src, int32_t* perm_dst,
                                     cudaStream_t s);
 
-// out[p] = in[idx[p] / div] for p < rows (bf16 rows of h elements); `in` has
+// out[p] = in[idx[p] / div] for p < rows (bf16 rows of h elements), and only
+// for p < *nvalid when nvalid is given; idx < 0 gives a zero row.  `in` has
 // src_rows rows and source indices are clamped into it.
 cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                                long long src_rows, int h, uint16_t* out, int num_sms,
-                               cudaStream_t s);
+                               cudaStream_t s, const int32_t* nvalid = nullptr);
 
 // y[t] = sum_j g[t,j] O[perm_dst[t*k+j]].
 cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t* perm_dst, int T,
@@ -45,7 +56,8 @@ cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t*
 // dO[p] = bf16(g[a] dy[t]), dg[a] = <dy[t], O[p]> with a = perm_src[p], t = a / k.
 cudaError_t launch_bwd_prep(const uint16_t* dy, const uint16_t* O, const float* gates,
                             const int32_t* perm_src, long long rows, int k, int h, uint16_t* dO,
-                            float* dg, int num_sms, cudaStream_t s);
+                            float* dg, int num_sms, cudaStream_t s,
+                            const int32_t* nvalid = nullptr);
 
 // WgT[e][i] = Wg[i][e].
 cudaError_t launch_transpose_wg(const float* Wg, int h, int E, float* WgT, cudaStream_t s);

@@ -21,6 +21,7 @@
 // no ordering between them) race on the array and produce wrong maps.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 #include <mutex>
 
@@ -67,7 +68,7 @@ extern "C" moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* t
                                           moe_stream_t stream_) {
   if (!dims) return MOE_ERR_INVALID_ARG;
   const moe_dims& d = *dims;
-  if (d.T < 0 || d.h <= 0 || d.f <= 0 || d.E <= 0 || d.k <= 0 || d.k > d.E)
+  if (d.T < 0 || d.h <= 0 || d.f <= 0 || d.E <= 0 || d.k <= 0 || d.capacity < 0)
     return MOE_ERR_INVALID_ARG;
   if (d.k > 8 || d.E > moe::kRouterMaxE || d.h % 64 != 0 || d.f % 64 != 0 ||
       static_cast<long long>(d.T) * d.k >= (1ll << 31))
@@ -90,15 +91,18 @@ extern "C" moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* t
   int32_t* bases = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(scratch) + part);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
-  if (moe::launch_dispatch_hist(topk_idx, R, d.E, blk_counts, s) != cudaSuccess ||
-      moe::launch_dispatch_scan(blk_counts, nblk, d.E, counts, offsets, bases, s) != cudaSuccess ||
-      moe::launch_dispatch_scatter(topk_idx, R, d.E, bases, perm_src, perm_dst, s) != cudaSuccess)
+  const moe::DispatchSel sel{0, d.E, d.capacity > 0 ? d.capacity : INT_MAX};
+  if (moe::launch_dispatch_hist(topk_idx, R, d.E, sel, blk_counts, s) != cudaSuccess ||
+      moe::launch_dispatch_scan(blk_counts, nblk, sel, counts, offsets, bases, s) != cudaSuccess ||
+      moe::launch_dispatch_scatter(topk_idx, R, d.E, sel, bases, offsets, perm_src, perm_dst, s) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
   if (x && x_perm) {
     int sms = 148, dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (moe::launch_gather_rows(x, perm_src, d.k, R, d.T, d.h, x_perm, sms, s) != cudaSuccess)
+    if (moe::launch_gather_rows(x, perm_src, d.k, R, d.T, d.h, x_perm, sms, s, offsets + d.E) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
   }
   return MOE_OK;

@@ -50,6 +50,7 @@ def _d(**kw):
     (dict(f=72), mb.MOE_ERR_UNSUPPORTED),
     (dict(T=-1), mb.MOE_ERR_INVALID_ARG),
     (dict(T=1 << 29, k=8), mb.MOE_ERR_UNSUPPORTED),
+    (dict(capacity=-1), mb.MOE_ERR_INVALID_ARG),
 ])
 def test_bad_dims_rejected(lib, kw, code):
     d = _d(**kw)
@@ -125,6 +126,26 @@ def test_sizes_cover_tensors(lib):
         assert all(o % 256 == 0 for o in offs)
     with pytest.raises(mb.MoeError):
         mb.moe_saved_view(_d(), FAKE, "nope")
+
+
+@pytest.mark.parametrize("lo,hi,ok", [(0, 8, True), (3, 4, True), (-1, 4, False), (4, 4, False),
+                                      (5, 3, False), (0, 9, False)])
+def test_permute_local_range_checked(lib, lo, hi, ok):
+    d = _d()
+    need = lib.moe_workspace_bytes(ctypes.byref(d), mb.OP_PERMUTE)
+    P = FAKE
+    # a valid range with a too-small workspace stops at the workspace check,
+    # so nothing is launched either way
+    st = lib.moe_permute_local(ctypes.byref(d), P, lo, hi, None, P, P, P, P, None, P, need - 1,
+                               None)
+    assert st == (mb.MOE_ERR_WORKSPACE if ok else mb.MOE_ERR_INVALID_ARG)
+
+
+def test_capacity_helper():
+    assert mb.capacity_for(16384, 2, 8, 1.0) == 4096
+    assert mb.capacity_for(10, 3, 4, 1.25) == 10   # ceil(9.375)
+    assert mb.dims(4, 64, 64, 4, 2, capacity=3).capacity == 3
+    assert mb.dims(4, 64, 64, 4, 2).capacity == 0
 
 
 def test_profile_hook_without_events(lib):
