@@ -33,8 +33,8 @@ from routing_grouped_expert_router_gb300 import metrics  # noqa: E402
 from routing_grouped_expert_router_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s fwd+bwd; GroupedGEMM TFLOP/s as % of GB300 BF16 peak"
-GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc2_dgrad_swiglu_bwd", "gg_fc2_wgrad",
-         "gg_fc1_dgrad", "gg_fc1_wgrad")
+GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc2_dgrad_swiglu_bwd",
+         "gg_fc2_dgrad_swiglu_bwd_sar", "gg_fc2_wgrad", "gg_fc1_dgrad", "gg_fc1_wgrad")
 
 
 def parse():
@@ -53,6 +53,11 @@ def parse():
     p.add_argument("--experts", type=int, default=0, help="override E (k = min(k, E))")
     # time one step of the path alone (profiling aid; not the bench line)
     p.add_argument("--stage", default="layer", choices=["layer", "router"])
+    # layer variants (the bench line names the variant in `config`)
+    p.add_argument("--sar", action="store_true",
+                   help="selective activation rematerialisation: keep A, B only")
+    p.add_argument("--capacity-factor", type=float, default=0.0,
+                   help="per-expert capacity = ceil(cf * T * k / E); 0 = dropless")
     return p.parse_args()
 
 
@@ -147,11 +152,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our layer ---
 class Layer:
-    def __init__(self, cfg, device):
+    def __init__(self, cfg, device, sar=False, capacity=0):
         from routing_grouped_expert_router_gb300 import binding as mb
         self.mb = mb
         self.cfg = cfg
-        self.d = mb.dims_of(cfg)
+        self.d = mb.dims_of(cfg, capacity=capacity, sar=sar)
         T, h, f, E = cfg.T, cfg.h, cfg.f, cfg.E
         dev = device
         self.saved = torch.zeros(mb.moe_saved_bytes(self.d), dtype=torch.uint8, device=dev)
@@ -176,6 +181,11 @@ class Layer:
         mb.moe_layer_bwd(self.d, x, dy, inp["Wg"], inp["W1"], inp["W3"], inp["W2"], self.saved,
                          self.dx, self.dWg, self.dW1, self.dW3, self.dW2, self.ws_b)
 
+    def mb_saved_offsets_last(self) -> int:
+        """offsets[E] of the last forward: the permuted rows kept."""
+        addr = self.mb.moe_saved_view(self.d, self.saved, "offsets") - self.saved.data_ptr()
+        return int(self.saved[addr:addr + 4 * (self.d.E + 1)].view(torch.int32)[-1].item())
+
 
 def run_ours(args, cfg, world, rank, local):
     from routing_grouped_expert_router_gb300 import binding as mb
@@ -192,7 +202,9 @@ def run_ours(args, cfg, world, rank, local):
     mb.load()
     cfg_r = mcfg.LayerConfig(**{**cfg.as_dict(), "seed": cfg.seed + 1000 * rank}) if rank else cfg
     inp = synth.make_layer(cfg_r, device)
-    layer = Layer(cfg_r, device)
+    cap = (mb.capacity_for(cfg.T, cfg.k, cfg.E, args.capacity_factor)
+           if args.capacity_factor > 0 else 0)
+    layer = Layer(cfg_r, device, sar=args.sar, capacity=cap)
     stream = torch.cuda.current_stream(device)
 
     for _ in range(args.warmup):
@@ -219,11 +231,13 @@ def run_ours(args, cfg, world, rank, local):
     torch.cuda.synchronize(device)
     sampler.start()
     mb.moe_profile_events(ctypes.addressof(handles), nev)
+    k0 = mb.moe_kernel_launches()
     start.record(stream)
     for _ in range(args.steps):
         layer.step(inp)
     end.record(stream)
     launches = mb.moe_profile_events(None, 0)
+    kernels_launched = mb.moe_kernel_launches() - k0
     torch.cuda.synchronize(device)
     clocks = sampler.stop()
     if world > 1:
@@ -243,7 +257,9 @@ def run_ours(args, cfg, world, rank, local):
         per_kernel.setdefault(names[i], []).append(dt)
         prev = evs[i]
 
-    result = {"ms": ms, "per_kernel": per_kernel, "launches": launches, "clocks": clocks}
+    result = {"ms": ms, "per_kernel": per_kernel, "launches": kernels_launched, "clocks": clocks,
+              "saved_bytes": layer.saved.numel(),
+              "kept_rows": int(layer.mb_saved_offsets_last()) if cap else cfg.T * cfg.k}
 
     # e2e: host buffers, H2D of the step's inputs, D2H of its outputs
     if not args.no_e2e:
@@ -398,6 +414,9 @@ def main():
     ms_step = r["ms"] / K
     tokens_per_s = job_tokens_per_s(cfg.T, n, K, r["ms"])
     work = metrics.kernel_work(cfg.T, cfg.h, cfg.f, cfg.E, cfg.k)
+    # the matmuls run on the kept rows only (all T*k when dropless)
+    kept_frac = r["kept_rows"] / float(cfg.T * cfg.k)
+    work["flops"] = {g: fl * kept_frac for g, fl in work["flops"].items()}
     kern = {}
     for name, ts in r["per_kernel"].items():
         avg = sum(ts) / len(ts)
@@ -409,7 +428,7 @@ def main():
             ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
         kern[name] = ent
     gemm_ms = sum(sum(r["per_kernel"].get(g, [])) for g in GEMMS)
-    gemm_flops = cfg.gemm_flops_fwd_bwd() * K
+    gemm_flops = cfg.gemm_flops_fwd_bwd() * K * kept_frac
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
     peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     dominant = max((g for g in GEMMS if g in r["per_kernel"]),
@@ -423,6 +442,10 @@ def main():
         "config": {"workload": workload, "T": cfg.T, "h": cfg.h, "h_ffn": cfg.f, "E": cfg.E,
                    "top_k": cfg.k, "tokens_per_gpu_per_step": cfg.T,
                    "parallelism": f"replicas{n}" if n > 1 else "single",
+                   "variant": ("sar" if args.sar else "default")
+                   + (f", capacity factor {args.capacity_factor}" if args.capacity_factor else
+                      ", dropless"),
+                   "saved_bytes": r["saved_bytes"], "kept_rows": r["kept_rows"],
                    "l2": "inputs larger than L2 (weights + activations ~ GBs per step), no flush"},
         "gemm_tflops": gemm_tflops,
         "gemm_pct_of_bf16_peak": (100.0 * gemm_tflops / peak_tf) if gemm_tflops else None,

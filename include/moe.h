@@ -87,6 +87,7 @@ typedef struct {
   int32_t k;         /* experts per token */
   int32_t has_bias;  /* 1: router bias b[E] is added to the logits */
   int32_t capacity;  /* 0: dropless; C > 0: at most C assignments per expert */
+  int32_t sar;       /* 1: selective activation rematerialisation (see below) */
 } moe_dims;
 
 typedef enum {
@@ -105,9 +106,18 @@ typedef enum {
 size_t moe_workspace_bytes(const moe_dims* dims, int op);
 
 /* Bytes of the forward->backward context that moe_layer_fwd writes into
- * `saved` and moe_layer_bwd reads: routing, dispatch maps, the permuted token
- * rows and the expert activations A = X W1, B = X W3, H = silu(A)*B, O = H W2
- * (the expensive activations are kept, per the review's 选择性激活重计算). */
+ * `saved` and moe_layer_bwd reads: routing, dispatch maps and activations.
+ *   sar = 0: the permuted token rows x_perm and all four expert activations
+ *            A = X W1, B = X W3, H = silu(A)*B, O = H W2; per layer
+ *            (2k + 3k f/h) T h bf16 elements.
+ *   sar = 1: selective activation rematerialisation (digest §3.3 "Inter-
+ *            operator overlap"; review 选择性激活重计算): only A and B, i.e.
+ *            2k (f/h) T h elements -- the pages' (2kf + ...) bsh/n after SAR,
+ *            against (... 2k + 3kf ...) bsh/n before, at n = 1.  The backward
+ *            gathers x_perm and dy again, rebuilds H from A and B inside the
+ *            FC2 dgrad, and takes the gate gradient <dy, O> as <H, dy W2^T>
+ *            (the same value), so O is never needed.  H, O and x_perm then live
+ *            in the forward workspace, which is not kept between the calls. */
 size_t moe_saved_bytes(const moe_dims* dims);
 
 /* Router logits l = x Wg (+ b), softmax over the E experts, top-k selection
@@ -252,8 +262,9 @@ moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x,
                          void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Views into a `saved` context (device pointers at fixed offsets; NULL on
- * invalid dims).  Names: "topk_idx", "gates", "counts", "offsets",
- * "perm_src", "perm_dst", "x_perm", "A", "B", "H", "O". */
+ * invalid dims, and for "x_perm", "H", "O" when dims.sar = 1).  Names:
+ * "topk_idx", "gates", "counts", "offsets", "perm_src", "perm_dst",
+ * "x_perm", "A", "B", "H", "O". */
 void* moe_saved_view(const moe_dims* dims, void* saved, const char* name);
 
 /* Human-readable name of a status. */
@@ -273,6 +284,11 @@ moe_status moe_clear_device_status(void* ws, moe_stream_t stream);
  * moe_profile_kernel_name(i) names the kernel recorded by event i. */
 int moe_profile_events(moe_event_t* events, int capacity);
 const char* moe_profile_kernel_name(int i);
+
+/* Number of CUDA kernels the library has launched from the calling host
+ * thread since it was loaded (a named step of the measurement hook may launch
+ * more than one kernel: the router and the router weight gradient run two). */
+int64_t moe_kernel_launches(void);
 
 /* Library build string (arch, version). */
 const char* moe_version(void);

@@ -37,16 +37,17 @@ class MoeError(RuntimeError):
 class moe_dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("h", ctypes.c_int32), ("f", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("has_bias", ctypes.c_int32),
-                ("capacity", ctypes.c_int32)]
+                ("capacity", ctypes.c_int32), ("sar", ctypes.c_int32)]
 
 
-def dims(T, h, f, E, k, has_bias=False, capacity=0) -> moe_dims:
-    return moe_dims(int(T), int(h), int(f), int(E), int(k), int(bool(has_bias)), int(capacity))
+def dims(T, h, f, E, k, has_bias=False, capacity=0, sar=False) -> moe_dims:
+    return moe_dims(int(T), int(h), int(f), int(E), int(k), int(bool(has_bias)), int(capacity),
+                    int(bool(sar)))
 
 
-def dims_of(cfg, has_bias=None, capacity=0) -> moe_dims:
+def dims_of(cfg, has_bias=None, capacity=0, sar=False) -> moe_dims:
     hb = cfg.zipf_s > 0 if has_bias is None else has_bias
-    return dims(cfg.T, cfg.h, cfg.f, cfg.E, cfg.k, hb, capacity)
+    return dims(cfg.T, cfg.h, cfg.f, cfg.E, cfg.k, hb, capacity, sar)
 
 
 def capacity_for(T, k, E, factor: float) -> int:
@@ -82,6 +83,7 @@ _SIGS = {
     "moe_clear_device_status": (_I, [_P, _P]),
     "moe_profile_events": (_I, [_P, _I]),
     "moe_profile_kernel_name": (ctypes.c_char_p, [_I]),
+    "moe_kernel_launches": (ctypes.c_int64, []),
     "moe_version": (ctypes.c_char_p, []),
 }
 
@@ -252,3 +254,7 @@ def moe_profile_events(events_array_addr: int | None, capacity: int) -> int:
 
 def moe_profile_kernel_name(i: int) -> str:
     return load().moe_profile_kernel_name(int(i)).decode()
+
+
+def moe_kernel_launches() -> int:
+    return int(load().moe_kernel_launches())

@@ -52,6 +52,7 @@ moe_status check_dims(const moe_dims* d, bool routed) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->T < 0 || d->h <= 0 || d->f <= 0 || d->E <= 0 || d->k <= 0) return MOE_ERR_INVALID_ARG;
   if ((routed && d->k > d->E) || d->capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (d->sar != 0 && d->sar != 1) return MOE_ERR_INVALID_ARG;
   if (d->k > 8 || d->E > moe::kRouterMaxE) return MOE_ERR_UNSUPPORTED;
   if (d->h % 64 != 0 || d->f % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(d->T) * d->k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
@@ -90,6 +91,13 @@ size_t rows_of(const moe_dims& d) { return static_cast<size_t>(d.T) * d.k; }
 struct SavedLayout {
   size_t topk_idx, gates, counts, offsets, perm_src, perm_dst, x_perm, A, B, H, O, total;
 };
+constexpr size_t kAbsent = ~size_t(0);  // a tensor this mode does not keep
+
+// The forward->backward context.  Default: the routing, the dispatch maps and
+// every expert activation (x_perm, A, B, H, O).  Selective activation
+// rematerialisation (dims.sar = 1): A and B only of the activations; x_perm is
+// gathered again, H rebuilt from A and B, and O is not needed because
+// <dy, O> = <H, dy W2^T> comes out of the FC2 dgrad.
 SavedLayout saved_layout(const moe_dims& d) {
   const size_t R = rows_of(d);
   Carve c;
@@ -100,11 +108,11 @@ SavedLayout saved_layout(const moe_dims& d) {
   L.offsets = c.take(static_cast<size_t>(d.E + 1) * 4);
   L.perm_src = c.take(R * 4);
   L.perm_dst = c.take(R * 4);
-  L.x_perm = c.take(R * d.h * 2);
+  L.x_perm = d.sar ? kAbsent : c.take(R * d.h * 2);
   L.A = c.take(R * d.f * 2);
   L.B = c.take(R * d.f * 2);
-  L.H = c.take(R * d.f * 2);
-  L.O = c.take(R * d.h * 2);
+  L.H = d.sar ? kAbsent : c.take(R * d.f * 2);
+  L.O = d.sar ? kAbsent : c.take(R * d.h * 2);
   L.total = c.off;
   return L;
 }
@@ -116,6 +124,8 @@ struct WsLayout {
   size_t dX = 0, dg = 0;                     // layer backward
   size_t dl = 0, WgT = 0, partial = 0;       // router backward
   size_t logits = 0;                         // router partial logits
+  size_t H = 0, O = 0;                       // sar forward: activations not kept
+  size_t gH = 0, gate_rows = 0, dg_part = 0;  // sar backward
   size_t total = 0;
 };
 WsLayout ws_layout(const moe_dims& d, int op) {
@@ -149,12 +159,22 @@ WsLayout ws_layout(const moe_dims& d, int op) {
     case MOE_OP_LAYER_FWD:
       route();
       dispatch();
+      if (d.sar) {
+        L.x_perm = c.take(R * d.h * 2);
+        L.H = c.take(R * d.f * 2);
+        L.O = c.take(R * d.h * 2);
+      }
       break;
     case MOE_OP_LAYER_BWD:
-      expert_bwd(false);
+      expert_bwd(d.sar != 0);
       L.dX = c.take(R * d.h * 4);
       L.dg = c.take(R * 4);
       router_bwd();
+      if (d.sar) {
+        L.gH = c.take(R * d.f * 2);
+        L.gate_rows = c.take(R * 4);
+        L.dg_part = c.take(R * static_cast<size_t>(moe::gemm_col_tiles(d.f)) * 4);
+      }
       break;
     default: return WsLayout{};
   }
@@ -259,6 +279,48 @@ moe_status do_ffn_bwd(const moe_dims& d, const uint16_t* x_perm, const uint16_t*
   return MOE_OK;
 }
 
+// Expert backward from a sar context (A, B kept): gathers x_perm and the
+// ungated dy rows again, rebuilds H inside the FC2 dgrad, and reduces the gate
+// gradients from the dgrad's per-tile partial sums.
+moe_status do_ffn_bwd_sar(const moe_dims& d, const uint16_t* x, const uint16_t* dy,
+                          const float* gates, const int32_t* psrc, const int32_t* offsets,
+                          const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                          const uint16_t* A, const uint16_t* B, float* dX, float* dg, float* dW1,
+                          float* dW3, float* dW2, void* ws, const WsLayout& L,
+                          cudaStream_t stream) {
+  const long long R = static_cast<long long>(rows_of(d));
+  uint16_t* xp = at<uint16_t>(ws, L.x_perm);
+  uint16_t* dyp = at<uint16_t>(ws, L.dO);
+  uint16_t* dA = at<uint16_t>(ws, L.dA);
+  uint16_t* dB = at<uint16_t>(ws, L.dB);
+  uint16_t* gH = at<uint16_t>(ws, L.gH);
+  float* grow = at<float>(ws, L.gate_rows);
+  float* part = at<float>(ws, L.dg_part);
+  const int32_t* nvalid = offsets + d.E;
+  MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, R, d.T, d.h, xp, num_sms(), stream, nvalid),
+          "permute_rows");
+  MOE_RUN(moe::launch_gather_rows(dy, psrc, d.k, R, d.T, d.h, dyp, num_sms(), stream, nvalid,
+                                  gates, grow),
+          "permute_dy");
+  if (R == 0) {
+    const size_t wbytes = static_cast<size_t>(d.E) * d.h * d.f * 4;
+    MOE_RUN(cudaMemsetAsync(dW1, 0, wbytes, stream), "zero_dW1");
+    MOE_RUN(cudaMemsetAsync(dW3, 0, wbytes, stream), "zero_dW3");
+    MOE_RUN(cudaMemsetAsync(dW2, 0, wbytes, stream), "zero_dW2");
+    return MOE_OK;
+  }
+  const GemmProblem g = problem(d, offsets, ws);
+  MOE_RUN(moe::gemm_fc2_dgrad_sar(g, dyp, W2, A, B, grow, dA, dB, gH, part, stream),
+          moe::kGemmSarDgradName);
+  MOE_RUN(moe::gemm_fc2_wgrad(g, gH, dyp, dW2, stream), moe::kGemmNames[4]);
+  MOE_RUN(moe::gemm_fc1_dgrad(g, dA, dB, W1, W3, dX, stream), moe::kGemmNames[3]);
+  MOE_RUN(moe::gemm_fc1_wgrad(g, xp, dA, dB, dW1, dW3, stream), moe::kGemmNames[5]);
+  MOE_RUN(moe::launch_dg_reduce(part, moe::gemm_col_tiles(d.f), psrc, R, nvalid, dg, num_sms(),
+                                stream),
+          "dg_reduce");
+  return MOE_OK;
+}
+
 moe_status do_router_bwd(const moe_dims& d, const uint16_t* x, const float* Wg,
                          const int32_t* idx, const float* gates, const float* dg,
                          const float* dX, const int32_t* pdst, uint16_t* dx, float* dWg, void* ws,
@@ -314,7 +376,7 @@ void* moe_saved_view(const moe_dims* dims, void* saved, const char* name) {
              {"x_perm", L.x_perm},     {"A", L.A},               {"B", L.B},
              {"H", L.H},               {"O", L.O}};
   for (auto& e : tab)
-    if (strcmp(e.n, name) == 0) return at<uint8_t>(saved, e.off);
+    if (strcmp(e.n, name) == 0) return e.off == kAbsent ? nullptr : at<uint8_t>(saved, e.off);
   return nullptr;
 }
 
@@ -325,6 +387,8 @@ int moe_profile_events(moe_event_t* events, int capacity) {
   g_prof.count = 0;
   return n;
 }
+
+int64_t moe_kernel_launches(void) { return moe::kernel_launches(); }
 
 const char* moe_profile_kernel_name(int i) {
   if (i < 0 || i >= 4096) return "";
@@ -532,8 +596,10 @@ moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* W
   int32_t* offsets = at<int32_t>(saved, S.offsets);
   int32_t* psrc = at<int32_t>(saved, S.perm_src);
   int32_t* pdst = at<int32_t>(saved, S.perm_dst);
-  uint16_t* xp = at<uint16_t>(saved, S.x_perm);
-  uint16_t* O = at<uint16_t>(saved, S.O);
+  // activations that sar does not keep live in the workspace
+  uint16_t* xp = d.sar ? at<uint16_t>(ws, L.x_perm) : at<uint16_t>(saved, S.x_perm);
+  uint16_t* H = d.sar ? at<uint16_t>(ws, L.H) : at<uint16_t>(saved, S.H);
+  uint16_t* O = d.sar ? at<uint16_t>(ws, L.O) : at<uint16_t>(saved, S.O);
   if ((st = do_route(d, x, Wg, b, idx, gates, ws, L, stream)) != MOE_OK) return st;
   if ((st = do_dispatch(d, selection(d, 0, d.E), idx, at<int32_t>(saved, S.counts), offsets, psrc,
                         pdst, ws, L, stream)) != MOE_OK)
@@ -542,7 +608,7 @@ moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* W
                                   num_sms(), stream, offsets + d.E),
           "permute_rows");
   if ((st = do_ffn_fwd(d, xp, offsets, W1, W3, W2, at<uint16_t>(saved, S.A),
-                       at<uint16_t>(saved, S.B), at<uint16_t>(saved, S.H), O, ws, stream)) != MOE_OK)
+                       at<uint16_t>(saved, S.B), H, O, ws, stream)) != MOE_OK)
     return st;
   MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
   return MOE_OK;
@@ -574,6 +640,13 @@ moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16
   float* dX = at<float>(ws, L.dX);
   float* dg = at<float>(ws, L.dg);
   const long long R = static_cast<long long>(rows_of(d));
+  if (d.sar) {
+    if ((st = do_ffn_bwd_sar(d, x, dy, gates, psrc, offsets, W1, W3, W2, at<uint16_t>(saved, S.A),
+                             at<uint16_t>(saved, S.B), dX, dg, dW1, dW3, dW2, ws, L, stream)) !=
+        MOE_OK)
+      return st;
+    return do_router_bwd(d, x, Wg, idx, gates, dg, dX, pdst, dx, dWg, ws, L, stream);
+  }
   MOE_RUN(moe::launch_bwd_prep(dy, at<uint16_t>(saved, S.O), gates, psrc, R, d.k, d.h, dO, dg,
                                num_sms(), stream, offsets + d.E),
           "bwd_prep");

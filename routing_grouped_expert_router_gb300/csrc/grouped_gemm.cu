@@ -25,6 +25,7 @@
 #include <cstring>
 
 #include "grouped_gemm.cuh"
+#include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -34,6 +35,7 @@ int g_pair_clusters = 0;  // co-resident CTA pairs of the last pair launch (diag
 const char* const kGemmNames[6] = {"gg_fc1_fwd_swiglu", "gg_fc2_fwd",
                                    "gg_fc2_dgrad_swiglu_bwd", "gg_fc1_dgrad",
                                    "gg_fc2_wgrad", "gg_fc1_wgrad"};
+const char* const kGemmSarDgradName = "gg_fc2_dgrad_swiglu_bwd_sar";
 
 namespace {
 
@@ -64,7 +66,14 @@ struct alignas(8) Ctrl {
 };
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + static_cast<int>(sizeof(Ctrl));
 
-enum Epi { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_SWIGLU_BWD = 2, EPI_F32 = 3, EPI_WGRAD = 4 };
+enum Epi {
+  EPI_SWIGLU = 0,
+  EPI_BF16 = 1,
+  EPI_SWIGLU_BWD = 2,
+  EPI_F32 = 3,
+  EPI_WGRAD = 4,
+  EPI_SWIGLU_BWD_SAR = 5  // SwiGLU backward that rebuilds H from A, B (no saved H or O)
+};
 
 struct Params {
   int E;
@@ -80,6 +89,9 @@ struct Params {
   void* out2;
   const void* in0;
   const void* in1;
+  const float* in2;  // EPI_SWIGLU_BWD_SAR: gate of each permuted row
+  float* part;       // EPI_SWIGLU_BWD_SAR: per-(row, n-tile) partial sums of <H, dY W2^T>
+  int part_ld;       // n-tiles per row of `part`
   int ldo;           // row stride (elements) of M-grouped outputs and inputs
   int* status;
   int ktiles;        // K-grouped: tiles in total
@@ -185,7 +197,8 @@ __device__ __forceinline__ void store_f32x32(void* dst, const float* v) {
 //   v0 (and v1 for two B operands): the fp32 accumulator values.
 template <int NUM_B, int EPI>
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, int grow, int orow,
-                                               int col, const float* v0, const float* v1) {
+                                               int col, const float* v0, const float* v1,
+                                               float& acc) {
   if (EPI == EPI_SWIGLU) {
     const size_t o = static_cast<size_t>(grow) * p.ldo + col;
     float hv[32];
@@ -213,6 +226,32 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, 
     }
     store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
     store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
+  } else if (EPI == EPI_SWIGLU_BWD_SAR) {
+    // The accumulator holds u = dy_perm W2^T without the gate.  With the row's
+    // gate g and H = silu(A) * B rebuilt from the kept A, B:
+    //   dH = g u;  dA, dB as in EPI_SWIGLU_BWD;  gH = g H (FC2 wgrad's operand,
+    //   since dW2 = H^T (g dy) = (g H)^T dy);  dg += <H, u> (= <dy, O>).
+    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+    float av[32], bv[32];
+    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in0) + o, av);
+    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in1) + o, bv);
+    const float g = __ldg(p.in2 + grow);
+    float da[32], db[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = av[i];
+      const float sg = 1.0f / (1.0f + expf(-a));
+      const float sl = a * sg;
+      const float hh = sl * bv[i];
+      const float dh = g * v0[i];
+      acc = fmaf(hh, v0[i], acc);
+      da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
+      db[i] = dh * sl;
+      av[i] = g * hh;  // gH
+    }
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, av);
   } else if (EPI == EPI_F32) {
     const size_t o = static_cast<size_t>(grow) * p.ldo + col;
     store_f32x32(static_cast<float*>(p.out0) + o, v0);
@@ -458,6 +497,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tbase = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int grow = tl.row0 + r;                        // M-grouped row
       const bool row_ok = GROUP_K ? (tl.mb * BM + r < p.M) : (grow < tl.row_end);
+      float acc = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < BNB / 32; ++ch) {
         float v0[32];
@@ -466,8 +506,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
         const int col = tl.nb * BNB + ch * 32;
         if (!row_ok || col >= p.N) continue;
-        epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1);
+        epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1, acc);
       }
+      if (EPI == EPI_SWIGLU_BWD_SAR && row_ok)
+        p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
       tc_fence_before();
       mbar_arrive(smem_u32(&c.tempty[buf]));
     }
@@ -766,6 +808,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tbase = tmem_base + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int grow = tl.row0 + half + r;           // M-grouped row
       const bool row_ok = GROUP_K ? (orow < p.M) : (grow < tl.row_end);
+      float acc = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < BNB / 32; ++ch) {
         float v0[32];
@@ -774,8 +817,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
         const int col = tl.nb * BNB + ch * 32;
         if (!row_ok || col >= p.N) continue;
-        epilogue_chunk<NUM_B, EPI>(p, tl, grow, orow, col, v0, v1);
+        epilogue_chunk<NUM_B, EPI>(p, tl, grow, orow, col, v0, v1, acc);
       }
+      if (EPI == EPI_SWIGLU_BWD_SAR && row_ok)
+        p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&c.tempty[buf]), 0));
@@ -837,7 +882,7 @@ int forced_ctas() {
 }
 bool pair_for(int epi) {
   if (forced_ctas()) return forced_ctas() == 2;
-  return epi == EPI_SWIGLU_BWD || epi == EPI_F32;
+  return epi == EPI_SWIGLU_BWD || epi == EPI_SWIGLU_BWD_SAR || epi == EPI_F32;
 }
 
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
@@ -855,7 +900,7 @@ cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num
     }
     const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(prm, maps);
-    return cudaGetLastError();
+    return launched();
   }
   auto kern = gg2_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
   static bool attr2_set = false;
@@ -889,7 +934,8 @@ cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num
   g_pair_clusters = max_clusters;
   const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, prm, maps);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm, maps);
+  return e == cudaSuccess ? launched() : e;
 }
 
 Params base_params(const GemmProblem& g) {
@@ -984,6 +1030,36 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.ldo = g.f;
   return launch<false, false, 1, EPI_SWIGLU_BWD, false>(p, m, mgrouped_tiles(g, EPI_SWIGLU_BWD, g.f, BN),
                                                          g.num_sms, s);
+}
+
+int gemm_col_tiles(int n) { return (n + BN - 1) / BN; }
+
+cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& g, const void* dy_perm, const void* W2,
+                               const void* A, const void* B, const float* gate_rows, void* dA,
+                               void* dB, void* gH, float* dg_part, cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  if (!make_map(&m.a0, dy_perm, g.h, g.rows, BK, BM) ||
+      !make_map(&m.b0, W2, g.h, static_cast<uint64_t>(g.E) * g.f, BK,
+                kmajor_b_rows(EPI_SWIGLU_BWD_SAR)))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Params p = base_params(g);
+  p.N = g.f;
+  p.kblocks = g.h / BK;
+  p.b_rows = g.f;
+  p.in0 = A;
+  p.in1 = B;
+  p.in2 = gate_rows;
+  p.part = dg_part;
+  p.part_ld = gemm_col_tiles(g.f);
+  p.out0 = dA;
+  p.out1 = dB;
+  p.out2 = gH;
+  p.ldo = g.f;
+  return launch<false, false, 1, EPI_SWIGLU_BWD_SAR, false>(
+      p, m, mgrouped_tiles(g, EPI_SWIGLU_BWD_SAR, g.f, BN), g.num_sms, s);
 }
 
 cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB, const void* W1,

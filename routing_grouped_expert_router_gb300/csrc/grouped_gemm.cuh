@@ -30,6 +30,16 @@ cudaError_t gemm_fc2_fwd(const GemmProblem& p, const void* H, const void* W2, vo
 // dB = dH * silu(A).  dO: [rows, h]; A, B, dA, dB: [rows, f] bf16.
 cudaError_t gemm_fc2_dgrad(const GemmProblem& p, const void* dO, const void* W2,
                            const void* A, const void* B, void* dA, void* dB, cudaStream_t s);
+// The same matmul for selective activation rematerialisation, where neither H
+// nor O was kept: the A operand is the ungated dy_perm [rows, h], and with
+// u = dy_perm W2^T, g = gate_rows[row] and H = silu(A) * B rebuilt here:
+//   dA, dB from dH = g u;  gH = g H (bf16 [rows, f]);
+//   dg_part[row, nt] = sum of H u over n-tile nt (fp32 [rows, gemm_col_tiles(f)]).
+cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& p, const void* dy_perm, const void* W2,
+                               const void* A, const void* B, const float* gate_rows, void* dA,
+                               void* dB, void* gH, float* dg_part, cudaStream_t s);
+// Output-column tiles of the M-grouped matmuls for n columns.
+int gemm_col_tiles(int n);
 // dX_perm = dA W1^T + dB W3^T (K = 2f), fp32 [rows, h].
 cudaError_t gemm_fc1_dgrad(const GemmProblem& p, const void* dA, const void* dB,
                            const void* W1, const void* W3, float* dX, cudaStream_t s);
@@ -42,5 +52,6 @@ cudaError_t gemm_fc1_wgrad(const GemmProblem& p, const void* x_perm, const void*
 
 // Kernel names, in launch order of a layer, for the measurement hook.
 extern const char* const kGemmNames[6];
+extern const char* const kGemmSarDgradName;
 
 }  // namespace moe

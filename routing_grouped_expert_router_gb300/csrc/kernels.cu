@@ -11,6 +11,17 @@
 #include "kernels.cuh"
 
 namespace moe {
+
+namespace {
+thread_local long long g_launches = 0;
+}  // namespace
+
+long long kernel_launches() { return g_launches; }
+
+cudaError_t launched() {
+  ++g_launches;
+  return cudaGetLastError();
+}
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -401,7 +412,7 @@ cudaError_t router_b_launch(const uint16_t* x, const float* Wg, int T, int h, in
   if (bpc < 1) bpc = 1;
   if (bpc > tiles) bpc = tiles;
   router_b_kernel<EP><<<nch * bpc, 256, S::SMEM, s>>>(x, Wg, T, h, E, nch, partial);
-  return cudaGetLastError();
+  return launched();
 }
 
 template <int EP>
@@ -411,7 +422,7 @@ cudaError_t router_select_launch(const float* partial, int nch, const float* b, 
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   router_select_kernel<EP><<<static_cast<int>(blocks), 128, 0, s>>>(partial, nch, b, T, E, k, idx,
                                                                    gates);
-  return cudaGetLastError();
+  return launched();
 }
 
 // ---------------------------------------------------------------- dispatch
@@ -513,12 +524,14 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t* __res
 // --------------------------------------------------------------- row moves
 // Warp per row, 16-byte pieces.
 // Rows p < *nvalid (all `rows` when nvalid is NULL); a negative index gives a
-// zero row.
+// zero row.  With gsrc/gdst, also gdst[p] = gsrc[idx[p]] (a value per row).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ in,
                                                           const int32_t* __restrict__ idx, int div,
                                                           long long rows, long long src_rows,
                                                           const int32_t* __restrict__ nvalid,
-                                                          int h8, uint4* __restrict__ out) {
+                                                          int h8, uint4* __restrict__ out,
+                                                          const float* __restrict__ gsrc,
+                                                          float* __restrict__ gdst) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -529,6 +542,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   for (long long p = gw; p < rows; p += nw) {
     const long long i = __ldg(idx + p);
     uint4* d = out + p * h8;
+    if (gdst && lane == 0) gdst[p] = i < 0 ? 0.f : __ldg(gsrc + i);
     if (i < 0) {
       for (int c = lane; c < h8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
       continue;
@@ -631,6 +645,25 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
     if (lane == 0) dg[a] = dot;
+  }
+}
+
+// dg[perm_src[p]] = sum over nt of part[p, nt], in nt order, for p < *nvalid.
+__global__ void __launch_bounds__(256) dg_reduce_kernel(const float* __restrict__ part, int nt,
+                                                        const int32_t* __restrict__ perm_src,
+                                                        long long rows,
+                                                        const int32_t* __restrict__ nvalid,
+                                                        float* __restrict__ dg) {
+  const long long nv = __ldg(nvalid);
+  const long long n = nv < rows ? (nv < 0 ? 0 : nv) : rows;
+  for (long long p = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; p < n;
+       p += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float* q = part + p * nt;
+    float s = 0.f;
+    for (int i = 0; i < nt; ++i) s += __ldg(q + i);
+    long long a = __ldg(perm_src + p);
+    a = a < 0 ? 0 : (a >= rows ? rows - 1 : a);
+    dg[a] = s;
   }
 }
 
@@ -850,7 +883,7 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
     if (bpc > tiles) bpc = tiles;
     router_a_kernel<<<nch * bpc, kRouterAThreads, kRouterASmem, s>>>(x, Wg, b, T, h, E, k, nch, idx, gates,
                                                         partial);
-    err = cudaGetLastError();
+    err = launched();
     if (err != cudaSuccess || nch == 1) return err;
     return router_select_launch<8>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
   }
@@ -871,7 +904,7 @@ cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E,
   dispatch_kernel<false><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, sel.e_lo, sel.count,
                                                         sel.capacity, blk_counts, nullptr, nullptr,
                                                         nullptr, nullptr);
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, const DispatchSel& sel,
@@ -879,7 +912,7 @@ cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, const Disp
                                  cudaStream_t s) {
   dispatch_scan_kernel<<<1, 256, 0, s>>>(blk_counts, nblk, sel.count, sel.capacity, counts,
                                          offsets, bases);
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
@@ -891,17 +924,19 @@ cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
   dispatch_kernel<true><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, sel.e_lo, sel.count,
                                                        sel.capacity, nullptr, bases, offsets,
                                                        perm_src, perm_dst);
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                                long long src_rows, int h, uint16_t* out, int num_sms,
-                               cudaStream_t s, const int32_t* nvalid) {
+                               cudaStream_t s, const int32_t* nvalid, const float* gsrc,
+                               float* gdst) {
   if (rows == 0 || src_rows == 0) return cudaSuccess;
   const int grid = grid_for(rows, num_sms, 8, 16);
   gather_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(in), idx, div, rows,
-                                          src_rows, nvalid, h / 8, reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
+                                          src_rows, nvalid, h / 8, reinterpret_cast<uint4*>(out),
+                                          gsrc, gdst);
+  return launched();
 }
 
 cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t* perm_dst, int T,
@@ -920,7 +955,17 @@ cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t*
     case 7: combine_kernel<7><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
     default: combine_kernel<8><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
   }
-  return cudaGetLastError();
+  return launched();
+}
+
+cudaError_t launch_dg_reduce(const float* part, int nt, const int32_t* perm_src, long long rows,
+                             const int32_t* nvalid, float* dg, int num_sms, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  long long blocks = (rows + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  dg_reduce_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, s>>>(part, nt, perm_src,
+                                                                                 rows, nvalid, dg);
+  return launched();
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* dy, const uint16_t* O, const float* gates,
@@ -931,7 +976,7 @@ cudaError_t launch_bwd_prep(const uint16_t* dy, const uint16_t* O, const float* 
   bwd_prep_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(dy),
                                        reinterpret_cast<const uint4*>(O), gates, perm_src, rows,
                                        nvalid, k, h / 8, reinterpret_cast<uint4*>(dO), dg);
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_transpose_wg(const float* Wg, int h, int E, float* WgT, cudaStream_t s) {
@@ -939,7 +984,7 @@ cudaError_t launch_transpose_wg(const float* Wg, int h, int E, float* WgT, cudaS
   int grid = static_cast<int>((n + 255) / 256);
   if (grid > 1024) grid = 1024;
   transpose_wg_kernel<<<grid, 256, 0, s>>>(Wg, h, E, WgT);
-  return cudaGetLastError();
+  return launched();
 }
 
 cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
@@ -962,7 +1007,7 @@ cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
     case 7: token_grad_kernel<7><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
     default: token_grad_kernel<8><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
   }
-  return cudaGetLastError();
+  return launched();
 }
 
 int wgrad_router_chunks(int T) { return (T + kWgChunk - 1) / kWgChunk; }
@@ -980,14 +1025,14 @@ cudaError_t launch_router_wgrad(const uint16_t* x, const float* dl, int T, int h
       router_wgrad_kernel<32><<<cols(WgShape<32>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
     else
       router_wgrad_kernel<64><<<cols(WgShape<64>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launched();
     if (e != cudaSuccess) return e;
   }
   const long long n = static_cast<long long>(h) * E;
   int grid2 = static_cast<int>((n + 255) / 256);
   if (grid2 > 2048) grid2 = 2048;
   router_wgrad_reduce_kernel<<<grid2, 256, 0, s>>>(partial, nchunks, h, E, dWg);
-  return cudaGetLastError();
+  return launched();
 }
 
 }  // namespace moe

@@ -7,6 +7,12 @@
 
 namespace moe {
 
+// Kernels launched so far by the calling host thread.  Every launcher calls
+// launched() right after each of its kernel launches: it counts the launch
+// and returns cudaGetLastError().
+long long kernel_launches();
+cudaError_t launched();
+
 constexpr int kDispatchChunk = 1024;  // assignments per dispatch block
 constexpr int kRouterMaxE = 64;
 
@@ -44,10 +50,15 @@ cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
 
 // out[p] = in[idx[p] / div] for p < rows (bf16 rows of h elements), and only
 // for p < *nvalid when nvalid is given; idx < 0 gives a zero row.  `in` has
-// src_rows rows and source indices are clamped into it.
+// src_rows rows and source indices are clamped into it.  With gsrc and gdst,
+// also gdst[p] = gsrc[idx[p]] (0 where idx < 0).
 cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                                long long src_rows, int h, uint16_t* out, int num_sms,
-                               cudaStream_t s, const int32_t* nvalid = nullptr);
+                               cudaStream_t s, const int32_t* nvalid = nullptr,
+                               const float* gsrc = nullptr, float* gdst = nullptr);
+// dg[perm_src[p]] = sum_{i < nt} part[p * nt + i] for p < *nvalid (fixed order).
+cudaError_t launch_dg_reduce(const float* part, int nt, const int32_t* perm_src, long long rows,
+                             const int32_t* nvalid, float* dg, int num_sms, cudaStream_t s);
 
 // y[t] = sum_j g[t,j] O[perm_dst[t*k+j]].
 cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t* perm_dst, int T,

@@ -24,6 +24,7 @@ def kernel_work(T: int, h: int, f: int, E: int, k: int) -> dict:
         "gg_fc1_fwd_swiglu": 2 * 2 * R * h * f,
         "gg_fc2_fwd": 2 * R * f * h,
         "gg_fc2_dgrad_swiglu_bwd": 2 * R * h * f,
+        "gg_fc2_dgrad_swiglu_bwd_sar": 2 * R * h * f,
         "gg_fc2_wgrad": 2 * R * f * h,
         "gg_fc1_dgrad": 2 * 2 * R * f * h,
         "gg_fc1_wgrad": 2 * 2 * R * h * f,
@@ -36,6 +37,8 @@ def kernel_work(T: int, h: int, f: int, E: int, k: int) -> dict:
         "permute_rows": T * h * 2 + R * h * 2 + R * 4,
         "combine": R * h * 2 + T * h * 2 + R * 8,
         "bwd_prep": T * h * 2 + 2 * R * h * 2 + R * 12,
+        "permute_dy": T * h * 2 + R * h * 2 + R * 12,
+        "dg_reduce": R * ((f + 255) // 256) * 4 + R * 8,
         "transpose_wg": 2 * h * E * 4,
         "token_grad": R * h * 4 + T * h * 2 + E * h * 4 + R * 16 + T * E * 4,
         "router_wgrad": T * h * 2 + T * E * 4 + h * E * 4,

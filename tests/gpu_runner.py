@@ -21,6 +21,10 @@ SAVED_TENSORS = {
 }
 
 
+# activations a sar context does not keep
+SAR_DROPPED = ("x_perm", "H", "O")
+
+
 def saved_tensor(d, saved: torch.Tensor, name: str) -> torch.Tensor:
     dtype, shp = SAVED_TENSORS[name]
     shape = shp(d)
@@ -70,7 +74,8 @@ class LayerRun:
         return saved_tensor(self.d, self.saved, name)
 
     def outputs(self) -> dict:
-        out = {n: self.saved_view(n).detach().cpu().clone() for n in SAVED_TENSORS}
+        kept = [n for n in SAVED_TENSORS if not (self.d.sar and n in SAR_DROPPED)]
+        out = {n: self.saved_view(n).detach().cpu().clone() for n in kept}
         for n in ("y", "dx", "dWg", "dW1", "dW3", "dW2"):
             out[n] = getattr(self, n).detach().cpu().clone()
         return out

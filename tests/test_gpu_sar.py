@@ -1,0 +1,111 @@
+"""GPU parity of the layer with selective activation rematerialisation
+(dims.sar = 1: the context keeps A and B only; the backward gathers x_perm and
+dy again, rebuilds H from A and B and takes the gate gradient from the FC2
+dgrad) against the oracle, at the same tolerances as the default mode:
+bit-exact routing and maps; y, dx relative L2 <= 5e-3; weight and router
+gradients <= 1e-2.  The forward is the default mode's, so y is bitwise equal.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routing_grouped_expert_router_gb300 import binding as mb
+from routing_grouped_expert_router_gb300 import build as mbuild
+from routing_grouped_expert_router_gb300 import synth
+from tests.gpu_runner import LayerRun
+from tests.helpers import conditioned_inputs, rel_l2, small_config
+
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+TOL_Y = 5e-3
+TOL_W = 1e-2
+
+CASES = {
+    "tiny": (dict(T=256, h=128, f=256, E=8, k=2, seed=0), 0),
+    "deepseek_mid": (dict(T=512, h=256, f=192, E=64, k=6, seed=1), 0),
+    "mixtral_mid": (dict(T=1024, h=512, f=1024, E=8, k=2, seed=2), 0),
+    "internal_mid_zipf": (dict(T=1024, h=384, f=448, E=32, k=3, seed=3, zipf_s=1.2), 0),
+    "hunyuan_mid": (dict(T=2048, h=320, f=576, E=16, k=1, seed=4), 0),
+    "experts_gt_tokens": (dict(T=20, h=64, f=64, E=32, k=4, seed=5), 0),
+    "one_token": (dict(T=1, h=64, f=128, E=4, k=2, seed=7), 0),
+    "ragged": (dict(T=777, h=192, f=320, E=5, k=3, seed=8), 0),
+    "ragged_capacity": (dict(T=777, h=192, f=320, E=5, k=3, seed=8), 300),
+}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mbuild.build()
+    return mb.load()
+
+
+def _to(inp, device):
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def _run(d, dev):
+    run = LayerRun(d)
+    run.fwd(dev)
+    run.bwd(dev)
+    torch.cuda.synchronize()
+    assert run.status() == mb.MOE_OK
+    return run.outputs()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_sar_layer_matches_oracle(lib, name):
+    shape, cap = CASES[name]
+    cfg = small_config(name=name, **shape)
+    inp = conditioned_inputs(cfg)
+    y, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
+                              cfg.k, capacity=cap or None)
+    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    dev = _to(inp, "cuda")
+    hb = cfg.zipf_s > 0
+    out = _run(mb.dims_of(cfg, has_bias=hb, capacity=cap, sar=True), dev)
+    n = int(ctx["offsets"][-1])
+    if cap:
+        assert n < cfg.T * cfg.k
+    np.testing.assert_array_equal(out["topk_idx"].numpy(), ctx["topk_idx"])
+    np.testing.assert_array_equal(out["offsets"].numpy(), ctx["offsets"])
+    np.testing.assert_array_equal(out["perm_src"].numpy()[:n], ctx["perm_src"])
+    np.testing.assert_array_equal(out["perm_dst"].numpy(), ctx["perm_dst"])
+    for key in ("A", "B"):
+        assert rel_l2(out[key][:n].double().numpy(), ctx[key]) <= TOL_Y, key
+    assert rel_l2(out["y"].double().numpy(), y) <= TOL_Y
+    assert rel_l2(out["dx"].double().numpy(), g["dx"]) <= TOL_Y
+    for key in ("dW1", "dW3", "dW2", "dWg"):
+        assert rel_l2(out[key].numpy(), g[key]) <= TOL_W, key
+    if cfg.k == 1:
+        assert torch.all(out["dWg"] == 0)
+    for e in np.nonzero(ctx["counts"] == 0)[0]:
+        assert torch.all(out["dW1"][e] == 0) and torch.all(out["dW2"][e] == 0)
+    # same forward kernels as the default mode: y is bitwise the same
+    ref = _run(mb.dims_of(cfg, has_bias=hb, capacity=cap), dev)
+    assert torch.equal(out["y"].view(torch.int16), ref["y"].view(torch.int16))
+    assert torch.equal(out["A"].view(torch.int16), ref["A"].view(torch.int16))
+
+
+def test_sar_deterministic_and_empty(lib):
+    cfg = small_config(name="det", T=1024, h=384, f=448, E=32, k=3, seed=3, zipf_s=1.2)
+    dev = _to(conditioned_inputs(cfg), "cuda")
+    d = mb.dims_of(cfg, has_bias=True, sar=True)
+    a, b = _run(d, dev), _run(d, dev)
+    for key in a:
+        x, y = a[key], b[key]
+        assert torch.equal(x.view(torch.uint8) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.uint8) if y.dtype == torch.bfloat16 else y), key
+    d0 = mb.dims(0, 128, 128, 8, 2, sar=True)
+    run = LayerRun(d0)
+    W = synth.make_layer(small_config(T=1, h=128, f=128, E=8, k=2), "cuda")
+    W["x"] = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    W["dy"] = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    run.dW2.fill_(3)
+    run.fwd(W)
+    run.bwd(W)
+    torch.cuda.synchronize()
+    assert run.status() == mb.MOE_OK
+    assert torch.all(run.dW2 == 0) and torch.all(run.dWg == 0)

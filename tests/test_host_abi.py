@@ -148,6 +148,28 @@ def test_capacity_helper():
     assert mb.dims(4, 64, 64, 4, 2).capacity == 0
 
 
+def test_saved_bytes_follow_sar_formula(lib):
+    """moe_saved_bytes against the activation-memory formula at n = 1: the
+    MoE terms 2k + 3kf (x_perm, O; A, B, H) before selective activation
+    rematerialisation and 2kf (A, B) after, in units of T*h bf16 elements."""
+    for cfg in CONFIGS.values():
+        R, T, h, f, k = cfg.T * cfg.k, cfg.T, cfg.h, cfg.f, cfg.k
+        maps = sum(-(-n // 256) * 256 for n in (R * 4, R * 4, cfg.E * 4, (cfg.E + 1) * 4,
+                                                 R * 4, R * 4))
+        fr = f / h
+        for sar, units in ((0, 2 * k + 3 * k * fr), (1, 2 * k * fr)):
+            d = mb.dims_of(cfg, sar=sar)
+            acts = lib.moe_saved_bytes(ctypes.byref(d)) - maps
+            assert abs(acts - 2 * units * T * h) < 256 * 5, (cfg.name, sar)
+        d = mb.dims_of(cfg, sar=True)
+        for name in ("x_perm", "H", "O"):
+            assert lib.moe_saved_view(ctypes.byref(d), FAKE, name.encode()) is None
+        for name in ("A", "B", "offsets"):
+            assert lib.moe_saved_view(ctypes.byref(d), FAKE, name.encode())
+    d = _d(sar=2)
+    assert lib.moe_saved_bytes(ctypes.byref(d)) == 0
+
+
 def test_profile_hook_without_events(lib):
     assert mb.moe_profile_events(None, 0) == 0
     assert mb.moe_profile_kernel_name(-1) == ""
