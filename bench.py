@@ -33,7 +33,8 @@ from routing_grouped_expert_router_gb300 import metrics  # noqa: E402
 from routing_grouped_expert_router_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s fwd+bwd; GroupedGEMM TFLOP/s as % of GB300 BF16 peak"
-GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc2_dgrad_swiglu_bwd",
+GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc1_fwd_swiglu_fp8", "gg_fc2_fwd_fp8",
+         "gg_fc2_dgrad_swiglu_bwd",
          "gg_fc2_dgrad_swiglu_bwd_sar", "gg_fc2_wgrad", "gg_fc1_dgrad", "gg_fc1_wgrad")
 
 
@@ -58,6 +59,8 @@ def parse():
                    help="selective activation rematerialisation: keep A, B only")
     p.add_argument("--capacity-factor", type=float, default=0.0,
                    help="per-expert capacity = ceil(cf * T * k / E); 0 = dropless")
+    p.add_argument("--fp8", action="store_true",
+                   help="e4m3 expert forward (weights quantised inside every step)")
     return p.parse_args()
 
 
@@ -152,16 +155,19 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our layer ---
 class Layer:
-    def __init__(self, cfg, device, sar=False, capacity=0):
+    def __init__(self, cfg, device, sar=False, capacity=0, fp8=False):
         from routing_grouped_expert_router_gb300 import binding as mb
         self.mb = mb
         self.cfg = cfg
+        self.fp8 = fp8
         self.d = mb.dims_of(cfg, capacity=capacity, sar=sar)
         T, h, f, E = cfg.T, cfg.h, cfg.f, cfg.E
         dev = device
         self.saved = torch.zeros(mb.moe_saved_bytes(self.d), dtype=torch.uint8, device=dev)
-        self.ws_f = torch.zeros(mb.moe_workspace_bytes(self.d, mb.OP_LAYER_FWD), dtype=torch.uint8,
-                                device=dev)
+        op_f = mb.OP_LAYER_FWD_FP8 if fp8 else mb.OP_LAYER_FWD
+        self.ws_f = torch.zeros(mb.moe_workspace_bytes(self.d, op_f), dtype=torch.uint8, device=dev)
+        self.qw = (torch.zeros(mb.moe_fp8_weight_bytes(self.d), dtype=torch.uint8, device=dev)
+                   if fp8 else None)
         self.ws_b = torch.zeros(mb.moe_workspace_bytes(self.d, mb.OP_LAYER_BWD), dtype=torch.uint8,
                                 device=dev)
         self.y = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
@@ -176,8 +182,13 @@ class Layer:
         x = inp["x"] if x is None else x
         dy = inp["dy"] if dy is None else dy
         b = inp["b"] if self.d.has_bias else None
-        mb.moe_layer_fwd(self.d, x, inp["Wg"], b, inp["W1"], inp["W3"], inp["W2"], self.y,
-                         self.saved, self.ws_f)
+        if self.fp8:
+            # training step: the weights changed since the last step
+            mb.moe_quantize_weights_fp8(self.d, inp["W1"], inp["W3"], inp["W2"], self.qw)
+            mb.moe_layer_fwd_fp8(self.d, x, inp["Wg"], b, self.qw, self.y, self.saved, self.ws_f)
+        else:
+            mb.moe_layer_fwd(self.d, x, inp["Wg"], b, inp["W1"], inp["W3"], inp["W2"], self.y,
+                             self.saved, self.ws_f)
         mb.moe_layer_bwd(self.d, x, dy, inp["Wg"], inp["W1"], inp["W3"], inp["W2"], self.saved,
                          self.dx, self.dWg, self.dW1, self.dW3, self.dW2, self.ws_b)
 
@@ -204,7 +215,7 @@ def run_ours(args, cfg, world, rank, local):
     inp = synth.make_layer(cfg_r, device)
     cap = (mb.capacity_for(cfg.T, cfg.k, cfg.E, args.capacity_factor)
            if args.capacity_factor > 0 else 0)
-    layer = Layer(cfg_r, device, sar=args.sar, capacity=cap)
+    layer = Layer(cfg_r, device, sar=args.sar, capacity=cap, fp8=args.fp8)
     stream = torch.cuda.current_stream(device)
 
     for _ in range(args.warmup):
@@ -435,23 +446,31 @@ def main():
                    key=lambda g: sum(r["per_kernel"][g]))
     dom_avg = sum(r["per_kernel"][dominant]) / len(r["per_kernel"][dominant])
     achieved = metrics.tflops(work["flops"][dominant], dom_avg)
+    # an e4m3 matmul is measured against twice the bf16 peak (the nominal
+    # dense fp8 : bf16 ratio, 4.5 : 2.25 PFLOP/s)
+    dom_f8 = dominant.endswith("_fp8")
+    peak_dom = peak_tf * (2.0 if dom_f8 else 1.0)
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": n,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3 fwd" if args.fp8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": workload, "T": cfg.T, "h": cfg.h, "h_ffn": cfg.f, "E": cfg.E,
                    "top_k": cfg.k, "tokens_per_gpu_per_step": cfg.T,
                    "parallelism": f"replicas{n}" if n > 1 else "single",
-                   "variant": ("sar" if args.sar else "default")
+                   "variant": ("fp8 forward, " if args.fp8 else "")
+                   + ("sar" if args.sar else "default")
                    + (f", capacity factor {args.capacity_factor}" if args.capacity_factor else
                       ", dropless"),
                    "saved_bytes": r["saved_bytes"], "kept_rows": r["kept_rows"],
                    "l2": "inputs larger than L2 (weights + activations ~ GBs per step), no flush"},
         "gemm_tflops": gemm_tflops,
         "gemm_pct_of_bf16_peak": (100.0 * gemm_tflops / peak_tf) if gemm_tflops else None,
-        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak_tf,
-                     "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": None,
-                     "peak_source": f"{peak_src} bf16 sustained"},
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": achieved,
+                     "peak": peak_dom, "unit": "TFLOP/s", "frac": achieved / peak_dom,
+                     "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained"
+                     + (" x 2 (fp8 : bf16 nominal ratio)" if dom_f8 else "")},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "kernels": kern,

@@ -97,7 +97,8 @@ typedef enum {
   MOE_OP_EXPERT_FFN_BWD = 3,
   MOE_OP_ROUTER_BWD = 4,
   MOE_OP_LAYER_FWD = 5,
-  MOE_OP_LAYER_BWD = 6
+  MOE_OP_LAYER_BWD = 6,
+  MOE_OP_LAYER_FWD_FP8 = 7
 } moe_op;
 
 /* Scratch bytes entry point `op` needs for `dims` (0 on invalid dims).  The
@@ -251,6 +252,59 @@ moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x,
                          const moe_bf16* W3, const moe_bf16* W2, moe_bf16* y,
                          void* saved, void* ws, size_t ws_bytes,
                          moe_stream_t stream);
+
+/* ---------------------------------------------------------------- FP8
+ * FP8 training with per-token quantisation instead of per-tensor (review §三
+ * 创新点 "FP8训练优化"; digest §3.4).  The expert forward matmuls run on e4m3
+ * codes (tcgen05 kind::f8f6f4) with float32 scales:
+ *   activations x_perm and H: one scale per row, s = amax(|row|) / 448;
+ *   weights: one scale per output column of each expert (amax over the
+ *   contraction dimension);
+ * q = e4m3(v / s) with an IEEE float32 division and round-to-nearest-even,
+ * saturating at 448; s = 1 for an all-zero row or column.  The matmul sums
+ * the exact code products in fp32 and multiplies by s_row * s_col.  H is
+ * quantised from its bf16 copy.  The backward is the bf16 moe_layer_bwd on
+ * the activations (A, B, H, O) this forward stores.  Requires h and f to be
+ * multiples of 128 (MOE_ERR_UNSUPPORTED otherwise). */
+
+/* Bytes of a quantised-weight buffer `qw` (0 on invalid or unsupported dims). */
+size_t moe_fp8_weight_bytes(const moe_dims* dims);
+
+/* Quantises the expert weights into `qw` (256-byte aligned, caller-owned):
+ *   "W13q" [E, 2f, h] e4m3, K-major: per expert, 128-row groups alternating
+ *          W1 columns and W3 columns (group 2j: W1[:, 128j + r], group 2j+1:
+ *          W3[:, 128j + r], r < 128; each row holds the h codes of a column);
+ *   "W2q"  [E, h, f] e4m3, K-major (row n holds the f codes of W2[:, n]);
+ *   "s1", "s3" [E, f] and "s2" [E, h] float32 column scales.
+ * Call it after every update of W1, W3, W2; moe_fp8_weight_view(name) gives
+ * each part's device address. */
+moe_status moe_quantize_weights_fp8(const moe_dims* dims, const moe_bf16* W1,
+                                    const moe_bf16* W3, const moe_bf16* W2,
+                                    void* qw, moe_stream_t stream);
+void* moe_fp8_weight_view(const moe_dims* dims, void* qw, const char* name);
+
+/* Row quantisation on its own: for p < rows, with src = idx[p] / div (or p
+ * when idx is NULL; then src_rows >= rows), q[p, :] = e4m3(in[src, :] / s[p]),
+ * s[p] = amax(|in[src, :]|) / 448.  in [src_rows, n] bf16, q [rows, n] bytes,
+ * scale [rows] float32; n a multiple of 16. */
+moe_status moe_quantize_rows_fp8(const moe_bf16* in, int64_t rows, int32_t n,
+                                 const int32_t* idx, int32_t div,
+                                 int64_t src_rows, uint8_t* q, float* scale,
+                                 moe_stream_t stream);
+
+/* moe_layer_fwd with the FP8 expert forward: route, dispatch, per-token
+ * quantisation of the permuted rows, FC1 (+SwiGLU) on e4m3 codes, per-token
+ * quantisation of H, FC2 on e4m3 codes, combine.  Weights come only from
+ * `qw` (moe_quantize_weights_fp8).  Writes y and the same `saved` context as
+ * moe_layer_fwd (A, B, H, O from the FP8 matmuls), for moe_layer_bwd.
+ * dims.sar = 1 is MOE_ERR_UNSUPPORTED here: the sar backward takes the gate
+ * gradient <dy, O> as <H, dy W2^T>, which needs O = H W2 exactly, and this
+ * O comes from the e4m3 codes of H and W2.
+ * Workspace: moe_workspace_bytes(dims, MOE_OP_LAYER_FWD_FP8). */
+moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x,
+                             const float* Wg, const float* b, const void* qw,
+                             moe_bf16* y, void* saved, void* ws,
+                             size_t ws_bytes, moe_stream_t stream);
 
 /* Whole layer backward from `saved`: writes dx [T,h] bf16 and the fp32
  * gradients dWg, dW1, dW3, dW2.  The router bias gets no gradient. */

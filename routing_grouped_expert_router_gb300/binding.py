@@ -23,7 +23,7 @@ MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
 
 OP_ROUTE, OP_PERMUTE, OP_EXPERT_FFN_FWD, OP_EXPERT_FFN_BWD, OP_ROUTER_BWD, \
-    OP_LAYER_FWD, OP_LAYER_BWD = range(7)
+    OP_LAYER_FWD, OP_LAYER_BWD, OP_LAYER_FWD_FP8 = range(8)
 
 HEADER = os.path.join(_build.ROOT, "include", "moe.h")
 
@@ -84,6 +84,12 @@ _SIGS = {
     "moe_profile_events": (_I, [_P, _I]),
     "moe_profile_kernel_name": (ctypes.c_char_p, [_I]),
     "moe_kernel_launches": (ctypes.c_int64, []),
+    "moe_fp8_weight_bytes": (_SZ, [_D]),
+    "moe_quantize_weights_fp8": (_I, [_D, _P, _P, _P, _P, _P]),
+    "moe_fp8_weight_view": (_P, [_D, _P, ctypes.c_char_p]),
+    "moe_quantize_rows_fp8": (_I, [_P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_int32,
+                                   ctypes.c_int64, _P, _P, _P]),
+    "moe_layer_fwd_fp8": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_version": (ctypes.c_char_p, []),
 }
 
@@ -92,7 +98,7 @@ def declared_symbols() -> list[str]:
     """Entry points declared in include/moe.h."""
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
 
 
 def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL:
@@ -258,3 +264,32 @@ def moe_profile_kernel_name(i: int) -> str:
 
 def moe_kernel_launches() -> int:
     return int(load().moe_kernel_launches())
+
+
+def moe_fp8_weight_bytes(d) -> int:
+    return int(load().moe_fp8_weight_bytes(ctypes.byref(d)))
+
+
+def moe_quantize_weights_fp8(d, W1, W3, W2, qw, stream=None):
+    _check(load().moe_quantize_weights_fp8(ctypes.byref(d), _addr(W1), _addr(W3), _addr(W2),
+                                           _addr(qw), _stream(stream)), "moe_quantize_weights_fp8")
+
+
+def moe_fp8_weight_view(d, qw, name: str) -> int:
+    p = load().moe_fp8_weight_view(ctypes.byref(d), _addr(qw), name.encode())
+    if not p:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"moe_fp8_weight_view({name})")
+    return int(p)
+
+
+def moe_quantize_rows_fp8(inp, rows, n, idx, div, src_rows, q, scale, stream=None):
+    _check(load().moe_quantize_rows_fp8(_addr(inp), int(rows), int(n), _addr(idx), int(div),
+                                        int(src_rows), _addr(q), _addr(scale), _stream(stream)),
+           "moe_quantize_rows_fp8")
+
+
+def moe_layer_fwd_fp8(d, x, Wg, b, qw, y, saved, ws, ws_bytes=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_layer_fwd_fp8(ctypes.byref(d), _addr(x), _addr(Wg), _addr(b), _addr(qw),
+                                    _addr(y), _addr(saved), _addr(ws), ws_bytes, _stream(stream)),
+           "moe_layer_fwd_fp8")

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 BUILDDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(LIBDIR, "libmoe_gb300.so")
-SOURCES = ["api.cu", "kernels.cu", "grouped_gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "kernels.cu", "grouped_gemm.cu", "noalloc.cu", "fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

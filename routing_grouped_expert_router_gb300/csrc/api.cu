@@ -60,8 +60,11 @@ moe_status check_dims(const moe_dims* d, bool routed) {
 }
 
 bool routed_op(int op) {
-  return op == MOE_OP_ROUTE || op == MOE_OP_LAYER_FWD || op == MOE_OP_LAYER_BWD;
+  return op == MOE_OP_ROUTE || op == MOE_OP_LAYER_FWD || op == MOE_OP_LAYER_BWD ||
+         op == MOE_OP_LAYER_FWD_FP8;
 }
+
+
 
 int num_sms() {
   static int cached[64] = {0};
@@ -85,6 +88,25 @@ struct Carve {
     return o;
   }
 };
+
+// ------------------------------------------------------ fp8 weights
+// The caller's quantised-weight buffer: codes K-major, then the scales.
+struct Fp8WeightLayout {
+  size_t W13q, W2q, s1, s3, s2, total;
+};
+Fp8WeightLayout fp8_weight_layout(const moe_dims& d) {
+  const size_t E = d.E, h = d.h, f = d.f;
+  Carve c;
+  Fp8WeightLayout L;
+  L.W13q = c.take(E * 2 * f * h);
+  L.W2q = c.take(E * h * f);
+  L.s1 = c.take(E * f * 4);
+  L.s3 = c.take(E * f * 4);
+  L.s2 = c.take(E * h * 4);
+  L.total = c.off;
+  return L;
+}
+bool fp8_shape_ok(const moe_dims& d) { return d.h % 128 == 0 && d.f % 128 == 0; }
 
 size_t rows_of(const moe_dims& d) { return static_cast<size_t>(d.T) * d.k; }
 
@@ -126,6 +148,7 @@ struct WsLayout {
   size_t logits = 0;                         // router partial logits
   size_t H = 0, O = 0;                       // sar forward: activations not kept
   size_t gH = 0, gate_rows = 0, dg_part = 0;  // sar backward
+  size_t Xq = 0, sx = 0, Hq = 0, sh = 0;     // fp8 forward
   size_t total = 0;
 };
 WsLayout ws_layout(const moe_dims& d, int op) {
@@ -157,8 +180,15 @@ WsLayout ws_layout(const moe_dims& d, int op) {
     case MOE_OP_EXPERT_FFN_BWD: expert_bwd(true); break;
     case MOE_OP_ROUTER_BWD: router_bwd(); break;
     case MOE_OP_LAYER_FWD:
+    case MOE_OP_LAYER_FWD_FP8:
       route();
       dispatch();
+      if (op == MOE_OP_LAYER_FWD_FP8) {
+        L.Xq = c.take(R * d.h);
+        L.sx = c.take(R * 4);
+        L.Hq = c.take(R * d.f);
+        L.sh = c.take(R * 4);
+      }
       if (d.sar) {
         L.x_perm = c.take(R * d.h * 2);
         L.H = c.take(R * d.f * 2);
@@ -610,6 +640,121 @@ moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* W
   if ((st = do_ffn_fwd(d, xp, offsets, W1, W3, W2, at<uint16_t>(saved, S.A),
                        at<uint16_t>(saved, S.B), H, O, ws, stream)) != MOE_OK)
     return st;
+  MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
+  return MOE_OK;
+}
+
+size_t moe_fp8_weight_bytes(const moe_dims* dims) {
+  if (check_dims(dims, false) != MOE_OK || !fp8_shape_ok(*dims)) return 0;
+  return fp8_weight_layout(*dims).total;
+}
+
+void* moe_fp8_weight_view(const moe_dims* dims, void* qw, const char* name) {
+  if (check_dims(dims, false) != MOE_OK || !fp8_shape_ok(*dims) || !qw || !name) return nullptr;
+  const Fp8WeightLayout L = fp8_weight_layout(*dims);
+  struct {
+    const char* n;
+    size_t off;
+  } tab[] = {{"W13q", L.W13q}, {"W2q", L.W2q}, {"s1", L.s1}, {"s3", L.s3}, {"s2", L.s2}};
+  for (auto& e : tab)
+    if (strcmp(e.n, name) == 0) return at<uint8_t>(qw, e.off);
+  return nullptr;
+}
+
+moe_status moe_quantize_weights_fp8(const moe_dims* dims, const moe_bf16* W1, const moe_bf16* W3,
+                                    const moe_bf16* W2, void* qw, moe_stream_t stream_) {
+  moe_status st = check_dims(dims, false);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!fp8_shape_ok(d)) return MOE_ERR_UNSUPPORTED;
+  if (!ptr_ok(W1) || !ptr_ok(W3) || !ptr_ok(W2) || !qw || !aligned(qw, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const Fp8WeightLayout L = fp8_weight_layout(d);
+  uint8_t* W13q = at<uint8_t>(qw, L.W13q);
+  // W1, W3 [E, h, f] -> interleaved 128-row groups of W13q [E, 2f, h]
+  MOE_RUN(moe::launch_quant_cols(W1, d.E, d.h, d.f, 2 * d.f, 256, 0, W13q, at<float>(qw, L.s1),
+                                 stream),
+          "quant_w1");
+  MOE_RUN(moe::launch_quant_cols(W3, d.E, d.h, d.f, 2 * d.f, 256, 1, W13q, at<float>(qw, L.s3),
+                                 stream),
+          "quant_w3");
+  // W2 [E, f, h] -> W2q [E, h, f]
+  MOE_RUN(moe::launch_quant_cols(W2, d.E, d.f, d.h, d.h, 128, 0, at<uint8_t>(qw, L.W2q),
+                                 at<float>(qw, L.s2), stream),
+          "quant_w2");
+  return MOE_OK;
+}
+
+moe_status moe_quantize_rows_fp8(const moe_bf16* in, int64_t rows, int32_t n, const int32_t* idx,
+                                 int32_t div, int64_t src_rows, uint8_t* q, float* scale,
+                                 moe_stream_t stream_) {
+  if (rows < 0 || src_rows < 0 || n <= 0 || n % 16 != 0 || (idx && div <= 0))
+    return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && (!ptr_ok(in) || !ptr_ok(q) || !ptr_ok(scale) || (idx && !ptr_ok(idx))))
+    return MOE_ERR_INVALID_ARG;
+  if (rows > 0 && !idx && src_rows < rows) return MOE_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  MOE_RUN(moe::launch_quant_rows(in, idx, idx ? div : 1, rows, src_rows, n, q, scale, num_sms(),
+                                 stream),
+          "quant_rows");
+  return MOE_OK;
+}
+
+moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x, const float* Wg,
+                             const float* b, const void* qw, moe_bf16* y, void* saved, void* ws,
+                             size_t ws_bytes, moe_stream_t stream_) {
+  moe_status st = check_dims(dims, true);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!fp8_shape_ok(d)) return MOE_ERR_UNSUPPORTED;
+  // The sar backward takes <dy, O> as <H, dy W2^T>, which needs O = H W2
+  // exactly; here O comes from the e4m3 codes of H and W2.
+  if (d.sar) return MOE_ERR_UNSUPPORTED;
+  const size_t T = d.T;
+  if (!buf_ok(x, T) || !ptr_ok(Wg) || !qw || !aligned(qw, kAlign) || !buf_ok(y, T) ||
+      (d.has_bias && !ptr_ok(b)) || !saved || !aligned(saved, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_LAYER_FWD_FP8, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_LAYER_FWD_FP8);
+  const SavedLayout S = saved_layout(d);
+  const Fp8WeightLayout Q = fp8_weight_layout(d);
+  int32_t* idx = at<int32_t>(saved, S.topk_idx);
+  float* gates = at<float>(saved, S.gates);
+  int32_t* offsets = at<int32_t>(saved, S.offsets);
+  int32_t* psrc = at<int32_t>(saved, S.perm_src);
+  int32_t* pdst = at<int32_t>(saved, S.perm_dst);
+  uint16_t* H = at<uint16_t>(saved, S.H);
+  uint16_t* O = at<uint16_t>(saved, S.O);
+  uint8_t* Xq = at<uint8_t>(ws, L.Xq);
+  uint8_t* Hq = at<uint8_t>(ws, L.Hq);
+  float* sx = at<float>(ws, L.sx);
+  float* sh = at<float>(ws, L.sh);
+  const long long R = static_cast<long long>(rows_of(d));
+  const int32_t* nvalid = offsets + d.E;
+  if ((st = do_route(d, x, Wg, b, idx, gates, ws, L, stream)) != MOE_OK) return st;
+  if ((st = do_dispatch(d, selection(d, 0, d.E), idx, at<int32_t>(saved, S.counts), offsets, psrc,
+                        pdst, ws, L, stream)) != MOE_OK)
+    return st;
+  // the backward's FC1 weight gradient takes the bf16 rows
+  MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, R, d.T, d.h, at<uint16_t>(saved, S.x_perm),
+                                  num_sms(), stream, nvalid),
+          "permute_rows");
+  MOE_RUN(moe::launch_quant_rows(x, psrc, d.k, R, d.T, d.h, Xq, sx, num_sms(), stream, nvalid),
+          "quant_x_perm");
+  if (R > 0) {
+    const GemmProblem g = problem(d, offsets, ws);
+    MOE_RUN(moe::gemm_fc1_fwd_fp8(g, Xq, sx, at<uint8_t>(qw, Q.W13q), at<float>(qw, Q.s1),
+                                  at<float>(qw, Q.s3), at<uint16_t>(saved, S.A),
+                                  at<uint16_t>(saved, S.B), H, stream),
+            "gg_fc1_fwd_swiglu_fp8");
+    MOE_RUN(moe::launch_quant_rows(H, nullptr, 1, R, R, d.f, Hq, sh, num_sms(), stream, nvalid),
+            "quant_h");
+    MOE_RUN(moe::gemm_fc2_fwd_fp8(g, Hq, sh, at<uint8_t>(qw, Q.W2q), at<float>(qw, Q.s2), O,
+                                  stream),
+            "gg_fc2_fwd_fp8");
+  }
   MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
   return MOE_OK;
 }

@@ -72,8 +72,17 @@ enum Epi {
   EPI_SWIGLU_BWD = 2,
   EPI_F32 = 3,
   EPI_WGRAD = 4,
-  EPI_SWIGLU_BWD_SAR = 5  // SwiGLU backward that rebuilds H from A, B (no saved H or O)
+  EPI_SWIGLU_BWD_SAR = 5,  // SwiGLU backward that rebuilds H from A, B (no saved H or O)
+  EPI_SWIGLU_F8 = 6,       // EPI_SWIGLU on e4m3 operands: sums rescaled by row x column scales
+  EPI_BF16_F8 = 7          // EPI_BF16 on e4m3 operands, likewise
 };
+__host__ __device__ constexpr bool is_f8(int epi) {
+  return epi == EPI_SWIGLU_F8 || epi == EPI_BF16_F8;
+}
+// The epilogue an FP8 matmul runs after rescaling its sums.
+__host__ __device__ constexpr int base_epi(int epi) {
+  return epi == EPI_SWIGLU_F8 ? EPI_SWIGLU : (epi == EPI_BF16_F8 ? EPI_BF16 : epi);
+}
 
 struct Params {
   int E;
@@ -92,6 +101,9 @@ struct Params {
   const float* in2;  // EPI_SWIGLU_BWD_SAR: gate of each permuted row
   float* part;       // EPI_SWIGLU_BWD_SAR: per-(row, n-tile) partial sums of <H, dY W2^T>
   int part_ld;       // n-tiles per row of `part`
+  const float* row_scale;   // FP8: scale of each A row (permuted row)
+  const float* col_scale0;  // FP8: [E, N] scales of the B columns (first operand)
+  const float* col_scale1;  // FP8: [E, N] scales of the second operand's columns
   int ldo;           // row stride (elements) of M-grouped outputs and inputs
   int* status;
   int ktiles;        // K-grouped: tiles in total
@@ -195,10 +207,11 @@ __device__ __forceinline__ void store_f32x32(void* dst, const float* v) {
 // One 32-column chunk of the epilogue for one accumulator row.
 //   grow: M-grouped output row (permuted row);  orow: K-grouped output row.
 //   v0 (and v1 for two B operands): the fp32 accumulator values.
-template <int NUM_B, int EPI>
+template <int NUM_B, int EPI_>
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, int grow, int orow,
                                                int col, const float* v0, const float* v1,
                                                float& acc) {
+  constexpr int EPI = base_epi(EPI_);
   if (EPI == EPI_SWIGLU) {
     const size_t o = static_cast<size_t>(grow) * p.ldo + col;
     float hv[32];
@@ -262,6 +275,21 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, 
   }
 }
 
+// FP8: the sums of e4m3 products times the row's and the columns' scales.
+template <int NUM_B>
+__device__ __forceinline__ void rescale_f8(const Params& p, const Tile& tl, int grow, int col,
+                                           float* v0, float* v1) {
+  const float sr = __ldg(p.row_scale + grow);
+  const float* c0 = p.col_scale0 + static_cast<size_t>(tl.e) * p.N + col;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v0[i] *= sr * __ldg(c0 + i);
+  if (NUM_B == 2) {
+    const float* c1 = p.col_scale1 + static_cast<size_t>(tl.e) * p.N + col;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v1[i] *= sr * __ldg(c1 + i);
+  }
+}
+
 // Weight gradient of an expert without tokens: zeros for this row's columns.
 template <int NUM_B>
 __device__ __forceinline__ void zero_wgrad_row(const Params& p, const Tile& tl, int orow) {
@@ -303,6 +331,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr int BNB = BN / NUM_B;  // accumulator columns per B operand
+  constexpr bool F8 = is_f8(EPI);  // e4m3 operands (K-major only): 128 per 128-byte row
+  constexpr int BKE = F8 ? 2 * BK : BK;  // K elements per stage
+  static_assert(!F8 || (!A_MN && !B_MN && !GROUP_K), "FP8 matmuls take K-major operands");
 
   // ------------------------------------------------------------ set-up
   if (warp == 0 && lane == 0) {
@@ -367,11 +398,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b_dst = a_dst + A_BYTES;
           if (!GROUP_K) {
             const bool second = p.kconcat == 2 && kb >= p.kblocks;
-            const int kx = (second ? kb - p.kblocks : kb) * BK;
+            const int kx = (second ? kb - p.kblocks : kb) * BKE;
             tma_load_2d(a_dst, second ? &maps.a1 : &maps.a0, kx, tl.row0, full);
             if (!B_MN) {
-              tma_load_2d(b_dst, second ? &maps.b1 : &maps.b0, kx, tl.e * p.b_rows + tl.nb * BNB,
-                          full);
+              // FP8 FC1: one 256-row tile of the interleaved W1/W3 operand
+              tma_load_2d(b_dst, second ? &maps.b1 : &maps.b0, kx,
+                          tl.e * p.b_rows + tl.nb * (F8 ? BN : BNB), full);
             } else {
 #pragma unroll
               for (int i = 0; i < NUM_B; ++i)
@@ -407,8 +439,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // MN-major B tiles are stored as 64-column chunks 8 KiB apart, so the two
     // 128-column operands of NUM_B = 2 form one 256-column operand: a single
     // N = 256 MMA fills both accumulators and reads the A tile once per K step.
-    constexpr bool B_FUSED = B_MN || NUM_B == 1;
-    constexpr uint32_t IDESC = idesc_bf16(BM, B_FUSED ? BN : BNB, A_MN, B_MN);
+    constexpr bool B_FUSED = B_MN || NUM_B == 1 || F8;
+    constexpr uint32_t IDESC =
+        F8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, B_FUSED ? BN : BNB, A_MN, B_MN);
     constexpr uint32_t A_LBO = A_MN ? CHUNK_BYTES : 16;
     constexpr uint32_t B_LBO = B_MN ? CHUNK_BYTES : 16;
     constexpr uint32_t A_KSTEP = A_MN ? 2048 : 32;  // bytes per 16-deep K step
@@ -448,7 +481,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = smem_desc(a_base + kk * A_KSTEP, A_LBO, 1024);
-            if (B_FUSED) {
+            if (F8) {
+              umma_e4m3(acc, ad, smem_desc(b_base + kk * B_KSTEP, B_LBO, 1024), IDESC,
+                        (kb | kk) != 0);
+            } else if (B_FUSED) {
               umma_bf16(acc, ad, smem_desc(b_base + kk * B_KSTEP, B_LBO, 1024), IDESC,
                         (kb | kk) != 0);
             } else {
@@ -506,6 +542,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
         const int col = tl.nb * BNB + ch * 32;
         if (!row_ok || col >= p.N) continue;
+        if (is_f8(EPI)) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
         epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1, acc);
       }
       if (EPI == EPI_SWIGLU_BWD_SAR && row_ok)
@@ -857,14 +894,15 @@ EncodeTiledFn encode_fn() {
 
 // bf16 matrix [outer, inner] (row-major), box {box_inner, box_outer}, 128B swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer) {
+              uint32_t box_inner, uint32_t box_outer, bool bytes = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * (bytes ? 1 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -881,6 +919,7 @@ int forced_ctas() {
   return v;
 }
 bool pair_for(int epi) {
+  if (is_f8(epi)) return false;  // the FP8 matmuls run on the one-CTA kernel only
   if (forced_ctas()) return forced_ctas() == 2;
   return epi == EPI_SWIGLU_BWD || epi == EPI_SWIGLU_BWD_SAR || epi == EPI_F32;
 }
@@ -889,7 +928,7 @@ template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
 cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num_sms,
                    cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
-  if (!pair_for(EPI)) {
+  if (is_f8(EPI) || !pair_for(EPI)) {
     auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -902,40 +941,44 @@ cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(prm, maps);
     return launched();
   }
-  auto kern = gg2_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
-  static bool attr2_set = false;
-  if (!attr2_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
-    if (e != cudaSuccess) return e;
-    attr2_set = true;
+  if constexpr (is_f8(EPI)) {
+    return cudaErrorInvalidValue;
+  } else {
+    auto kern = gg2_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
+    static bool attr2_set = false;
+    if (!attr2_set) {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+      if (e != cudaSuccess) return e;
+      attr2_set = true;
+    }
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM2_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // A persistent grid must fit on the GPU at once: SMs that cannot pair up
+    // inside their GPC host no cluster, so size the grid by what is co-resident.
+    static int max_clusters = 0;
+    if (max_clusters == 0) {
+      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
+      max_clusters = n;
+    }
+    g_pair_clusters = max_clusters;
+    const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm, maps);
+    return e == cudaSuccess ? launched() : e;
   }
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM2_BYTES;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // A persistent grid must fit on the GPU at once: SMs that cannot pair up
-  // inside their GPC host no cluster, so size the grid by what is co-resident.
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
-    max_clusters = n;
-  }
-  g_pair_clusters = max_clusters;
-  const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm, maps);
-  return e == cudaSuccess ? launched() : e;
 }
 
 Params base_params(const GemmProblem& g) {
@@ -1033,6 +1076,56 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
 }
 
 int gemm_col_tiles(int n) { return (n + BN - 1) / BN; }
+
+// FP8 forward.  Operands are e4m3 codes, K-major, one byte each: a K block is
+// 128 codes (one 128-byte swizzled row), and the MMA is kind::f8f6f4.
+cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& g, const void* Xq, const float* sx,
+                             const void* W13q, const float* s1, const float* s3, void* A, void* B,
+                             void* H, cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  // A: Xq [rows, h];  B: W13q viewed as [E * 2f rows (N), h (K)], 256-row tiles
+  if (!make_map(&m.a0, Xq, g.h, g.rows, 2 * BK, BM, true) ||
+      !make_map(&m.b0, W13q, g.h, static_cast<uint64_t>(g.E) * 2 * g.f, 2 * BK, BN, true))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Params p = base_params(g);
+  p.N = g.f;
+  p.kblocks = g.h / (2 * BK);
+  p.b_rows = 2 * g.f;
+  p.row_scale = sx;
+  p.col_scale0 = s1;
+  p.col_scale1 = s3;
+  p.out0 = A;
+  p.out1 = B;
+  p.out2 = H;
+  p.ldo = g.f;
+  return launch<false, false, 2, EPI_SWIGLU_F8, false>(
+      p, m, mgrouped_tiles(g, EPI_SWIGLU_F8, g.f, BN / 2), g.num_sms, s);
+}
+
+cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& g, const void* Hq, const float* sh,
+                             const void* W2q, const float* s2, void* O, cudaStream_t s) {
+  Maps m;
+  memset(&m, 0, sizeof(m));
+  // A: Hq [rows, f];  B: W2q viewed as [E * h rows (N), f (K)]
+  if (!make_map(&m.a0, Hq, g.f, g.rows, 2 * BK, BM, true) ||
+      !make_map(&m.b0, W2q, g.f, static_cast<uint64_t>(g.E) * g.h, 2 * BK, BN, true))
+    return cudaErrorInvalidValue;
+  m.a1 = m.a0;
+  m.b1 = m.b0;
+  Params p = base_params(g);
+  p.N = g.h;
+  p.kblocks = g.f / (2 * BK);
+  p.b_rows = g.h;
+  p.row_scale = sh;
+  p.col_scale0 = s2;
+  p.out0 = O;
+  p.ldo = g.h;
+  return launch<false, false, 1, EPI_BF16_F8, false>(p, m, mgrouped_tiles(g, EPI_BF16_F8, g.h, BN),
+                                                     g.num_sms, s);
+}
 
 cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& g, const void* dy_perm, const void* W2,
                                const void* A, const void* B, const float* gate_rows, void* dA,

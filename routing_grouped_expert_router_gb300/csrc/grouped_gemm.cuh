@@ -38,6 +38,17 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& p, const void* dO, const void* W2,
 cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& p, const void* dy_perm, const void* W2,
                                const void* A, const void* B, const float* gate_rows, void* dA,
                                void* dB, void* gH, float* dg_part, cudaStream_t s);
+// FP8 forward (e4m3 codes, per-row and per-column float32 scales; h and f
+// multiples of 128):
+//   A = sx * s1 * (Xq W1q), B = sx * s3 * (Xq W3q), H = silu(A) * B   (bf16 out)
+//   Xq [rows, h]; W13q [E, 2f, h] with 128-row groups alternating W1 and W3
+//   columns; s1, s3 [E, f]; sx [rows].
+cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& p, const void* Xq, const float* sx,
+                             const void* W13q, const float* s1, const float* s3, void* A, void* B,
+                             void* H, cudaStream_t s);
+//   O = sh * s2 * (Hq W2q): Hq [rows, f]; W2q [E, h, f]; s2 [E, h]; sh [rows].
+cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& p, const void* Hq, const float* sh,
+                             const void* W2q, const float* s2, void* O, cudaStream_t s);
 // Output-column tiles of the M-grouped matmuls for n columns.
 int gemm_col_tiles(int n);
 // dX_perm = dA W1^T + dB W3^T (K = 2f), fp32 [rows, h].

@@ -1,0 +1,160 @@
+"""GPU parity of the FP8 (e4m3, per-token scale) expert forward with the
+oracle's FP8 forward.
+
+Bit-exact: every weight code and scale (moe_quantize_weights_fp8) and every
+code and scale of the permuted token rows (moe_quantize_rows_fp8), since both
+come from exact bf16 inputs.  Floating point: A, B, H, O, y relative L2
+<= 5e-3 against the oracle run with the same quantisation (the remaining
+differences are fp32 summation order and bf16 storage); the bf16 backward on
+the FP8 activations at the default tolerances (dx <= 5e-3, weight and router
+gradients <= 1e-2).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routing_grouped_expert_router_gb300 import binding as mb
+from routing_grouped_expert_router_gb300 import build as mbuild
+from tests.gpu_runner import LayerRun, workspace
+from tests.helpers import conditioned_inputs, rel_l2, small_config
+
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+TOL_Y = 5e-3
+TOL_W = 1e-2
+
+CASES = {
+    "tiny": dict(T=256, h=128, f=256, E=8, k=2, seed=0),
+    "deepseek_mid": dict(T=512, h=256, f=256, E=64, k=6, seed=1),
+    "mixtral_mid": dict(T=1024, h=512, f=1024, E=8, k=2, seed=2),
+    "internal_mid_zipf": dict(T=1024, h=384, f=512, E=32, k=3, seed=3, zipf_s=1.2),
+    "hunyuan_mid": dict(T=2048, h=384, f=640, E=16, k=1, seed=4),
+    "one_token": dict(T=1, h=128, f=128, E=4, k=2, seed=7),
+    "ragged_tokens": dict(T=777, h=256, f=384, E=5, k=3, seed=8),
+}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mbuild.build()
+    return mb.load()
+
+
+def _to(inp, device):
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def _codes(t: torch.Tensor) -> np.ndarray:
+    """e4m3 bytes -> their exact values."""
+    return t.cpu().view(torch.float8_e4m3fn).float().double().numpy()
+
+
+def _view(d, qw, name, shape, dtype):
+    off = mb.moe_fp8_weight_view(d, qw, name) - qw.data_ptr()
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    return qw[off:off + n].view(dtype).view(shape)
+
+
+def _quant_weights(d, dev):
+    qw = torch.zeros(mb.moe_fp8_weight_bytes(d), dtype=torch.uint8, device="cuda")
+    mb.moe_quantize_weights_fp8(d, dev["W1"], dev["W3"], dev["W2"], qw)
+    return qw
+
+
+def test_weight_codes_and_scales_bit_exact(lib):
+    cfg = small_config(name="wq", T=8, h=384, f=640, E=3, k=2, seed=21)
+    inp = conditioned_inputs(cfg)
+    d = mb.dims_of(cfg, has_bias=False)
+    qw = _quant_weights(d, _to(inp, "cuda"))
+    torch.cuda.synchronize()
+    E, h, f = cfg.E, cfg.h, cfg.f
+    W1q, s1 = oracle.quantize_cols_e4m3(oracle.as_f64(inp["W1"]))
+    W3q, s3 = oracle.quantize_cols_e4m3(oracle.as_f64(inp["W3"]))
+    W2q, s2 = oracle.quantize_cols_e4m3(oracle.as_f64(inp["W2"]))
+    np.testing.assert_array_equal(_view(d, qw, "s1", (E, f), torch.float32).cpu().numpy(), s1)
+    np.testing.assert_array_equal(_view(d, qw, "s3", (E, f), torch.float32).cpu().numpy(), s3)
+    np.testing.assert_array_equal(_view(d, qw, "s2", (E, h), torch.float32).cpu().numpy(), s2)
+    W13 = _codes(_view(d, qw, "W13q", (E, f // 128, 2, 128, h), torch.uint8))
+    np.testing.assert_array_equal(W13[:, :, 0].reshape(E, f, h), np.transpose(W1q, (0, 2, 1)))
+    np.testing.assert_array_equal(W13[:, :, 1].reshape(E, f, h), np.transpose(W3q, (0, 2, 1)))
+    W2 = _codes(_view(d, qw, "W2q", (E, h, f), torch.uint8))
+    np.testing.assert_array_equal(W2, np.transpose(W2q, (0, 2, 1)))
+
+
+def test_row_codes_and_scales_bit_exact(lib):
+    cfg = small_config(name="xq", T=333, h=512, f=128, E=8, k=2, seed=22)
+    inp = conditioned_inputs(cfg)
+    inp["x"][17] = 0                               # a zero row: scale 1, codes 0
+    _, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
+                              cfg.k)
+    R = cfg.T * cfg.k
+    q = torch.empty(R, cfg.h, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(R, dtype=torch.float32, device="cuda")
+    psrc = torch.from_numpy(ctx["perm_src"]).cuda()
+    mb.moe_quantize_rows_fp8(inp["x"].cuda(), R, cfg.h, psrc, cfg.k, cfg.T, q, sc)
+    torch.cuda.synchronize()
+    Xq, sx = oracle.quantize_rows_e4m3(ctx["x_perm"])
+    np.testing.assert_array_equal(sc.cpu().numpy(), sx)
+    np.testing.assert_array_equal(_codes(q), Xq)
+    assert np.sum(sx == 1.0) == cfg.k
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fp8_layer_matches_fp8_oracle(lib, name):
+    cfg = small_config(name=name, **CASES[name])
+    inp = conditioned_inputs(cfg)
+    y, ctx = oracle.layer_fwd_fp8(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
+                                  inp["W2"], cfg.k)
+    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    dev = _to(inp, "cuda")
+    d = mb.dims_of(cfg, has_bias=cfg.zipf_s > 0)
+    qw = _quant_weights(d, dev)
+    run = LayerRun(d)
+    ws = workspace(d, mb.OP_LAYER_FWD_FP8)
+    mb.moe_layer_fwd_fp8(d, dev["x"], dev["Wg"], dev["b"] if d.has_bias else None, qw, run.y,
+                         run.saved, ws)
+    run.bwd(dev)
+    torch.cuda.synchronize()
+    assert mb.moe_read_device_status(ws) == mb.MOE_OK and run.status() == mb.MOE_OK
+    out = run.outputs()
+    np.testing.assert_array_equal(out["topk_idx"].numpy(), ctx["topk_idx"])
+    np.testing.assert_array_equal(out["perm_src"].numpy(), ctx["perm_src"])
+    np.testing.assert_array_equal(out["x_perm"].double().numpy(), ctx["x_perm"])
+    for key in ("A", "B", "H", "O"):
+        assert rel_l2(out[key].double().numpy(), ctx[key]) <= TOL_Y, key
+    assert rel_l2(out["y"].double().numpy(), y) <= TOL_Y
+    assert rel_l2(out["dx"].double().numpy(), g["dx"]) <= TOL_Y
+    for key in ("dW1", "dW3", "dW2", "dWg"):
+        assert rel_l2(out[key].numpy(), g[key]) <= TOL_W, key
+
+
+def test_fp8_layer_with_capacity(lib):
+    cfg = small_config(name="fp8_cap", T=1024, h=512, f=1024, E=8, k=2, seed=2)
+    inp = conditioned_inputs(cfg)
+    cap = mb.capacity_for(cfg.T, cfg.k, cfg.E, 1.0)
+    y, ctx = oracle.layer_fwd_fp8(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
+                                  inp["W2"], cfg.k, capacity=cap)
+    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    assert int(ctx["offsets"][-1]) < cfg.T * cfg.k
+    dev = _to(inp, "cuda")
+    d = mb.dims_of(cfg, has_bias=False, capacity=cap)
+    qw = _quant_weights(d, dev)
+    run = LayerRun(d)
+    ws = workspace(d, mb.OP_LAYER_FWD_FP8)
+    mb.moe_layer_fwd_fp8(d, dev["x"], dev["Wg"], None, qw, run.y, run.saved, ws)
+    run.bwd(dev)
+    torch.cuda.synchronize()
+    assert mb.moe_read_device_status(ws) == mb.MOE_OK and run.status() == mb.MOE_OK
+    out = run.outputs()
+    assert rel_l2(out["y"].double().numpy(), y) <= TOL_Y
+    assert rel_l2(out["dx"].double().numpy(), g["dx"]) <= TOL_Y
+    for key in ("dW1", "dW3", "dW2", "dWg"):
+        assert rel_l2(out[key].numpy(), g[key]) <= TOL_W, key
+    # the sar context does not combine with the FP8 forward
+    ds = mb.dims_of(cfg, has_bias=False, capacity=cap, sar=True)
+    with pytest.raises(mb.MoeError) as err:
+        mb.moe_layer_fwd_fp8(ds, dev["x"], dev["Wg"], None, qw, run.y, run.saved, ws)
+    assert err.value.status == mb.MOE_ERR_UNSUPPORTED

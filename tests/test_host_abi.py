@@ -170,6 +170,28 @@ def test_saved_bytes_follow_sar_formula(lib):
     assert lib.moe_saved_bytes(ctypes.byref(d)) == 0
 
 
+def test_fp8_shape_and_argument_checks(lib):
+    d = _d(h=192)                                # h not a multiple of 128
+    assert lib.moe_fp8_weight_bytes(ctypes.byref(d)) == 0
+    assert lib.moe_quantize_weights_fp8(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, None) \
+        == mb.MOE_ERR_UNSUPPORTED
+    d = _d(h=256, f=384, E=4)
+    need = lib.moe_fp8_weight_bytes(ctypes.byref(d))
+    assert need >= 4 * (2 * 384 * 256 + 256 * 384) + 4 * 4 * (384 * 2 + 256)
+    assert lib.moe_quantize_weights_fp8(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE + 16, None) \
+        == mb.MOE_ERR_INVALID_ARG
+    offs = [mb.moe_fp8_weight_view(d, FAKE, n) - FAKE for n in ("W13q", "W2q", "s1", "s3", "s2")]
+    assert offs == sorted(offs) and offs[-1] < need and all(o % 256 == 0 for o in offs)
+    ws = lib.moe_workspace_bytes(ctypes.byref(d), mb.OP_LAYER_FWD_FP8)
+    assert ws >= lib.moe_workspace_bytes(ctypes.byref(d), mb.OP_LAYER_FWD) + 64 * 2 * (256 + 384)
+    assert lib.moe_layer_fwd_fp8(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, ws - 1,
+                                 None) == mb.MOE_ERR_WORKSPACE
+    assert lib.moe_quantize_rows_fp8(FAKE, 4, 24, None, 1, 4, FAKE, FAKE, None) \
+        == mb.MOE_ERR_INVALID_ARG           # n not a multiple of 16
+    assert lib.moe_quantize_rows_fp8(FAKE, 8, 32, None, 1, 4, FAKE, FAKE, None) \
+        == mb.MOE_ERR_INVALID_ARG           # rows beyond the source without idx
+
+
 def test_profile_hook_without_events(lib):
     assert mb.moe_profile_events(None, 0) == 0
     assert mb.moe_profile_kernel_name(-1) == ""
