@@ -149,6 +149,7 @@ struct WsLayout {
   size_t H = 0, O = 0;                       // sar forward: activations not kept
   size_t gH = 0, gate_rows = 0, dg_part = 0;  // sar backward
   size_t Xq = 0, sx = 0, Hq = 0, sh = 0;     // fp8 forward
+  size_t h_amax = 0;                         // fp8 forward: per-tile amax of H
   size_t total = 0;
 };
 WsLayout ws_layout(const moe_dims& d, int op) {
@@ -188,6 +189,7 @@ WsLayout ws_layout(const moe_dims& d, int op) {
         L.sx = c.take(R * 4);
         L.Hq = c.take(R * d.f);
         L.sh = c.take(R * 4);
+        L.h_amax = c.take(R * static_cast<size_t>(moe::gemm_fc1_col_tiles(d.f)) * 4);
       }
       if (d.sar) {
         L.x_perm = c.take(R * d.h * 2);
@@ -674,14 +676,14 @@ moe_status moe_quantize_weights_fp8(const moe_dims* dims, const moe_bf16* W1, co
   uint8_t* W13q = at<uint8_t>(qw, L.W13q);
   // W1, W3 [E, h, f] -> interleaved 128-row groups of W13q [E, 2f, h]
   MOE_RUN(moe::launch_quant_cols(W1, d.E, d.h, d.f, 2 * d.f, 256, 0, W13q, at<float>(qw, L.s1),
-                                 stream),
+                                 num_sms(), stream),
           "quant_w1");
   MOE_RUN(moe::launch_quant_cols(W3, d.E, d.h, d.f, 2 * d.f, 256, 1, W13q, at<float>(qw, L.s3),
-                                 stream),
+                                 num_sms(), stream),
           "quant_w3");
   // W2 [E, f, h] -> W2q [E, h, f]
   MOE_RUN(moe::launch_quant_cols(W2, d.E, d.f, d.h, d.h, 128, 0, at<uint8_t>(qw, L.W2q),
-                                 at<float>(qw, L.s2), stream),
+                                 at<float>(qw, L.s2), num_sms(), stream),
           "quant_w2");
   return MOE_OK;
 }
@@ -747,9 +749,10 @@ moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x, const floa
     const GemmProblem g = problem(d, offsets, ws);
     MOE_RUN(moe::gemm_fc1_fwd_fp8(g, Xq, sx, at<uint8_t>(qw, Q.W13q), at<float>(qw, Q.s1),
                                   at<float>(qw, Q.s3), at<uint16_t>(saved, S.A),
-                                  at<uint16_t>(saved, S.B), H, stream),
+                                  at<uint16_t>(saved, S.B), H, at<float>(ws, L.h_amax), stream),
             "gg_fc1_fwd_swiglu_fp8");
-    MOE_RUN(moe::launch_quant_rows(H, nullptr, 1, R, R, d.f, Hq, sh, num_sms(), stream, nvalid),
+    MOE_RUN(moe::launch_quant_rows(H, nullptr, 1, R, R, d.f, Hq, sh, num_sms(), stream, nvalid,
+                                   at<float>(ws, L.h_amax), moe::gemm_fc1_col_tiles(d.f)),
             "quant_h");
     MOE_RUN(moe::gemm_fc2_fwd_fp8(g, Hq, sh, at<uint8_t>(qw, Q.W2q), at<float>(qw, Q.s2), O,
                                   stream),

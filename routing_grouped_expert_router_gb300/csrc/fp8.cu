@@ -18,6 +18,7 @@
 //                    2j+1 = the same W3 columns), so one 256-row B tile holds
 //                    matching W1 and W3 columns;
 //   W2q  [E, h, f].
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -47,14 +48,18 @@ __device__ __forceinline__ uint32_t q2(float a, float b, float s) {
 
 // Row p of the output quantises row src(p) of `in` (idx[p] / div when idx is
 // given, else p).  A warp per row: one pass for the amax, one to quantise (the
-// row is then in L1 or L2).  Rows p >= *nvalid (when nvalid is given) are
-// skipped.
+// row is then in L1 or L2).  With amax_part, the row's amax is instead the
+// bf16 rounding of the largest of its nt fp32 partial maxima (the same value,
+// since rounding to nearest is monotone and symmetric) and the row is read
+// once.  Rows p >= *nvalid (when nvalid is given) are skipped.
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ in,
                                                          const int32_t* __restrict__ idx, int div,
                                                          long long rows, long long src_rows,
                                                          const int32_t* __restrict__ nvalid,
                                                          int n8, uint2* __restrict__ q,
-                                                         float* __restrict__ scale) {
+                                                         float* __restrict__ scale,
+                                                         const float* __restrict__ amax_part,
+                                                         int nt) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -67,15 +72,20 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     src = src < 0 ? 0 : (src >= src_rows ? src_rows - 1 : src);
     const uint4* r = in + src * n8;
     float amax = 0.f;
-    for (int c = lane; c < n8; c += 32) {
-      const uint4 w = __ldg(r + c);
-      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    if (amax_part) {
+      for (int i = lane; i < nt; i += 32) amax = fmaxf(amax, __ldg(amax_part + p * nt + i));
+    } else {
+      for (int c = lane; c < n8; c += 32) {
+        const uint4 w = __ldg(r + c);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+        for (int j = 0; j < 4; ++j)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+    if (amax_part) amax = __bfloat162float(__float2bfloat16_rn(amax));
     const float s = scale_of(amax);
     if (lane == 0) scale[p] = s;
     uint2* out = q + p * n8;
@@ -91,74 +101,113 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
 // Expert weights W [E, K, N] bf16 (N contiguous) -> per-(e, n) scales and
 // K-major codes: output row of column n of expert e is
 //   e * rows_per_e + (n / 128) * group_stride + slot * 128 + n % 128,
-// row length K bytes.  A block takes 64 columns of one expert: pass 1 reduces
-// their amax over K, pass 2 moves 64 x 64 tiles through shared memory,
-// quantising and transposing them.
-constexpr int kQcCols = 64;
-constexpr int kQcRows = 64;
+// row length K bytes.
+//
+// A persistent grid of one 512-thread block per SM walks slabs of 64 columns
+// of one expert.  Pass 1 reads the slab with 16-byte loads (8 threads per
+// 128-byte row segment, 64 rows at a time) and reduces each column's amax;
+// pass 2 reads the slab again -- from L2, since the slabs in flight at once
+// (one per SM, K x 128 bytes each) fit in it for K up to about 6k -- in
+// chunks of 256 rows staged in shared memory, and writes each column's codes
+// as 32-byte runs of its K-major output row.  The next chunk's loads are
+// issued before the current chunk is written.
+constexpr int kQcCols = 64;        // columns per slab
+constexpr int kQcThreads = 512;
+constexpr int kQcChunk = 256;      // K rows per pass-2 chunk (4 tiles of 64)
+constexpr int kQcPitch = kQcCols + 8;  // bf16 elements per staged row (144 bytes)
 
-__global__ void __launch_bounds__(256) quant_cols_kernel(const uint16_t* __restrict__ W, int K,
-                                                         int N, int rows_per_e, int group_stride,
-                                                         int slot, uint8_t* __restrict__ q,
-                                                         float* __restrict__ scale) {
-  __shared__ float part[4][kQcCols];
+__global__ void __launch_bounds__(kQcThreads, 1) quant_cols_kernel(
+    const uint16_t* __restrict__ W, int E, int K, int N, int rows_per_e, int group_stride,
+    int slot, uint8_t* __restrict__ q, float* __restrict__ scale) {
+  // pass 1 uses it as float [64][65], pass 2 as bf16 [256][kQcPitch]
+  __shared__ __align__(16) uint8_t smem[kQcChunk * kQcPitch * 2];
   __shared__ float s_col[kQcCols];
-  __shared__ uint16_t tile[kQcRows][kQcCols + 2];
-  const int e = blockIdx.y;
-  const int n0 = blockIdx.x * kQcCols;
+  float* red = reinterpret_cast<float*>(smem);
+  uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
   const int t = threadIdx.x;
-  const uint16_t* We = W + static_cast<size_t>(e) * K * N;
+  const int c8 = t & 7;      // 8-column group of the loads
+  const int rg = t >> 3;     // row within a 64-row step
+  const int warp = t >> 5;
+  const int lane = t & 31;
+  const int nslab = (N + kQcCols - 1) / kQcCols;
+  for (int slab = blockIdx.x; slab < E * nslab; slab += gridDim.x) {
+    const int e = slab / nslab;
+    const int n0 = (slab - e * nslab) * kQcCols;
+    const uint16_t* We = W + static_cast<size_t>(e) * K * N + n0 + 8 * c8;
+    const bool col_ok = n0 + 8 * c8 < N;  // N is a multiple of 64: whole groups
 
-  // pass 1: amax of each column (4 row groups per column, then combined)
-  {
-    const int c = t & (kQcCols - 1);
-    const int g = t >> 6;
-    float amax = 0.f;
-    if (n0 + c < N)
-      for (int k = g; k < K; k += 4)
-        amax = fmaxf(amax, fabsf(__uint_as_float(static_cast<uint32_t>(
-                               __ldg(We + static_cast<size_t>(k) * N + n0 + c)) << 16)));
-    part[g][c] = amax;
-  }
-  __syncthreads();
-  if (t < kQcCols) {
-    const float amax = fmaxf(fmaxf(part[0][t], part[1][t]), fmaxf(part[2][t], part[3][t]));
-    const float s = scale_of(amax);
-    s_col[t] = s;
-    if (n0 + t < N) scale[static_cast<size_t>(e) * N + n0 + t] = s;
-  }
-  __syncthreads();
-
-  // pass 2: 64 x 64 tiles, quantised and written K-major
-  for (int k0 = 0; k0 < K; k0 += kQcRows) {
-    for (int i = t; i < kQcRows * kQcCols; i += 256) {
-      const int r = i / kQcCols;
-      const int c = i % kQcCols;
-      tile[r][c] = (k0 + r < K && n0 + c < N) ? __ldg(We + static_cast<size_t>(k0 + r) * N + n0 + c)
-                                             : static_cast<uint16_t>(0);
+    // ---- pass 1: column amax
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = 0.f;
+    if (col_ok) {
+#pragma unroll 8
+      for (int k = rg; k < K; k += 64) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(We + static_cast<size_t>(k) * N));
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          m[2 * j] = fmaxf(m[2 * j], fabsf(bf16_lo(u[j])));
+          m[2 * j + 1] = fmaxf(m[2 * j + 1], fabsf(bf16_hi(u[j])));
+        }
+      }
+    }
+    __syncthreads();  // the previous slab's pass 2 is done with the buffer
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[rg * 65 + 8 * c8 + i] = m[i];
+    __syncthreads();
+    if (t < kQcCols) {
+      float a = 0.f;
+      for (int r = 0; r < 64; ++r) a = fmaxf(a, red[r * 65 + t]);
+      const float sc = scale_of(a);
+      s_col[t] = sc;
+      if (n0 + t < N) scale[static_cast<size_t>(e) * N + n0 + t] = sc;
     }
     __syncthreads();
-    // thread -> (column c, 16-row segment g): 16 codes, one 16-byte store
-    const int c = t >> 2;
-    const int g = t & 3;
-    const int n = n0 + c;
-    if (n < N && k0 + g * 16 < K) {
-      const float s = s_col[c];
-      uint32_t w[4];
+
+    // ---- pass 2: quantise and transpose, 256 rows at a time
+    // write-phase roles: lane -> column, warp -> 32-row segment of the chunk
+    const int wc = lane + 32 * (warp & 1);
+    const int seg = warp >> 1;  // 0..7
+    const int n = n0 + wc;
+    const float sc = s_col[wc];
+    const size_t orow = static_cast<size_t>(e) * rows_per_e + (n / 128) * group_stride +
+                        slot * 128 + n % 128;
+    uint4 v[4];
+    auto load_chunk = [&](int k0) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int r = g * 16 + 4 * j;
-        const float v0 = __uint_as_float(static_cast<uint32_t>(tile[r + 0][c]) << 16);
-        const float v1 = __uint_as_float(static_cast<uint32_t>(tile[r + 1][c]) << 16);
-        const float v2 = __uint_as_float(static_cast<uint32_t>(tile[r + 2][c]) << 16);
-        const float v3 = __uint_as_float(static_cast<uint32_t>(tile[r + 3][c]) << 16);
-        w[j] = q2(v0, v1, s) | (q2(v2, v3, s) << 16);
+        const int k = k0 + 64 * j + rg;
+        v[j] = (col_ok && k < K)
+                   ? __ldg(reinterpret_cast<const uint4*>(We + static_cast<size_t>(k) * N))
+                   : make_uint4(0, 0, 0, 0);
       }
-      const size_t orow = static_cast<size_t>(e) * rows_per_e + (n / 128) * group_stride +
-                          slot * 128 + n % 128;
-      *reinterpret_cast<uint4*>(q + orow * K + k0 + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    };
+    load_chunk(0);
+    for (int k0 = 0; k0 < K; k0 += kQcChunk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(tile + (64 * j + rg) * kQcPitch + 8 * c8) = v[j];
+      __syncthreads();
+      if (k0 + kQcChunk < K) load_chunk(k0 + kQcChunk);  // in flight during the writes
+      const int kk = k0 + 32 * seg;
+      if (n < N && kk < K) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint16_t* col = tile + (32 * seg + 4 * i) * kQcPitch + wc;
+          const float x0 = __uint_as_float(static_cast<uint32_t>(col[0]) << 16);
+          const float x1 = __uint_as_float(static_cast<uint32_t>(col[kQcPitch]) << 16);
+          const float x2 = __uint_as_float(static_cast<uint32_t>(col[2 * kQcPitch]) << 16);
+          const float x3 = __uint_as_float(static_cast<uint32_t>(col[3 * kQcPitch]) << 16);
+          w[i] = q2(x0, x1, sc) | (q2(x2, x3, sc) << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(q + orow * K + kk);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
 }
 
@@ -173,20 +222,23 @@ int grid_rows(long long rows, int num_sms) {
 
 cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                               long long src_rows, int n, uint8_t* q, float* scale, int num_sms,
-                              cudaStream_t s, const int32_t* nvalid) {
+                              cudaStream_t s, const int32_t* nvalid, const float* amax_part,
+                              int nt) {
   if (rows == 0 || src_rows == 0) return cudaSuccess;
   quant_rows_kernel<<<grid_rows(rows, num_sms), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(in), idx, div, rows, src_rows, nvalid, n / 8,
-      reinterpret_cast<uint2*>(q), scale);
+      reinterpret_cast<uint2*>(q), scale, amax_part, nt);
   return launched();
 }
 
 cudaError_t launch_quant_cols(const uint16_t* W, int E, int K, int N, int rows_per_e,
-                              int group_stride, int slot, uint8_t* q, float* scale,
+                              int group_stride, int slot, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s) {
   if (E == 0 || K == 0 || N == 0) return cudaSuccess;
-  const dim3 grid((N + kQcCols - 1) / kQcCols, E);
-  quant_cols_kernel<<<grid, 256, 0, s>>>(W, K, N, rows_per_e, group_stride, slot, q, scale);
+  const int slabs = E * ((N + kQcCols - 1) / kQcCols);
+  const int grid = slabs < num_sms ? slabs : num_sms;
+  quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(W, E, K, N, rows_per_e, group_stride, slot, q,
+                                                scale);
   return launched();
 }
 

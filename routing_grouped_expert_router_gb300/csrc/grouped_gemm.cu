@@ -99,7 +99,8 @@ struct Params {
   const void* in0;
   const void* in1;
   const float* in2;  // EPI_SWIGLU_BWD_SAR: gate of each permuted row
-  float* part;       // EPI_SWIGLU_BWD_SAR: per-(row, n-tile) partial sums of <H, dY W2^T>
+  float* part;       // EPI_SWIGLU_BWD_SAR: per-(row, n-tile) partial sums of <H, dY W2^T>;
+                     // EPI_SWIGLU_F8: per-(row, n-tile) amax of H
   int part_ld;       // n-tiles per row of `part`
   const float* row_scale;   // FP8: scale of each A row (permuted row)
   const float* col_scale0;  // FP8: [E, N] scales of the B columns (first operand)
@@ -217,6 +218,10 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, 
     float hv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) hv[i] = silu_f(v0[i]) * v1[i];
+    if (EPI_ == EPI_SWIGLU_F8) {  // amax of H for its per-row e4m3 scale
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc = fmaxf(acc, fabsf(hv[i]));
+    }
     store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
     store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, v1);
     store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, hv);
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (is_f8(EPI)) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
         epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1, acc);
       }
-      if (EPI == EPI_SWIGLU_BWD_SAR && row_ok)
+      if ((EPI == EPI_SWIGLU_BWD_SAR || EPI == EPI_SWIGLU_F8) && row_ok)
         p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
       tc_fence_before();
       mbar_arrive(smem_u32(&c.tempty[buf]));
@@ -1076,12 +1081,13 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
 }
 
 int gemm_col_tiles(int n) { return (n + BN - 1) / BN; }
+int gemm_fc1_col_tiles(int f) { return (f + BN / 2 - 1) / (BN / 2); }
 
 // FP8 forward.  Operands are e4m3 codes, K-major, one byte each: a K block is
 // 128 codes (one 128-byte swizzled row), and the MMA is kind::f8f6f4.
 cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& g, const void* Xq, const float* sx,
                              const void* W13q, const float* s1, const float* s3, void* A, void* B,
-                             void* H, cudaStream_t s) {
+                             void* H, float* h_amax, cudaStream_t s) {
   Maps m;
   memset(&m, 0, sizeof(m));
   // A: Xq [rows, h];  B: W13q viewed as [E * 2f rows (N), h (K)], 256-row tiles
@@ -1097,6 +1103,8 @@ cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& g, const void* Xq, const float* 
   p.row_scale = sx;
   p.col_scale0 = s1;
   p.col_scale1 = s3;
+  p.part = h_amax;
+  p.part_ld = g.f / (BN / 2);
   p.out0 = A;
   p.out1 = B;
   p.out2 = H;

@@ -43,9 +43,12 @@ cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& p, const void* dy_perm, const 
 //   A = sx * s1 * (Xq W1q), B = sx * s3 * (Xq W3q), H = silu(A) * B   (bf16 out)
 //   Xq [rows, h]; W13q [E, 2f, h] with 128-row groups alternating W1 and W3
 //   columns; s1, s3 [E, f]; sx [rows].
+//   h_amax [rows, gemm_fc1_col_tiles(f)]: amax of |H| (fp32, before the bf16
+//   store) over each 128-column tile of a row.
 cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& p, const void* Xq, const float* sx,
                              const void* W13q, const float* s1, const float* s3, void* A, void* B,
-                             void* H, cudaStream_t s);
+                             void* H, float* h_amax, cudaStream_t s);
+int gemm_fc1_col_tiles(int f);
 //   O = sh * s2 * (Hq W2q): Hq [rows, f]; W2q [E, h, f]; s2 [E, h]; sh [rows].
 cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& p, const void* Hq, const float* sh,
                              const void* W2q, const float* s2, void* O, cudaStream_t s);

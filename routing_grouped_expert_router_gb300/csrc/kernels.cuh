@@ -60,14 +60,17 @@ cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, 
 // scale[p] = amax(|in[src]|) / 448 (1 for a zero row), src = idx[p] / div (p
 // when idx is NULL), for p < rows (and p < *nvalid when given); n elements per
 // row, q row stride n bytes.
+// With amax_part [rows, nt] (fp32 partial maxima of |row|), the amax is taken
+// from it, rounded to bf16, and the row is read once.
 cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                               long long src_rows, int n, uint8_t* q, float* scale, int num_sms,
-                              cudaStream_t s, const int32_t* nvalid = nullptr);
+                              cudaStream_t s, const int32_t* nvalid = nullptr,
+                              const float* amax_part = nullptr, int nt = 0);
 // Columns of expert weights W [E, K, N]: scale[e, n] = amax_k |W[e, k, n]| / 448;
 // codes written K-major to row e * rows_per_e + (n / 128) * group_stride +
 // slot * 128 + n % 128 of q (K bytes per row).
 cudaError_t launch_quant_cols(const uint16_t* W, int E, int K, int N, int rows_per_e,
-                              int group_stride, int slot, uint8_t* q, float* scale,
+                              int group_stride, int slot, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s);
 // dg[perm_src[p]] = sum_{i < nt} part[p * nt + i] for p < *nvalid (fixed order).
 cudaError_t launch_dg_reduce(const float* part, int nt, const int32_t* perm_src, long long rows,
