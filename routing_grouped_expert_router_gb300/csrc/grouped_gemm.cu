@@ -280,6 +280,73 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, 
   }
 }
 
+// Eight bf16 pairs (two 16-byte pieces x 4) -> 32 floats.
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&q)[4], float* v) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+// The SwiGLU-backward epilogues on a 32-column chunk whose A and B values
+// were loaded ahead (raw bf16).  EPI_SWIGLU_BWD: v0 = dH.  EPI_SWIGLU_BWD_SAR:
+// v0 = dy W2^T without the gate (see epilogue_chunk).
+template <int EPI>
+__device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, int grow, int col,
+                                                 const float* v0, const uint4 (&ra)[4],
+                                                 const uint4 (&rb)[4], float& acc) {
+  const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+  float av[32], bv[32];
+  unpack_bf16x32(ra, av);
+  unpack_bf16x32(rb, bv);
+  float da[32], db[32];
+  if (EPI == EPI_SWIGLU_BWD) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = av[i];
+      const float sg = 1.0f / (1.0f + expf(-a));
+      const float dh = v0[i];
+      da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
+      db[i] = dh * a * sg;
+    }
+  } else {
+    const float g = __ldg(p.in2 + grow);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = av[i];
+      const float sg = 1.0f / (1.0f + expf(-a));
+      const float sl = a * sg;
+      const float hh = sl * bv[i];
+      const float dh = g * v0[i];
+      acc = fmaf(hh, v0[i], acc);
+      da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
+      db[i] = dh * sl;
+      av[i] = g * hh;  // gH
+    }
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, av);
+  }
+  store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
+  store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
+}
+
+// The next chunk's A and B pieces (nothing for rows or columns out of range).
+__device__ __forceinline__ void load_ab_chunk(const Params& p, bool ok, size_t o, uint4 (&ra)[4],
+                                              uint4 (&rb)[4]) {
+  if (!ok) return;
+  const uint4* a = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.in0) + o);
+  const uint4* b = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.in1) + o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ra[i] = __ldg(a + i);
+    rb[i] = __ldg(b + i);
+  }
+}
+
 // FP8: the sums of e4m3 products times the row's and the columns' scales.
 template <int NUM_B>
 __device__ __forceinline__ void rescale_f8(const Params& p, const Tile& tl, int grow, int col,
@@ -539,16 +606,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int grow = tl.row0 + r;                        // M-grouped row
       const bool row_ok = GROUP_K ? (tl.mb * BM + r < p.M) : (grow < tl.row_end);
       float acc = 0.f;
+      if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
+        // A and B of chunk ch + 1 are in flight while chunk ch is computed
+        const size_t o0 = static_cast<size_t>(grow) * p.ldo + tl.nb * BNB;
+        uint4 ra[4], rb[4];
+        load_ab_chunk(p, row_ok && tl.nb * BNB < p.N, o0, ra, rb);
 #pragma unroll 1
-      for (int ch = 0; ch < BNB / 32; ++ch) {
-        float v0[32];
-        float v1[32];
-        tmem_ld32(tbase + ch * 32, v0);
-        if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
-        const int col = tl.nb * BNB + ch * 32;
-        if (!row_ok || col >= p.N) continue;
-        if (is_f8(EPI)) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
-        epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1, acc);
+        for (int ch = 0; ch < BNB / 32; ++ch) {
+          uint4 ca[4], cb[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            ca[i] = ra[i];
+            cb[i] = rb[i];
+          }
+          const int col = tl.nb * BNB + ch * 32;
+          if (ch + 1 < BNB / 32)
+            load_ab_chunk(p, row_ok && col + 32 < p.N, o0 + (ch + 1) * 32, ra, rb);
+          float v0[32];
+          tmem_ld32(tbase + ch * 32, v0);
+          if (!row_ok || col >= p.N) continue;
+          swiglu_bwd_chunk<EPI>(p, grow, col, v0, ca, cb, acc);
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < BNB / 32; ++ch) {
+          float v0[32];
+          float v1[32];
+          tmem_ld32(tbase + ch * 32, v0);
+          if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
+          const int col = tl.nb * BNB + ch * 32;
+          if (!row_ok || col >= p.N) continue;
+          if (is_f8(EPI)) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
+          epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1, acc);
+        }
       }
       if ((EPI == EPI_SWIGLU_BWD_SAR || EPI == EPI_SWIGLU_F8) && row_ok)
         p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
@@ -851,15 +941,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int grow = tl.row0 + half + r;           // M-grouped row
       const bool row_ok = GROUP_K ? (orow < p.M) : (grow < tl.row_end);
       float acc = 0.f;
+      if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
+        // A and B of chunk ch + 1 are in flight while chunk ch is computed
+        const size_t o0 = static_cast<size_t>(grow) * p.ldo + tl.nb * BNB;
+        uint4 ra[4], rb[4];
+        load_ab_chunk(p, row_ok && tl.nb * BNB < p.N, o0, ra, rb);
 #pragma unroll 1
-      for (int ch = 0; ch < BNB / 32; ++ch) {
-        float v0[32];
-        float v1[32];
-        tmem_ld32(tbase + ch * 32, v0);
-        if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
-        const int col = tl.nb * BNB + ch * 32;
-        if (!row_ok || col >= p.N) continue;
-        epilogue_chunk<NUM_B, EPI>(p, tl, grow, orow, col, v0, v1, acc);
+        for (int ch = 0; ch < BNB / 32; ++ch) {
+          uint4 ca[4], cb[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            ca[i] = ra[i];
+            cb[i] = rb[i];
+          }
+          const int col = tl.nb * BNB + ch * 32;
+          if (ch + 1 < BNB / 32)
+            load_ab_chunk(p, row_ok && col + 32 < p.N, o0 + (ch + 1) * 32, ra, rb);
+          float v0[32];
+          tmem_ld32(tbase + ch * 32, v0);
+          if (!row_ok || col >= p.N) continue;
+          swiglu_bwd_chunk<EPI>(p, grow, col, v0, ca, cb, acc);
+        }
+      } else {
+#pragma unroll 1
+        for (int ch = 0; ch < BNB / 32; ++ch) {
+          float v0[32];
+          float v1[32];
+          tmem_ld32(tbase + ch * 32, v0);
+          if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
+          const int col = tl.nb * BNB + ch * 32;
+          if (!row_ok || col >= p.N) continue;
+          epilogue_chunk<NUM_B, EPI>(p, tl, grow, orow, col, v0, v1, acc);
+        }
       }
       if (EPI == EPI_SWIGLU_BWD_SAR && row_ok)
         p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
