@@ -111,16 +111,21 @@ __device__ __forceinline__ void select_topk(const float (&l)[EP], int E, int k, 
 // ---- E <= 8: lanes split the columns (8-element slices); each lane keeps
 // all 8 partial logits of TOK tokens and reads its rows of the weights as
 // conflict-free 16-byte loads from a padded layout (lane l's eight rows are
-// one block + 16 bytes).  x streams through a ring of NSTAGE shared-memory
-// stages filled with cp.async (256 columns of the block's 64 tokens each), so
+// one block + 16 bytes).  Within a slice the weights are stored by column
+// pair, expert, column: a bf16x2 word of x (two adjacent columns) and the two
+// weights of one expert for those columns form the operands of one packed
+// fp32x2 FMA, which keeps separate sums for even and odd columns (added at
+// the end).  x streams through a ring of NSTAGE shared-memory stages filled
+// with cp.async (256 columns of the block's tokens each; every warp copies
+// and reads only its own tokens' rows, so a stage needs no block barrier), so
 // several steps of loads are in flight without holding registers.  A
 // butterfly gives every lane the full logits.
-constexpr int kRouterAThreads = 512;
+constexpr int kRouterAThreads = 384;
 constexpr int kRouterATok = 4;                      // tokens per warp
 constexpr int kRouterATile = kRouterAThreads / 32 * kRouterATok;  // tokens per block tile
 constexpr int kRouterACh = 2048;                    // columns per weight chunk
 constexpr int kRouterASlice = 8 * 8 + 4;
-constexpr int kRouterAStage = kRouterATile * 256;   // bf16 per x stage (32 KiB)
+constexpr int kRouterAStage = kRouterATile * 256;   // bf16 per x stage (24 KiB)
 constexpr int kRouterANStage = 3;
 constexpr int kRouterASmem =
     (kRouterACh / 8) * kRouterASlice * 4 + kRouterANStage * kRouterAStage * 2;
@@ -154,12 +159,6 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
   const int c0 = c * CH;
   const int rows = min(CH, h - c0);
   const int nsteps = (rows + 255) / 256;  // 256-column steps of a tile
-  for (int q = threadIdx.x; q < rows * EP; q += kRouterAThreads) {
-    const int lr = q / EP;
-    const int e = q - lr * EP;
-    sw[(lr >> 3) * SLICE + (lr & 7) * EP + e] =
-        (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
-  }
   // this block's tiles, flattened with their steps into one stream of stages
   const int ntiles = (T + TILE - 1) / TILE;
   const int my_tiles = sub < ntiles ? (ntiles - sub + bpc - 1) / bpc : 0;
@@ -169,34 +168,40 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
       const int t0 = (sub + (g / nsteps) * bpc) * TILE;
       const int cs = (g % nsteps) * 256;
       const uint32_t base = smem_addr(xs + (g % NST) * kRouterAStage);
+      // each warp copies (and later reads) only its own TOK tokens' rows
 #pragma unroll
-      for (int i = 0; i < TILE * 32 / kRouterAThreads; ++i) {
-        const int id = i * kRouterAThreads + threadIdx.x;
-        const int tok = id >> 5;
-        const int c16 = id & 31;
+      for (int i = 0; i < TOK; ++i) {
+        const int tok = warp * TOK + i;
         const int t = t0 + tok;
-        const bool ok = t < T && cs + 8 * c16 < rows;
-        const uint16_t* src = ok ? x + static_cast<size_t>(t) * h + c0 + cs + 8 * c16 : x;
-        cp_async16(base + (tok * 256 + 8 * c16) * 2, src, ok);
+        const bool ok = t < T && cs + 8 * lane < rows;
+        const uint16_t* src = ok ? x + static_cast<size_t>(t) * h + c0 + cs + 8 * lane : x;
+        cp_async16(base + (tok * 256 + 8 * lane) * 2, src, ok);
       }
     }
     cp_async_commit();  // an empty group keeps the group count uniform
   };
 #pragma unroll
   for (int g = 0; g < NST - 1; ++g) issue(g);
+  // the weights are staged while the first x stages are in flight
+  for (int q = threadIdx.x; q < rows * EP; q += kRouterAThreads) {
+    const int lr = q / EP;
+    const int e = q - lr * EP;
+    sw[(lr >> 3) * SLICE + ((lr & 7) >> 1) * (2 * EP) + 2 * e + (lr & 1)] =
+        (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
+  }
   __syncthreads();  // weights staged
 
-  float acc[TOK][EP];
+  float2 acc2[TOK][EP];  // (even-column, odd-column) partial sums
   for (int g = 0; g < total; ++g) {
     issue(g + NST - 1);
     cp_async_wait<NST - 1>();
-    __syncthreads();  // stage g landed for every thread's copies
+    __syncwarp();  // stage g landed for every lane's copies (the warp's own rows)
     const int step = g % nsteps;
     if (step == 0) {
 #pragma unroll
       for (int u = 0; u < TOK; ++u)
 #pragma unroll
-        for (int e = 0; e < EP; ++e) acc[u][e] = 0.f;
+        for (int e = 0; e < EP; ++e) acc2[u][e] = make_float2(0.f, 0.f);
     }
     const int lc = step * 256 + 8 * lane;
     if (lc < rows) {
@@ -206,35 +211,38 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
       for (int u = 0; u < TOK; ++u) xq[u] = *reinterpret_cast<const uint4*>(xt + u * 256);
       const float4* wb = reinterpret_cast<const float4*>(sw + (lc >> 3) * SLICE);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float xv[TOK];
+      for (int j2 = 0; j2 < 4; ++j2) {  // column pairs of the lane's slice
+        float2 xp[TOK];                 // (column 2 j2, column 2 j2 + 1) of each token
 #pragma unroll
         for (int u = 0; u < TOK; ++u) {
-          const uint32_t w = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
-          xv[u] = (j & 1) ? bf16_hi(w) : bf16_lo(w);
+          const uint32_t w = j2 == 0 ? xq[u].x : j2 == 1 ? xq[u].y : j2 == 2 ? xq[u].z : xq[u].w;
+          xp[u] = make_float2(bf16_lo(w), bf16_hi(w));
         }
 #pragma unroll
-        for (int e4 = 0; e4 < EP / 4; ++e4) {
-          const float4 wv = wb[(j * EP) / 4 + e4];
+        for (int e2 = 0; e2 < EP / 2; ++e2) {  // the same columns' weights of experts 2 e2, 2 e2 + 1
+          const float4 w4 = wb[j2 * (EP / 2) + e2];
+          const float2 wa = make_float2(w4.x, w4.y);
+          const float2 wc = make_float2(w4.z, w4.w);
 #pragma unroll
           for (int u = 0; u < TOK; ++u) {
-            acc[u][4 * e4 + 0] = fmaf(xv[u], wv.x, acc[u][4 * e4 + 0]);
-            acc[u][4 * e4 + 1] = fmaf(xv[u], wv.y, acc[u][4 * e4 + 1]);
-            acc[u][4 * e4 + 2] = fmaf(xv[u], wv.z, acc[u][4 * e4 + 2]);
-            acc[u][4 * e4 + 3] = fmaf(xv[u], wv.w, acc[u][4 * e4 + 3]);
+            acc2[u][2 * e2] = __ffma2_rn(xp[u], wa, acc2[u][2 * e2]);
+            acc2[u][2 * e2 + 1] = __ffma2_rn(xp[u], wc, acc2[u][2 * e2 + 1]);
           }
         }
       }
     }
-    __syncthreads();  // stage g's slot may be refilled from the next iteration on
+    __syncwarp();  // every lane is done with slot g before it is refilled
     if (step == nsteps - 1) {
+      float acc[TOK][EP];
 #pragma unroll
       for (int u = 0; u < TOK; ++u)
 #pragma unroll
-        for (int e = 0; e < EP; ++e)
+        for (int e = 0; e < EP; ++e) {
+          acc[u][e] = acc2[u][e].x + acc2[u][e].y;
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1)
             acc[u][e] += __shfl_xor_sync(kFull, acc[u][e], off);
+        }
       const int tw = (sub + (g / nsteps) * bpc) * TILE + warp * TOK;
 #pragma unroll
       for (int u = 0; u < TOK; ++u) {
