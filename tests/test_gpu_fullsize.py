@@ -38,14 +38,28 @@ def _f64(t):
 
 @pytest.mark.parametrize("name", ["mixtral8x7b", "deepseekmoe", "internal352b", "hunyuan"])
 def test_fullsize_sampled(lib, name):
+    _check_fullsize(CONFIGS[name])
+
+
+@pytest.mark.parametrize("name,factor,sar", [("mixtral8x7b", 0.0, True),
+                                             ("internal352b", 1.0, False),
+                                             ("deepseekmoe", 1.0, True)])
+def test_fullsize_variants(lib, name, factor, sar):
+    """The same sampled checks with a per-expert capacity (token dropping) and
+    with the selective-rematerialisation context."""
     cfg = CONFIGS[name]
+    cap = mb.capacity_for(cfg.T, cfg.k, cfg.E, factor) if factor else 0
+    _check_fullsize(cfg, capacity=cap, sar=sar)
+
+
+def _check_fullsize(cfg, capacity=0, sar=False):
     T, h, f, E, k = cfg.T, cfg.h, cfg.f, cfg.E, cfg.k
     inp = synth.make_layer(cfg, "cuda")
     x_cpu, n_fix = oracle.condition_router_margins(
         inp["x"].cpu(), inp["Wg"].cpu(), inp["b"].cpu(), k,
         lambda r, a: synth.replacement_x_rows(cfg, r, a))
     inp["x"] = x_cpu.cuda()
-    d = mb.dims_of(cfg)
+    d = mb.dims_of(cfg, capacity=capacity, sar=sar)
     run = LayerRun(d)
     run.fwd(inp)
     run.bwd(inp)
@@ -55,20 +69,26 @@ def test_fullsize_sampled(lib, name):
     # ---- routing and dispatch: every token, bit-exact
     Wg_cpu, b_cpu = inp["Wg"].cpu(), inp["b"].cpu()
     idx, gates, _ = oracle.route(x_cpu, Wg_cpu, b_cpu, k)
-    counts, offsets, psrc, pdst = oracle.dispatch(idx, E)
+    counts, offsets, psrc, pdst = oracle.dispatch(idx, E, capacity or None)
+    nkept = int(offsets[-1])
+    if capacity:
+        assert nkept < T * k, "the capacity must drop assignments"
     np.testing.assert_array_equal(run.saved_view("topk_idx").cpu().numpy(), idx)
     assert np.max(np.abs(_f64(run.saved_view("gates")) - gates)) <= 1e-5
     np.testing.assert_array_equal(run.saved_view("counts").cpu().numpy(), counts)
     np.testing.assert_array_equal(run.saved_view("offsets").cpu().numpy(), offsets)
-    np.testing.assert_array_equal(run.saved_view("perm_src").cpu().numpy(), psrc)
+    np.testing.assert_array_equal(run.saved_view("perm_src").cpu().numpy()[:nkept], psrc)
     np.testing.assert_array_equal(run.saved_view("perm_dst").cpu().numpy(), pdst)
-    if cfg.zipf_s > 0:
+    if cfg.zipf_s > 0 and not capacity:
         assert counts[-1] == 0 and counts[0] > 0.25 * T * k
 
     # ---- sampled tokens: y and dx rows
     rng = np.random.default_rng(cfg.seed)
     ntok = 4 if k >= 3 else 6
     toks = sorted(set([0, T - 1] + rng.choice(T, ntok - 2, replace=False).tolist()))
+    if capacity:  # include tokens with dropped slots
+        dropped = np.nonzero(np.any(pdst.reshape(T, k) < 0, axis=1))[0]
+        toks = sorted(set(toks) | set(dropped[:: max(1, len(dropped) // 3)][:3].tolist()))
     dy_cpu = inp["dy"].cpu()
     needed = {}
     for t in toks:
@@ -82,8 +102,11 @@ def test_fullsize_sampled(lib, name):
                                                 gates[t, j], W1e, W3e, W2e)
         del W1e, W3e, W2e
     y_ref, dx_ref = [], []
+    zero = {"o": np.zeros((1, h)), "dg": np.zeros(1), "dx": np.zeros((1, h))}
     for t in toks:
-        r = oracle.assemble_token(gates[t], idx[t], [terms[(t, j)] for j in range(k)], Wg_cpu)
+        # a dropped slot adds nothing to y and has dg = 0
+        tt = [terms[(t, j)] if pdst[t * k + j] >= 0 else zero for j in range(k)]
+        r = oracle.assemble_token(gates[t], idx[t], tt, Wg_cpu)
         y_ref.append(r["y"])
         dx_ref.append(r["dx"])
     y_gpu = _f64(run.y[toks])
