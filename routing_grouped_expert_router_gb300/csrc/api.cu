@@ -739,12 +739,11 @@ moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x, const floa
   if ((st = do_dispatch(d, selection(d, 0, d.E), idx, at<int32_t>(saved, S.counts), offsets, psrc,
                         pdst, ws, L, stream)) != MOE_OK)
     return st;
-  // the backward's FC1 weight gradient takes the bf16 rows
-  MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, R, d.T, d.h, at<uint16_t>(saved, S.x_perm),
-                                  num_sms(), stream, nvalid),
-          "permute_rows");
-  MOE_RUN(moe::launch_quant_rows(x, psrc, d.k, R, d.T, d.h, Xq, sx, num_sms(), stream, nvalid),
-          "quant_x_perm");
+  // e4m3 rows for FC1 and, in the same pass, the bf16 rows the backward's FC1
+  // weight gradient takes
+  MOE_RUN(moe::launch_quant_rows(x, psrc, d.k, R, d.T, d.h, Xq, sx, num_sms(), stream, nvalid,
+                                 nullptr, 0, at<uint16_t>(saved, S.x_perm)),
+          "permute_quant_x");
   if (R > 0) {
     const GemmProblem g = problem(d, offsets, ws);
     MOE_RUN(moe::gemm_fc1_fwd_fp8(g, Xq, sx, at<uint8_t>(qw, Q.W13q), at<float>(qw, Q.s1),

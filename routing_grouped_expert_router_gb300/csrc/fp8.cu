@@ -51,7 +51,9 @@ __device__ __forceinline__ uint32_t q2(float a, float b, float s) {
 // row is then in L1 or L2).  With amax_part, the row's amax is instead the
 // bf16 rounding of the largest of its nt fp32 partial maxima (the same value,
 // since rounding to nearest is monotone and symmetric) and the row is read
-// once.  Rows p >= *nvalid (when nvalid is given) are skipped.
+// once.  With copy, the quantising pass also writes the bf16 row to copy[p]
+// (the permute of the same rows, fused).  Rows p >= *nvalid (when nvalid is
+// given) are skipped.
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ in,
                                                          const int32_t* __restrict__ idx, int div,
                                                          long long rows, long long src_rows,
@@ -59,7 +61,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
                                                          int n8, uint2* __restrict__ q,
                                                          float* __restrict__ scale,
                                                          const float* __restrict__ amax_part,
-                                                         int nt) {
+                                                         int nt, uint4* __restrict__ copy) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -89,8 +91,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     const float s = scale_of(amax);
     if (lane == 0) scale[p] = s;
     uint2* out = q + p * n8;
+    uint4* cp = copy ? copy + p * n8 : nullptr;
     for (int c = lane; c < n8; c += 32) {
       const uint4 w = __ldg(r + c);
+      if (cp) cp[c] = w;
       const uint32_t lo = q2(bf16_lo(w.x), bf16_hi(w.x), s) | (q2(bf16_lo(w.y), bf16_hi(w.y), s) << 16);
       const uint32_t hi = q2(bf16_lo(w.z), bf16_hi(w.z), s) | (q2(bf16_lo(w.w), bf16_hi(w.w), s) << 16);
       out[c] = make_uint2(lo, hi);
@@ -103,11 +107,11 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
 //   e * rows_per_e + (n / 128) * group_stride + slot * 128 + n % 128,
 // row length K bytes.
 //
-// A persistent grid of one 512-thread block per SM walks slabs of 64 columns
+// A persistent grid of two 512-thread blocks per SM walks slabs of 64 columns
 // of one expert.  Pass 1 reads the slab with 16-byte loads (8 threads per
 // 128-byte row segment, 64 rows at a time) and reduces each column's amax;
-// pass 2 reads the slab again -- from L2, since the slabs in flight at once
-// (one per SM, K x 128 bytes each) fit in it for K up to about 6k -- in
+// pass 2 reads the slab again -- mostly from L2, which holds most of the
+// slabs in flight at once (two per SM, K x 128 bytes each) -- in
 // chunks of 256 rows staged in shared memory, and writes each column's codes
 // as 32-byte runs of its K-major output row.  The next chunk's loads are
 // issued before the current chunk is written.
@@ -116,7 +120,7 @@ constexpr int kQcThreads = 512;
 constexpr int kQcChunk = 256;      // K rows per pass-2 chunk (4 tiles of 64)
 constexpr int kQcPitch = kQcCols + 8;  // bf16 elements per staged row (144 bytes)
 
-__global__ void __launch_bounds__(kQcThreads, 1) quant_cols_kernel(
+__global__ void __launch_bounds__(kQcThreads, 2) quant_cols_kernel(
     const uint16_t* __restrict__ W, int E, int K, int N, int rows_per_e, int group_stride,
     int slot, uint8_t* __restrict__ q, float* __restrict__ scale) {
   // pass 1 uses it as float [64][65], pass 2 as bf16 [256][kQcPitch]
@@ -223,11 +227,11 @@ int grid_rows(long long rows, int num_sms) {
 cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                               long long src_rows, int n, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s, const int32_t* nvalid, const float* amax_part,
-                              int nt) {
+                              int nt, uint16_t* copy) {
   if (rows == 0 || src_rows == 0) return cudaSuccess;
   quant_rows_kernel<<<grid_rows(rows, num_sms), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(in), idx, div, rows, src_rows, nvalid, n / 8,
-      reinterpret_cast<uint2*>(q), scale, amax_part, nt);
+      reinterpret_cast<uint2*>(q), scale, amax_part, nt, reinterpret_cast<uint4*>(copy));
   return launched();
 }
 
@@ -236,7 +240,7 @@ cudaError_t launch_quant_cols(const uint16_t* W, int E, int K, int N, int rows_p
                               cudaStream_t s) {
   if (E == 0 || K == 0 || N == 0) return cudaSuccess;
   const int slabs = E * ((N + kQcCols - 1) / kQcCols);
-  const int grid = slabs < num_sms ? slabs : num_sms;
+  const int grid = slabs < 2 * num_sms ? slabs : 2 * num_sms;  // two blocks per SM
   quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(W, E, K, N, rows_per_e, group_stride, slot, q,
                                                 scale);
   return launched();

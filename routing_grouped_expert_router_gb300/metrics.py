@@ -42,6 +42,7 @@ def kernel_work(T: int, h: int, f: int, E: int, k: int) -> dict:
         "permute_dy": T * h * 2 + R * h * 2 + R * 12,
         "dg_reduce": R * ((f + 255) // 256) * 4 + R * 8,
         "quant_x_perm": T * h * 2 + R * h + R * 8,
+        "permute_quant_x": T * h * 2 + R * h * 2 + R * h + R * 8,
         "quant_h": R * f * 2 + R * f + R * 4,
         "quant_w1": E * h * f * (2 + 1) + E * f * 4,
         "quant_w3": E * h * f * (2 + 1) + E * f * 4,
