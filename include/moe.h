@@ -331,6 +331,13 @@ moe_status moe_read_device_status(void* ws, moe_stream_t stream);
 /* Zeroes the status word at the start of `ws` (asynchronous). */
 moe_status moe_clear_device_status(void* ws, moe_stream_t stream);
 
+/* Failure-path self test: launches one thread that waits on an mbarrier
+ * nothing will complete, with the same bounded wait the matmul pipelines use
+ * but a limit of limit_us microseconds (1 .. 1000000).  The wait gives up,
+ * records MOE_ERR_DEVICE_TIMEOUT in the status word at the start of `ws` and
+ * the kernel returns; the context stays usable.  No fault, trap or hang. */
+moe_status moe_selftest_wait_timeout(void* ws, uint32_t limit_us, moe_stream_t stream);
+
 /* Measurement hook: while `events` is non-NULL, every kernel the library
  * launches from this host thread is followed by cudaEventRecord of the next
  * event on the launching stream (up to `capacity`).  Pass NULL to stop; the

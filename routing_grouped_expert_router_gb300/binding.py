@@ -84,6 +84,7 @@ _SIGS = {
     "moe_profile_events": (_I, [_P, _I]),
     "moe_profile_kernel_name": (ctypes.c_char_p, [_I]),
     "moe_kernel_launches": (ctypes.c_int64, []),
+    "moe_selftest_wait_timeout": (_I, [_P, ctypes.c_uint32, _P]),
     "moe_fp8_weight_bytes": (_SZ, [_D]),
     "moe_quantize_weights_fp8": (_I, [_D, _P, _P, _P, _P, _P]),
     "moe_fp8_weight_view": (_P, [_D, _P, ctypes.c_char_p]),
@@ -260,6 +261,11 @@ def moe_profile_events(events_array_addr: int | None, capacity: int) -> int:
 
 def moe_profile_kernel_name(i: int) -> str:
     return load().moe_profile_kernel_name(int(i)).decode()
+
+
+def moe_selftest_wait_timeout(ws, limit_us: int, stream=None):
+    _check(load().moe_selftest_wait_timeout(_addr(ws), int(limit_us), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_kernel_launches() -> int:

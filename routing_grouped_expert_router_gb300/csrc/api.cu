@@ -437,6 +437,14 @@ moe_status moe_read_device_status(void* ws, moe_stream_t stream) {
   return static_cast<moe_status>(v);
 }
 
+moe_status moe_selftest_wait_timeout(void* ws, uint32_t limit_us, moe_stream_t stream_) {
+  if (!ws || !aligned(ws, kAlign) || limit_us == 0 || limit_us > 1000000u) return MOE_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  MOE_RUN(moe::launch_wait_timeout_probe(at<int>(ws, 0), 1000ull * limit_us, stream),
+          "wait_timeout_probe");
+  return MOE_OK;
+}
+
 moe_status moe_clear_device_status(void* ws, moe_stream_t stream) {
   if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
   MOE_CU(cudaMemsetAsync(ws, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)));

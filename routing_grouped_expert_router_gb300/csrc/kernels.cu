@@ -9,6 +9,7 @@
 #include <cstdint>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -963,6 +964,24 @@ cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t*
     case 7: combine_kernel<7><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
     default: combine_kernel<8><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
   }
+  return launched();
+}
+
+// The bounded-wait path on its own: one thread waits on an mbarrier that
+// nothing will ever complete; the wait gives up after limit_ns and records
+// MOE_ERR_DEVICE_TIMEOUT (5) in *status, as a stalled matmul pipeline would.
+__global__ void wait_timeout_probe_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status, 5, limit_ns);
+}
+
+cudaError_t launch_wait_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t s) {
+  wait_timeout_probe_kernel<<<1, 32, 0, s>>>(status, limit_ns);
   return launched();
 }
 

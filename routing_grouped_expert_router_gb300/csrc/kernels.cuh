@@ -74,6 +74,8 @@ cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, l
 cudaError_t launch_quant_cols(const uint16_t* W, int E, int K, int N, int rows_per_e,
                               int group_stride, int slot, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s);
+// One bounded mbarrier wait that cannot complete: records status 5 after limit_ns.
+cudaError_t launch_wait_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t s);
 // dg[perm_src[p]] = sum_{i < nt} part[p * nt + i] for p < *nvalid (fixed order).
 cudaError_t launch_dg_reduce(const float* part, int nt, const int32_t* perm_src, long long rows,
                              const int32_t* nvalid, float* dg, int num_sms, cudaStream_t s);

@@ -49,14 +49,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records `code` in *status) if it has not completed after kWaitLimitNs.
+// records `code` in *status) if it has not completed after limit_ns
+// (kWaitLimitNs unless given).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
-                                          int code) {
+                                          int code, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       atomicExch(status, code);
       return false;
     }

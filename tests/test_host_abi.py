@@ -192,6 +192,13 @@ def test_fp8_shape_and_argument_checks(lib):
         == mb.MOE_ERR_INVALID_ARG           # rows beyond the source without idx
 
 
+def test_selftest_arguments_checked(lib):
+    assert lib.moe_selftest_wait_timeout(None, 10, None) == mb.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(FAKE + 16, 10, None) == mb.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(FAKE, 0, None) == mb.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(FAKE, 2000000, None) == mb.MOE_ERR_INVALID_ARG
+
+
 def test_profile_hook_without_events(lib):
     assert mb.moe_profile_events(None, 0) == 0
     assert mb.moe_profile_kernel_name(-1) == ""
