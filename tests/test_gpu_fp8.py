@@ -158,3 +158,68 @@ def test_fp8_layer_with_capacity(lib):
     with pytest.raises(mb.MoeError) as err:
         mb.moe_layer_fwd_fp8(ds, dev["x"], dev["Wg"], None, qw, run.y, run.saved, ws)
     assert err.value.status == mb.MOE_ERR_UNSUPPORTED
+
+
+def test_fp8_fullsize_sampled(lib):
+    """The FP8 forward at the full Mixtral-shaped size, in the bench's launch
+    configuration: routing and maps bit-exact; every code and scale of two
+    experts' quantised weights bit-exact; A, B and y rows of tokens routed to
+    those two experts against the FP8 oracle run on just those rows and
+    experts (row scales are per row, column scales per expert, so the
+    sampled computation is the full one restricted)."""
+    from routing_grouped_expert_router_gb300 import synth
+    from routing_grouped_expert_router_gb300.configs import CONFIGS
+    cfg = CONFIGS["mixtral8x7b"]
+    T, h, f, E, k = cfg.T, cfg.h, cfg.f, cfg.E, cfg.k
+    inp = synth.make_layer(cfg, "cuda")
+    x_cpu, _ = oracle.condition_router_margins(
+        inp["x"].cpu(), inp["Wg"].cpu(), inp["b"].cpu(), k,
+        lambda r, a: synth.replacement_x_rows(cfg, r, a))
+    inp["x"] = x_cpu.cuda()
+    d = mb.dims_of(cfg)
+    qw = _quant_weights(d, inp)
+    run = LayerRun(d)
+    ws = workspace(d, mb.OP_LAYER_FWD_FP8)
+    mb.moe_layer_fwd_fp8(d, inp["x"], inp["Wg"], None, qw, run.y, run.saved, ws)
+    run.bwd(inp)
+    torch.cuda.synchronize()
+    assert mb.moe_read_device_status(ws) == mb.MOE_OK and run.status() == mb.MOE_OK
+
+    idx, gates, _ = oracle.route(x_cpu, inp["Wg"].cpu(), inp["b"].cpu(), k)
+    counts, offsets, psrc, pdst = oracle.dispatch(idx, E)
+    np.testing.assert_array_equal(run.saved_view("topk_idx").cpu().numpy(), idx)
+    np.testing.assert_array_equal(run.saved_view("perm_src").cpu().numpy(), psrc)
+
+    pair = (0, 1)
+    both = np.nonzero(np.all(np.isin(idx, pair), axis=1))[0]
+    assert both.size >= 4
+    toks = both[np.linspace(0, both.size - 1, 4).astype(int)]
+    W13 = _view(d, qw, "W13q", (E, f // 128, 2, 128, h), torch.uint8)
+    W2v = _view(d, qw, "W2q", (E, h, f), torch.uint8)
+    s1v = _view(d, qw, "s1", (E, f), torch.float32).cpu().numpy()
+    s3v = _view(d, qw, "s3", (E, f), torch.float32).cpu().numpy()
+    s2v = _view(d, qw, "s2", (E, h), torch.float32).cpu().numpy()
+    x64 = oracle.as_f64(x_cpu)
+    O_rows = {}
+    A_gpu = run.saved_view("A")
+    B_gpu = run.saved_view("B")
+    for e in pair:
+        rows = [(int(t), j) for t in toks for j in range(k) if idx[t, j] == e]
+        X = x64[[t for t, _ in rows]]
+        f8 = oracle.expert_ffn_fwd_fp8(X, np.array([0, len(rows)]), inp["W1"][e:e + 1].cpu(),
+                                       inp["W3"][e:e + 1].cpu(), inp["W2"][e:e + 1].cpu())
+        # the expert's quantised weights, every code and scale
+        np.testing.assert_array_equal(s1v[e], f8["s1"][0])
+        np.testing.assert_array_equal(s3v[e], f8["s3"][0])
+        np.testing.assert_array_equal(s2v[e], f8["s2"][0])
+        Wg = _codes(W13[e])
+        np.testing.assert_array_equal(Wg[:, 0].reshape(f, h), f8["W1q"][0].T)
+        np.testing.assert_array_equal(Wg[:, 1].reshape(f, h), f8["W3q"][0].T)
+        np.testing.assert_array_equal(_codes(W2v[e]), f8["W2q"][0].T)
+        prow = [int(pdst[t * k + j]) for t, j in rows]
+        assert rel_l2(A_gpu[prow].double().cpu().numpy(), f8["A"]) <= 5e-3
+        assert rel_l2(B_gpu[prow].double().cpu().numpy(), f8["B"]) <= 5e-3
+        for i, key in enumerate(rows):
+            O_rows[key] = f8["O"][i]
+    y_ref = np.stack([sum(gates[t, j] * O_rows[(int(t), j)] for j in range(k)) for t in toks])
+    assert rel_l2(run.y[torch.from_numpy(toks)].double().cpu().numpy(), y_ref) <= 5e-3
