@@ -266,22 +266,25 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
   cp_async_wait<0>();
 }
 
-// ---- E > 8: lanes own experts.  A group of GL = min(32, EP) lanes handles
-// TOK tokens, lane i of a group the experts i, i + 32, ...  Each warp stages
-// its tokens' x slice (XS columns) in shared memory and reads it as
-// broadcasts; every weight value a lane loads from the staged chunk (one
-// conflict-free 4-byte load) then feeds TOK tokens.  No cross-lane reduction.
-constexpr int kRouterBTok = 16;
+// ---- E > 8: lanes own experts.  A group of GL = EP / 4 lanes handles TOK
+// tokens; lane i of a group owns the four consecutive experts 4i .. 4i + 3,
+// whose weights for one column are one conflict-free 16-byte shared-memory
+// load, so every unpacked x value feeds four FMAs.  Each warp stages its
+// tokens' x slice (XS columns) in shared memory and reads it as broadcasts
+// (the NG = 32 / GL groups of a warp read different token rows, which the
+// padded row pitch puts in different banks); every weight value a lane loads
+// then feeds TOK tokens.  No cross-lane reduction.
 constexpr int kRouterBXs = 64;
 constexpr int kRouterBXsp = kRouterBXs + 8;  // padded row (bf16) of a staged x slice
 
 template <int EP>
 struct RouterB {
-  static constexpr int GL = EP >= 32 ? 32 : EP;  // lanes per token group
+  static constexpr int EPL = 4;                  // experts per lane
+  static constexpr int GL = EP / EPL;            // lanes per token group
   static constexpr int NG = 32 / GL;             // token groups per warp
-  static constexpr int EPL = EP / GL;            // experts per lane
+  static constexpr int TOK = 8;                  // tokens per group
   static constexpr int CH = 32768 / EP;          // columns per chunk (128 KiB of weights)
-  static constexpr int XROWS = NG * kRouterBTok; // staged token rows per warp
+  static constexpr int XROWS = NG * TOK;         // staged token rows per warp
   static constexpr int SMEM = CH * EP * 4 + 8 * XROWS * kRouterBXsp * 2;
 };
 
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __rest
                                                           int h, int E, int nch,
                                                           float* __restrict__ partial) {
   using S = RouterB<EP>;
-  constexpr int TOK = kRouterBTok, XS = kRouterBXs, XSP = kRouterBXsp;
+  constexpr int TOK = S::TOK, EPL = S::EPL, XS = kRouterBXs, XSP = kRouterBXsp;
   extern __shared__ float sw[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(sw + S::CH * EP);
   const int lane = threadIdx.x & 31;
@@ -313,11 +316,11 @@ __global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __rest
   const int btile = 8 * S::XROWS;
   for (int t0 = sub * btile; t0 < T; t0 += bpc * btile) {
     const int tw = t0 + warp * S::XROWS;  // this warp's first token
-    float acc[TOK][S::EPL];
+    float acc[TOK][EPL];
 #pragma unroll
     for (int u = 0; u < TOK; ++u)
 #pragma unroll
-      for (int i = 0; i < S::EPL; ++i) acc[u][i] = 0.f;
+      for (int i = 0; i < EPL; ++i) acc[u][i] = 0.f;
     for (int cs = 0; cs < rows; cs += XS) {
       // stage x[tw .. tw + XROWS)[c0 + cs .. + XS) (rows of 128 bytes)
 #pragma unroll
@@ -326,9 +329,10 @@ __global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __rest
         const int row = id / (XS / 8);
         const int c8 = id % (XS / 8);
         const int t = tw + row;
-        const uint4 v = (t < T) ? __ldg(reinterpret_cast<const uint4*>(
-                                      x + static_cast<size_t>(t) * h + c0 + cs + 8 * c8))
-                                : make_uint4(0, 0, 0, 0);
+        const bool ok = t < T && cs + 8 * c8 < rows;
+        const uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(
+                                 x + static_cast<size_t>(t) * h + c0 + cs + 8 * c8))
+                           : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(xw + row * XSP + 8 * c8) = v;
       }
       __syncwarp();
@@ -338,18 +342,18 @@ __global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __rest
 #pragma unroll
         for (int u = 0; u < TOK; ++u)
           xq[u] = *reinterpret_cast<const uint4*>(xw + (g * TOK + u) * XSP + 8 * c8);
-        const float* wr = sw + (cs + 8 * c8) * EP + el;
+        const float4* wr = reinterpret_cast<const float4*>(sw + (cs + 8 * c8) * EP) + el;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float w[S::EPL];
-#pragma unroll
-          for (int i = 0; i < S::EPL; ++i) w[i] = wr[j * EP + S::GL * i];
+          const float4 w = wr[j * (EP / 4)];
 #pragma unroll
           for (int u = 0; u < TOK; ++u) {
             const uint32_t q = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
             const float xv = (j & 1) ? bf16_hi(q) : bf16_lo(q);
-#pragma unroll
-            for (int i = 0; i < S::EPL; ++i) acc[u][i] = fmaf(xv, w[i], acc[u][i]);
+            acc[u][0] = fmaf(xv, w.x, acc[u][0]);
+            acc[u][1] = fmaf(xv, w.y, acc[u][1]);
+            acc[u][2] = fmaf(xv, w.z, acc[u][2]);
+            acc[u][3] = fmaf(xv, w.w, acc[u][3]);
           }
         }
       }
@@ -359,9 +363,8 @@ __global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __rest
     for (int u = 0; u < TOK; ++u) {
       const int t = tw + g * TOK + u;
       if (t >= T) continue;
-      float* dst = partial + (static_cast<size_t>(c) * T + t) * EP + el;
-#pragma unroll
-      for (int i = 0; i < S::EPL; ++i) dst[S::GL * i] = acc[u][i];
+      *reinterpret_cast<float4*>(partial + (static_cast<size_t>(c) * T + t) * EP + EPL * el) =
+          make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
     }
   }
 }
