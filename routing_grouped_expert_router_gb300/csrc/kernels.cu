@@ -270,10 +270,11 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
 // tokens; lane i of a group owns the four consecutive experts 4i .. 4i + 3,
 // whose weights for one column are one conflict-free 16-byte shared-memory
 // load, so every unpacked x value feeds four FMAs.  Each warp stages its
-// tokens' x slice (XS columns) in shared memory and reads it as broadcasts
-// (the NG = 32 / GL groups of a warp read different token rows, which the
-// padded row pitch puts in different banks); every weight value a lane loads
-// then feeds TOK tokens.  No cross-lane reduction.
+// tokens' x slice (XS columns) in shared memory and reads it as broadcasts;
+// the slice is stored token-interleaved (token u of group g at row u NG + g),
+// so the NG groups of a warp read adjacent rows, which the padded pitch puts
+// in different banks.  Every weight value a lane loads then feeds TOK tokens.
+// No cross-lane reduction.
 constexpr int kRouterBXs = 64;
 constexpr int kRouterBXsp = kRouterBXs + 8;  // padded row (bf16) of a staged x slice
 
@@ -333,7 +334,8 @@ __global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __rest
         const uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(
                                  x + static_cast<size_t>(t) * h + c0 + cs + 8 * c8))
                            : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(xw + row * XSP + 8 * c8) = v;
+        const int srow = (row % TOK) * S::NG + row / TOK;  // token-interleaved
+        *reinterpret_cast<uint4*>(xw + srow * XSP + 8 * c8) = v;
       }
       __syncwarp();
 #pragma unroll 1
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __rest
         uint4 xq[TOK];
 #pragma unroll
         for (int u = 0; u < TOK; ++u)
-          xq[u] = *reinterpret_cast<const uint4*>(xw + (g * TOK + u) * XSP + 8 * c8);
+          xq[u] = *reinterpret_cast<const uint4*>(xw + (u * S::NG + g) * XSP + 8 * c8);
         const float4* wr = reinterpret_cast<const float4*>(sw + (cs + 8 * c8) * EP) + el;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
