@@ -184,11 +184,24 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
 #pragma unroll
   for (int g = 0; g < NST - 1; ++g) issue(g);
   // the weights are staged while the first x stages are in flight
-  for (int q = threadIdx.x; q < rows * EP; q += kRouterAThreads) {
-    const int lr = q / EP;
-    const int e = q - lr * EP;
-    sw[(lr >> 3) * SLICE + ((lr & 7) >> 1) * (2 * EP) + 2 * e + (lr & 1)] =
-        (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
+  if (E == EP) {
+    // a column pair per thread: two 32-byte rows in, four interleaved float4 out
+    for (int lr = 2 * threadIdx.x; lr < rows; lr += 2 * kRouterAThreads) {
+      const float4* src = reinterpret_cast<const float4*>(Wg + static_cast<size_t>(c0 + lr) * EP);
+      const float4 a0 = __ldg(src), a1 = __ldg(src + 1), b0 = __ldg(src + 2), b1 = __ldg(src + 3);
+      float4* dst = reinterpret_cast<float4*>(sw + (lr >> 3) * SLICE + ((lr & 7) >> 1) * (2 * EP));
+      dst[0] = make_float4(a0.x, b0.x, a0.y, b0.y);
+      dst[1] = make_float4(a0.z, b0.z, a0.w, b0.w);
+      dst[2] = make_float4(a1.x, b1.x, a1.y, b1.y);
+      dst[3] = make_float4(a1.z, b1.z, a1.w, b1.w);
+    }
+  } else {
+    for (int q = threadIdx.x; q < rows * EP; q += kRouterAThreads) {
+      const int lr = q / EP;
+      const int e = q - lr * EP;
+      sw[(lr >> 3) * SLICE + ((lr & 7) >> 1) * (2 * EP) + 2 * e + (lr & 1)] =
+          (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
+    }
   }
   __syncthreads();  // weights staged
 
