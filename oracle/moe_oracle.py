@@ -50,7 +50,8 @@ __all__ = [
     "expert_wgrad_columns", "condition_router_margins", "router_margin",
     "gemm_macs_fwd", "dispatch_bytes_per_token", "activation_bytes",
     "E4M3_MAX", "e4m3_round", "bf16_round", "quantize_rows_e4m3", "quantize_cols_e4m3",
-    "expert_ffn_fwd_fp8", "layer_fwd_fp8",
+    "expert_ffn_fwd_fp8", "layer_fwd_fp8", "quantize_rows_joint_e4m3", "fc2_dgrad_fp8",
+    "fc1_dgrad_fp8", "expert_ffn_bwd_fp8", "layer_bwd_fp8",
 ]
 
 
@@ -585,4 +586,102 @@ def layer_fwd_fp8(x, Wg, b, W1, W3, W2, k, capacity=None):
                perm_src=perm_src, perm_dst=perm_dst, x_perm=x_perm, k=k, fp8=f8,
                A=f8["A"], B=f8["B"], H=f8["H"], O=f8["O"])
     return y, ctx
+
+
+# ----------------------------------------------------- FP8 (e4m3) dgrads ---
+#
+# The backward's two data-gradient matmuls on e4m3 codes, with the same
+# per-token reading as the forward: the left operand's rows get one scale each
+# and the weights' output rows one scale each (amax over the contraction
+# dimension), so the scales again factor out of the sums.
+#   FC2 dgrad  dH = dO W2^T:  dO per row (its bf16 copy, dO = bf16(g * dy) in
+#              float32); W2[e] per row f (over h).
+#   FC1 dgrad  dX = dA W1^T + dB W3^T, one contraction over both halves: a row
+#              of dA and the same row of dB share one scale (amax over both
+#              bf16 rows), and row n of W1[e] and row n of W3[e] share one.
+# The weight gradients stay bf16 matmuls on the bf16 dO, dA, dB.
+
+def quantize_rows_joint_e4m3(X0, X1):
+    """Row i of X0 and row i of X1 quantised with one shared float32 scale
+    amax(|X0[i]|, |X1[i]|) / 448 (1 if both rows are zero)."""
+    X0_32 = np.asarray(X0, dtype=np.float32)
+    X1_32 = np.asarray(X1, dtype=np.float32)
+    amax = np.maximum(np.max(np.abs(X0_32), axis=1), np.max(np.abs(X1_32), axis=1))
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q0 = e4m3_round((X0_32 / s[:, None]).astype(np.float32))
+    q1 = e4m3_round((X1_32 / s[:, None]).astype(np.float32))
+    return q0, q1, s
+
+
+def fc2_dgrad_fp8(dO, W2e):
+    """dH = dO W2e^T on e4m3 codes: dO [n, h] per row, W2e [f, h] per row."""
+    dOq, sd = quantize_rows_e4m3(dO)
+    Wq, sw = quantize_rows_e4m3(W2e)
+    return (dOq @ Wq.T) * sd[:, None].astype(np.float64) * sw[None, :].astype(np.float64)
+
+
+def fc1_dgrad_fp8(dA, dB, W1e, W3e):
+    """dX = dA W1e^T + dB W3e^T on e4m3 codes: rows of dA and dB [n, f] share a
+    scale; rows n of W1e and W3e ([h, f]) share a scale."""
+    aq, bq, sa = quantize_rows_joint_e4m3(dA, dB)
+    w1q, w3q, sw = quantize_rows_joint_e4m3(W1e, W3e)
+    return (aq @ w1q.T + bq @ w3q.T) * sa[:, None].astype(np.float64) * sw[None, :].astype(
+        np.float64)
+
+
+def expert_ffn_bwd_fp8(dO, x_perm, offsets, W1, W3, W2, A, B, H):
+    """expert_ffn_bwd with both dgrads on e4m3 codes (recipe above).  dO must
+    be the bf16 values of g * dy; dA and dB are rounded to bf16 (as stored)
+    before the FC1 dgrad and the weight gradients use those bf16 copies."""
+    W1, W3, W2 = as_f64(W1), as_f64(W3), as_f64(W2)
+    E, h, f = W1.shape
+    X = np.asarray(x_perm, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    dW1 = np.zeros((E, h, f)); dW3 = np.zeros((E, h, f)); dW2 = np.zeros((E, f, h))
+    dA = np.zeros_like(A); dB = np.zeros_like(B); dX = np.zeros_like(X)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        dH = fc2_dgrad_fp8(dO[lo:hi], W2[e])
+        a = A[lo:hi]
+        sg = _sigmoid(a)
+        dA[lo:hi] = bf16_round(dH * B[lo:hi] * sg * (1.0 + a * (1.0 - sg)))
+        dB[lo:hi] = bf16_round(dH * silu(a))
+        dW2[e] = H[lo:hi].T @ dO[lo:hi]
+        dW1[e] = X[lo:hi].T @ dA[lo:hi]
+        dW3[e] = X[lo:hi].T @ dB[lo:hi]
+        dX[lo:hi] = fc1_dgrad_fp8(dA[lo:hi], dB[lo:hi], W1[e], W3[e])
+    return dict(dA=dA, dB=dB, dX_perm=dX, dW1=dW1, dW3=dW3, dW2=dW2)
+
+
+def layer_bwd_fp8(dy, x, Wg, W1, W3, W2, ctx):
+    """layer_bwd with the expert dgrads of expert_ffn_bwd_fp8; dO = bf16(g dy)
+    with the product in float32, dg = <dy, O> in float64."""
+    k = ctx["k"]
+    dy64 = as_f64(dy)
+    T, h = dy64.shape
+    Wg64 = as_f64(Wg)
+    E = Wg64.shape[1]
+    perm_src = np.asarray(ctx["perm_src"], dtype=np.int64)
+    perm_dst = np.asarray(ctx["perm_dst"], dtype=np.int64)
+    g32 = np.asarray(ctx["gates"], dtype=np.float32).ravel()
+    tok = perm_src // k
+    dO = bf16_round(g32[perm_src][:, None] * dy64[tok].astype(np.float32))
+    dg_perm = np.einsum("ph,ph->p", dy64[tok], ctx["O"])
+    dg = np.zeros(T * k)
+    dg[perm_src] = dg_perm
+    dg = dg.reshape(T, k)
+    ex = expert_ffn_bwd_fp8(dO, ctx["x_perm"], ctx["offsets"], W1, W3, W2,
+                            ctx["A"], ctx["B"], ctx["H"])
+    dl_sel = router_bwd(ctx["gates"], dg)
+    idx = np.asarray(ctx["topk_idx"], dtype=np.int64)
+    dl = np.zeros((T, E))
+    np.put_along_axis(dl, idx, dl_sel, axis=1)
+    dx = unpermute_rows(ex["dX_perm"], perm_dst).reshape(T, k, h).sum(axis=1)
+    dx = dx + dl @ Wg64.T
+    dWg = as_f64(x).T @ dl
+    out = dict(dx=dx, dWg=dWg, dg=dg, dl=dl, dO=dO)
+    out.update(ex)
+    return out
 

@@ -132,3 +132,69 @@ def test_fp8_layer_close_to_exact_and_backward_runs(E, k):
     g8 = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx8)
     for key in ("dx", "dW1", "dW2", "dWg"):
         assert rel_l2(g8[key], g[key]) < 0.2, key
+
+
+# ------------------------------------------------------------ FP8 dgrads ---
+
+def _codes_scaled(rng, shape, lo, hi):
+    """e4m3 codes times a power of two per row, with 448 in every row."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    c = codes.float().double().numpy()
+    c = c[np.isfinite(c) & (np.abs(c) <= 16)]
+    q = rng.choice(c, shape)
+    q[:, int(rng.integers(0, shape[1]))] = 448.0
+    j = rng.integers(lo, hi, shape[0])
+    return q * np.ldexp(1.0, j)[:, None], q, np.ldexp(1.0, j)
+
+
+def test_joint_row_quantiser_equals_quantiser_of_the_concatenation():
+    rng = np.random.default_rng(7)
+    X0 = rng.standard_normal((40, 24)) * np.exp(rng.uniform(-3, 3, (40, 1)))
+    X1 = rng.standard_normal((40, 16)) * np.exp(rng.uniform(-3, 3, (40, 1)))
+    X1[3] *= 100.0                                   # the amax sits in X1 for some rows
+    q0, q1, s = oracle.quantize_rows_joint_e4m3(X0, X1)
+    qc, sc = oracle.quantize_rows_e4m3(np.concatenate([X0, X1], axis=1))
+    np.testing.assert_array_equal(s, sc)
+    np.testing.assert_array_equal(np.concatenate([q0, q1], axis=1), qc)
+
+
+def test_fc2_dgrad_fp8_exact_on_quantisable_rows():
+    rng = np.random.default_rng(8)
+    dO, _, _ = _codes_scaled(rng, (12, 32), -14, -4)
+    W2, _, _ = _codes_scaled(rng, (20, 32), -12, -6)      # [f, h]: rows are f
+    np.testing.assert_allclose(oracle.fc2_dgrad_fp8(dO, W2), dO @ W2.T, rtol=1e-13, atol=0)
+    # the other axis (a scale per h column of W2, over f) is not exact here
+    Wq, sw = oracle.quantize_cols_e4m3(W2[None])
+    dq, sd = oracle.quantize_rows_e4m3(dO)
+    wrong = (dq * sd[:, None]) @ (Wq[0] * sw[0][None, :]).T
+    assert not np.allclose(wrong, dO @ W2.T, rtol=1e-9, atol=0)
+
+
+def test_fc1_dgrad_fp8_exact_on_jointly_quantisable_rows():
+    rng = np.random.default_rng(9)
+    dAB, _, _ = _codes_scaled(rng, (10, 48), -14, -4)
+    dA, dB = dAB[:, :24], dAB[:, 24:]
+    W13, _, _ = _codes_scaled(rng, (16, 48), -12, -6)     # rows n of [W1 | W3]
+    W1, W3 = W13[:, :24], W13[:, 24:]
+    np.testing.assert_allclose(oracle.fc1_dgrad_fp8(dA, dB, W1, W3), dA @ W1.T + dB @ W3.T,
+                               rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("E,k", [(4, 2), (6, 3)])
+def test_fp8_backward_close_to_exact_and_dO_is_bf16_of_fp32_product(E, k):
+    cfg = small_config(T=64, h=64, f=96, E=E, k=k, seed=700 + E)
+    inp = conditioned_inputs(cfg)
+    y, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"], k)
+    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    g8 = oracle.layer_bwd_fp8(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"],
+                              ctx)
+    # dO: the float32 product of gate and dy, rounded to bf16 (torch's conversion)
+    a = torch.from_numpy(np.asarray(ctx["perm_src"], dtype=np.int64))
+    gt = torch.from_numpy(np.asarray(ctx["gates"], dtype=np.float32)).reshape(-1)[a]
+    ref = (gt[:, None] * inp["dy"].float()[a // k]).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(g8["dO"], ref)
+    np.testing.assert_array_equal(g8["dg"], g["dg"])
+    for key in ("dx", "dW1", "dW3", "dW2", "dWg"):
+        e = rel_l2(g8[key], g[key])
+        assert e < 0.12, (key, e)
+    assert rel_l2(g8["dx"], g["dx"]) > 1e-3          # the quantisation is really there
