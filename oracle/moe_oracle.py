@@ -631,12 +631,16 @@ def fc1_dgrad_fp8(dA, dB, W1e, W3e):
 
 def expert_ffn_bwd_fp8(dO, x_perm, offsets, W1, W3, W2, A, B, H):
     """expert_ffn_bwd with both dgrads on e4m3 codes (recipe above).  dO must
-    be the bf16 values of g * dy; dA and dB are rounded to bf16 (as stored)
-    before the FC1 dgrad and the weight gradients use those bf16 copies."""
+    be the bf16 values of g * dy.  The activations are taken as stored, in
+    bf16 (A, B, H are rounded here): the e4m3 codes of dA and dB are integer
+    decisions, so they are made from the same values the layer keeps.  dA and
+    dB are rounded to bf16 (as stored) before the FC1 dgrad, and the weight
+    gradients use those bf16 copies."""
     W1, W3, W2 = as_f64(W1), as_f64(W3), as_f64(W2)
     E, h, f = W1.shape
     X = np.asarray(x_perm, dtype=np.float64)
     dO = np.asarray(dO, dtype=np.float64)
+    A, B, H = bf16_round(A), bf16_round(B), bf16_round(H)
     dW1 = np.zeros((E, h, f)); dW3 = np.zeros((E, h, f)); dW2 = np.zeros((E, f, h))
     dA = np.zeros_like(A); dB = np.zeros_like(B); dX = np.zeros_like(X)
     for e in range(E):
