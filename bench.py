@@ -34,7 +34,7 @@ from routing_grouped_expert_router_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s fwd+bwd; GroupedGEMM TFLOP/s as % of GB300 BF16 peak"
 GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc1_fwd_swiglu_fp8", "gg_fc2_fwd_fp8",
-         "gg_fc2_dgrad_swiglu_bwd",
+         "gg_fc2_dgrad_swiglu_bwd", "gg_fc2_dgrad_swiglu_bwd_fp8", "gg_fc1_dgrad_fp8",
          "gg_fc2_dgrad_swiglu_bwd_sar", "gg_fc2_wgrad", "gg_fc1_dgrad", "gg_fc1_wgrad")
 
 
@@ -61,6 +61,8 @@ def parse():
                    help="per-expert capacity = ceil(cf * T * k / E); 0 = dropless")
     p.add_argument("--fp8", action="store_true",
                    help="e4m3 expert forward (weights quantised inside every step)")
+    p.add_argument("--fp8-dgrad", action="store_true",
+                   help="e4m3 data-gradient matmuls in the backward (weights quantised every step)")
     return p.parse_args()
 
 
@@ -185,11 +187,12 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our layer ---
 class Layer:
-    def __init__(self, cfg, device, sar=False, capacity=0, fp8=False):
+    def __init__(self, cfg, device, sar=False, capacity=0, fp8=False, fp8_dgrad=False):
         from routing_grouped_expert_router_gb300 import binding as mb
         self.mb = mb
         self.cfg = cfg
         self.fp8 = fp8
+        self.fp8_dgrad = fp8_dgrad
         self.d = mb.dims_of(cfg, capacity=capacity, sar=sar)
         T, h, f, E = cfg.T, cfg.h, cfg.f, cfg.E
         dev = device
@@ -198,8 +201,10 @@ class Layer:
         self.ws_f = torch.zeros(mb.moe_workspace_bytes(self.d, op_f), dtype=torch.uint8, device=dev)
         self.qw = (torch.zeros(mb.moe_fp8_weight_bytes(self.d), dtype=torch.uint8, device=dev)
                    if fp8 else None)
-        self.ws_b = torch.zeros(mb.moe_workspace_bytes(self.d, mb.OP_LAYER_BWD), dtype=torch.uint8,
-                                device=dev)
+        self.qwb = (torch.zeros(mb.moe_fp8_bwd_weight_bytes(self.d), dtype=torch.uint8,
+                                device=dev) if fp8_dgrad else None)
+        op_b = mb.OP_LAYER_BWD_FP8 if fp8_dgrad else mb.OP_LAYER_BWD
+        self.ws_b = torch.zeros(mb.moe_workspace_bytes(self.d, op_b), dtype=torch.uint8, device=dev)
         self.y = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
         self.dx = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
         self.dWg = torch.empty(h, E, dtype=torch.float32, device=dev)
@@ -226,6 +231,12 @@ class Layer:
     def bwd(self, inp, x=None, dy=None):
         x = inp["x"] if x is None else x
         dy = inp["dy"] if dy is None else dy
+        if self.fp8_dgrad:
+            mb = self.mb
+            mb.moe_quantize_weights_fp8_bwd(self.d, inp["W1"], inp["W3"], inp["W2"], self.qwb)
+            mb.moe_layer_bwd_fp8(self.d, x, dy, inp["Wg"], self.qwb, self.saved, self.dx,
+                                 self.dWg, self.dW1, self.dW3, self.dW2, self.ws_b)
+            return
         self.mb.moe_layer_bwd(self.d, x, dy, inp["Wg"], inp["W1"], inp["W3"], inp["W2"],
                               self.saved, self.dx, self.dWg, self.dW1, self.dW3, self.dW2,
                               self.ws_b)
@@ -253,7 +264,8 @@ def run_ours(args, cfg, world, rank, local):
     inp = synth.make_layer(cfg_r, device)
     cap = (mb.capacity_for(cfg.T, cfg.k, cfg.E, args.capacity_factor)
            if args.capacity_factor > 0 else 0)
-    layer = Layer(cfg_r, device, sar=args.sar, capacity=cap, fp8=args.fp8)
+    layer = Layer(cfg_r, device, sar=args.sar, capacity=cap, fp8=args.fp8,
+                  fp8_dgrad=args.fp8_dgrad)
     stream = torch.cuda.current_stream(device)
 
     for _ in range(args.warmup):
@@ -522,12 +534,14 @@ def main():
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": n,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3 fwd" if args.fp8 else "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("bf16+e4m3" if (args.fp8 or args.fp8_dgrad) else "bf16"),
         "data": "synthetic",
         "config": {"workload": workload, "T": cfg.T, "h": cfg.h, "h_ffn": cfg.f, "E": cfg.E,
                    "top_k": cfg.k, "tokens_per_gpu_per_step": cfg.T,
                    "parallelism": f"replicas{n}" if n > 1 else "single",
                    "variant": ("fp8 forward, " if args.fp8 else "")
+                   + ("fp8 dgrads, " if args.fp8_dgrad else "")
                    + ("sar" if args.sar else "default")
                    + (f", capacity factor {args.capacity_factor}" if args.capacity_factor else
                       ", dropless"),

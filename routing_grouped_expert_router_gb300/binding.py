@@ -23,7 +23,7 @@ MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
 
 OP_ROUTE, OP_PERMUTE, OP_EXPERT_FFN_FWD, OP_EXPERT_FFN_BWD, OP_ROUTER_BWD, \
-    OP_LAYER_FWD, OP_LAYER_BWD, OP_LAYER_FWD_FP8 = range(8)
+    OP_LAYER_FWD, OP_LAYER_BWD, OP_LAYER_FWD_FP8, OP_LAYER_BWD_FP8 = range(9)
 
 HEADER = os.path.join(_build.ROOT, "include", "moe.h")
 
@@ -91,6 +91,10 @@ _SIGS = {
     "moe_quantize_rows_fp8": (_I, [_P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_int32,
                                    ctypes.c_int64, _P, _P, _P]),
     "moe_layer_fwd_fp8": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_fp8_bwd_weight_bytes": (_SZ, [_D]),
+    "moe_quantize_weights_fp8_bwd": (_I, [_D, _P, _P, _P, _P, _P]),
+    "moe_fp8_bwd_weight_view": (_P, [_D, _P, ctypes.c_char_p]),
+    "moe_layer_bwd_fp8": (_I, [_D] + [_P] * 10 + [_P, _SZ, _P]),
     "moe_version": (ctypes.c_char_p, []),
 }
 
@@ -299,3 +303,30 @@ def moe_layer_fwd_fp8(d, x, Wg, b, qw, y, saved, ws, ws_bytes=None, stream=None)
     _check(load().moe_layer_fwd_fp8(ctypes.byref(d), _addr(x), _addr(Wg), _addr(b), _addr(qw),
                                     _addr(y), _addr(saved), _addr(ws), ws_bytes, _stream(stream)),
            "moe_layer_fwd_fp8")
+
+
+def moe_fp8_bwd_weight_bytes(d) -> int:
+    return int(load().moe_fp8_bwd_weight_bytes(ctypes.byref(d)))
+
+
+def moe_quantize_weights_fp8_bwd(d, W1, W3, W2, qwb, stream=None):
+    _check(load().moe_quantize_weights_fp8_bwd(ctypes.byref(d), _addr(W1), _addr(W3), _addr(W2),
+                                               _addr(qwb), _stream(stream)),
+           "moe_quantize_weights_fp8_bwd")
+
+
+def moe_fp8_bwd_weight_view(d, qwb, name: str) -> int:
+    p = load().moe_fp8_bwd_weight_view(ctypes.byref(d), _addr(qwb), name.encode())
+    if not p:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"moe_fp8_bwd_weight_view({name})")
+    return int(p)
+
+
+def moe_layer_bwd_fp8(d, x, dy, Wg, qwb, saved, dx, dWg, dW1, dW3, dW2, ws, ws_bytes=None,
+                      stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check(load().moe_layer_bwd_fp8(ctypes.byref(d), _addr(x), _addr(dy), _addr(Wg), _addr(qwb),
+                                    _addr(saved), _addr(dx), _addr(dWg), _addr(dW1), _addr(dW3),
+                                    _addr(dW2), _addr(ws), ws_bytes, _stream(stream)),
+           "moe_layer_bwd_fp8")
+

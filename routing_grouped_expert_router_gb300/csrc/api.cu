@@ -61,7 +61,7 @@ moe_status check_dims(const moe_dims* d, bool routed) {
 
 bool routed_op(int op) {
   return op == MOE_OP_ROUTE || op == MOE_OP_LAYER_FWD || op == MOE_OP_LAYER_BWD ||
-         op == MOE_OP_LAYER_FWD_FP8;
+         op == MOE_OP_LAYER_FWD_FP8 || op == MOE_OP_LAYER_BWD_FP8;
 }
 
 
@@ -108,6 +108,23 @@ Fp8WeightLayout fp8_weight_layout(const moe_dims& d) {
 }
 bool fp8_shape_ok(const moe_dims& d) { return d.h % 128 == 0 && d.f % 128 == 0; }
 
+// The backward's quantised weights: per output row of each dgrad matmul.
+struct Fp8BwdWeightLayout {
+  size_t W2r, W1r, W3r, s2r, s13r, total;
+};
+Fp8BwdWeightLayout fp8_bwd_weight_layout(const moe_dims& d) {
+  const size_t E = d.E, h = d.h, f = d.f;
+  Carve c;
+  Fp8BwdWeightLayout L;
+  L.W2r = c.take(E * f * h);
+  L.W1r = c.take(E * h * f);
+  L.W3r = c.take(E * h * f);
+  L.s2r = c.take(E * f * 4);
+  L.s13r = c.take(E * h * 4);
+  L.total = c.off;
+  return L;
+}
+
 size_t rows_of(const moe_dims& d) { return static_cast<size_t>(d.T) * d.k; }
 
 struct SavedLayout {
@@ -150,6 +167,7 @@ struct WsLayout {
   size_t gH = 0, gate_rows = 0, dg_part = 0;  // sar backward
   size_t Xq = 0, sx = 0, Hq = 0, sh = 0;     // fp8 forward
   size_t h_amax = 0;                         // fp8 forward: per-tile amax of H
+  size_t dOq = 0, sdo = 0, dAq = 0, dBq = 0, sab = 0, ab_amax = 0;  // fp8 backward
   size_t total = 0;
 };
 WsLayout ws_layout(const moe_dims& d, int op) {
@@ -198,6 +216,15 @@ WsLayout ws_layout(const moe_dims& d, int op) {
       }
       break;
     case MOE_OP_LAYER_BWD:
+    case MOE_OP_LAYER_BWD_FP8:
+      if (op == MOE_OP_LAYER_BWD_FP8) {
+        L.dOq = c.take(R * d.h);
+        L.sdo = c.take(R * 4);
+        L.dAq = c.take(R * d.f);
+        L.dBq = c.take(R * d.f);
+        L.sab = c.take(R * 4);
+        L.ab_amax = c.take(R * static_cast<size_t>(moe::gemm_col_tiles(d.f)) * 4);
+      }
       expert_bwd(d.sar != 0);
       L.dX = c.take(R * d.h * 4);
       L.dg = c.take(R * 4);
@@ -767,6 +794,113 @@ moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x, const floa
   }
   MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
   return MOE_OK;
+}
+
+size_t moe_fp8_bwd_weight_bytes(const moe_dims* dims) {
+  if (check_dims(dims, false) != MOE_OK || !fp8_shape_ok(*dims)) return 0;
+  return fp8_bwd_weight_layout(*dims).total;
+}
+
+void* moe_fp8_bwd_weight_view(const moe_dims* dims, void* qwb, const char* name) {
+  if (check_dims(dims, false) != MOE_OK || !fp8_shape_ok(*dims) || !qwb || !name) return nullptr;
+  const Fp8BwdWeightLayout L = fp8_bwd_weight_layout(*dims);
+  struct {
+    const char* n;
+    size_t off;
+  } tab[] = {{"W2r", L.W2r}, {"W1r", L.W1r}, {"W3r", L.W3r}, {"s2r", L.s2r}, {"s13r", L.s13r}};
+  for (auto& e : tab)
+    if (strcmp(e.n, name) == 0) return at<uint8_t>(qwb, e.off);
+  return nullptr;
+}
+
+moe_status moe_quantize_weights_fp8_bwd(const moe_dims* dims, const moe_bf16* W1,
+                                        const moe_bf16* W3, const moe_bf16* W2, void* qwb,
+                                        moe_stream_t stream_) {
+  moe_status st = check_dims(dims, false);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!fp8_shape_ok(d)) return MOE_ERR_UNSUPPORTED;
+  if (!ptr_ok(W1) || !ptr_ok(W3) || !ptr_ok(W2) || !qwb || !aligned(qwb, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const Fp8BwdWeightLayout L = fp8_bwd_weight_layout(d);
+  const long long Ef = static_cast<long long>(d.E) * d.f;
+  const long long Eh = static_cast<long long>(d.E) * d.h;
+  // W2 [E, f, h]: rows f, scale over h
+  MOE_RUN(moe::launch_quant_rows(W2, nullptr, 1, Ef, Ef, d.h, at<uint8_t>(qwb, L.W2r),
+                                 at<float>(qwb, L.s2r), num_sms(), stream),
+          "quant_w2_rows");
+  // W1, W3 [E, h, f]: rows h, one scale over both matrices' rows
+  MOE_RUN(moe::launch_quant_rows(W1, nullptr, 1, Eh, Eh, d.f, at<uint8_t>(qwb, L.W1r),
+                                 at<float>(qwb, L.s13r), num_sms(), stream, nullptr, nullptr, 0,
+                                 nullptr, W3, at<uint8_t>(qwb, L.W3r)),
+          "quant_w13_rows");
+  return MOE_OK;
+}
+
+moe_status moe_layer_bwd_fp8(const moe_dims* dims, const moe_bf16* x, const moe_bf16* dy,
+                             const float* Wg, const void* qwb, const void* saved, moe_bf16* dx,
+                             float* dWg, float* dW1, float* dW3, float* dW2, void* ws,
+                             size_t ws_bytes, moe_stream_t stream_) {
+  moe_status st = check_dims(dims, true);
+  if (st != MOE_OK) return st;
+  const moe_dims& d = *dims;
+  if (!fp8_shape_ok(d) || d.sar) return MOE_ERR_UNSUPPORTED;
+  const size_t T = d.T;
+  if (!buf_ok(x, T) || !buf_ok(dy, T) || !ptr_ok(Wg) || !qwb || !aligned(qwb, kAlign) ||
+      !saved || !aligned(saved, kAlign) || !buf_ok(dx, T) || !ptr_ok(dWg) || !ptr_ok(dW1) ||
+      !ptr_ok(dW3) || !ptr_ok(dW2))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = ws_check(d, MOE_OP_LAYER_BWD_FP8, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const WsLayout L = ws_layout(d, MOE_OP_LAYER_BWD_FP8);
+  const SavedLayout S = saved_layout(d);
+  const Fp8BwdWeightLayout Q = fp8_bwd_weight_layout(d);
+  const int32_t* idx = at<int32_t>(saved, S.topk_idx);
+  const float* gates = at<float>(saved, S.gates);
+  const int32_t* offsets = at<int32_t>(saved, S.offsets);
+  const int32_t* psrc = at<int32_t>(saved, S.perm_src);
+  const int32_t* pdst = at<int32_t>(saved, S.perm_dst);
+  uint16_t* dO = at<uint16_t>(ws, L.dO);
+  uint16_t* dA = at<uint16_t>(ws, L.dA);
+  uint16_t* dB = at<uint16_t>(ws, L.dB);
+  float* dX = at<float>(ws, L.dX);
+  float* dg = at<float>(ws, L.dg);
+  const long long R = static_cast<long long>(rows_of(d));
+  const int32_t* nvalid = offsets + d.E;
+  MOE_RUN(moe::launch_bwd_prep(dy, at<uint16_t>(saved, S.O), gates, psrc, R, d.k, d.h, dO, dg,
+                               num_sms(), stream, nvalid),
+          "bwd_prep");
+  if (R == 0) {
+    const size_t wbytes = static_cast<size_t>(d.E) * d.h * d.f * 4;
+    MOE_RUN(cudaMemsetAsync(dW1, 0, wbytes, stream), "zero_dW1");
+    MOE_RUN(cudaMemsetAsync(dW3, 0, wbytes, stream), "zero_dW3");
+    MOE_RUN(cudaMemsetAsync(dW2, 0, wbytes, stream), "zero_dW2");
+  } else {
+    const GemmProblem g = problem(d, offsets, ws);
+    MOE_RUN(moe::launch_quant_rows(dO, nullptr, 1, R, R, d.h, at<uint8_t>(ws, L.dOq),
+                                   at<float>(ws, L.sdo), num_sms(), stream, nvalid),
+            "quant_dO");
+    MOE_RUN(moe::gemm_fc2_dgrad_fp8(g, at<uint8_t>(ws, L.dOq), at<float>(ws, L.sdo),
+                                    at<uint8_t>(qwb, Q.W2r), at<float>(qwb, Q.s2r),
+                                    at<uint16_t>(saved, S.A), at<uint16_t>(saved, S.B), dA, dB,
+                                    at<float>(ws, L.ab_amax), stream),
+            "gg_fc2_dgrad_swiglu_bwd_fp8");
+    MOE_RUN(moe::launch_quant_rows(dA, nullptr, 1, R, R, d.f, at<uint8_t>(ws, L.dAq),
+                                   at<float>(ws, L.sab), num_sms(), stream, nvalid,
+                                   at<float>(ws, L.ab_amax), moe::gemm_col_tiles(d.f), nullptr,
+                                   dB, at<uint8_t>(ws, L.dBq)),
+            "quant_dAdB");
+    MOE_RUN(moe::gemm_fc2_wgrad(g, at<uint16_t>(saved, S.H), dO, dW2, stream),
+            moe::kGemmNames[4]);
+    MOE_RUN(moe::gemm_fc1_dgrad_fp8(g, at<uint8_t>(ws, L.dAq), at<uint8_t>(ws, L.dBq),
+                                    at<float>(ws, L.sab), at<uint8_t>(qwb, Q.W1r),
+                                    at<uint8_t>(qwb, Q.W3r), at<float>(qwb, Q.s13r), dX, stream),
+            "gg_fc1_dgrad_fp8");
+    MOE_RUN(moe::gemm_fc1_wgrad(g, at<uint16_t>(saved, S.x_perm), dA, dB, dW1, dW3, stream),
+            moe::kGemmNames[5]);
+  }
+  return do_router_bwd(d, x, Wg, idx, gates, dg, dX, pdst, dx, dWg, ws, L, stream);
 }
 
 moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16* dy,

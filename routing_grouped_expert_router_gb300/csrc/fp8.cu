@@ -52,8 +52,9 @@ __device__ __forceinline__ uint32_t q2(float a, float b, float s) {
 // bf16 rounding of the largest of its nt fp32 partial maxima (the same value,
 // since rounding to nearest is monotone and symmetric) and the row is read
 // once.  With copy, the quantising pass also writes the bf16 row to copy[p]
-// (the permute of the same rows, fused).  Rows p >= *nvalid (when nvalid is
-// given) are skipped.
+// (the permute of the same rows, fused).  With in1/q1, row src of in1 is
+// quantised into q1 with the same scale, the amax taken over both rows.  Rows
+// p >= *nvalid (when nvalid is given) are skipped.
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ in,
                                                          const int32_t* __restrict__ idx, int div,
                                                          long long rows, long long src_rows,
@@ -61,7 +62,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
                                                          int n8, uint2* __restrict__ q,
                                                          float* __restrict__ scale,
                                                          const float* __restrict__ amax_part,
-                                                         int nt, uint4* __restrict__ copy) {
+                                                         int nt, uint4* __restrict__ copy,
+                                                         const uint4* __restrict__ in1,
+                                                         uint2* __restrict__ q1) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -73,16 +76,21 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     long long src = idx ? __ldg(idx + p) / div : p;
     src = src < 0 ? 0 : (src >= src_rows ? src_rows - 1 : src);
     const uint4* r = in + src * n8;
+    const uint4* r1 = in1 ? in1 + src * n8 : nullptr;
     float amax = 0.f;
     if (amax_part) {
       for (int i = lane; i < nt; i += 32) amax = fmaxf(amax, __ldg(amax_part + p * nt + i));
     } else {
       for (int c = lane; c < n8; c += 32) {
-        const uint4 w = __ldg(r + c);
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+        for (int which = 0; which < 2; ++which) {
+          if (which == 1 && !r1) break;
+          const uint4 w = __ldg((which ? r1 : r) + c);
+          const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+        }
       }
     }
 #pragma unroll
@@ -98,6 +106,14 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
       const uint32_t lo = q2(bf16_lo(w.x), bf16_hi(w.x), s) | (q2(bf16_lo(w.y), bf16_hi(w.y), s) << 16);
       const uint32_t hi = q2(bf16_lo(w.z), bf16_hi(w.z), s) | (q2(bf16_lo(w.w), bf16_hi(w.w), s) << 16);
       out[c] = make_uint2(lo, hi);
+      if (r1) {
+        const uint4 w1 = __ldg(r1 + c);
+        const uint32_t lo1 =
+            q2(bf16_lo(w1.x), bf16_hi(w1.x), s) | (q2(bf16_lo(w1.y), bf16_hi(w1.y), s) << 16);
+        const uint32_t hi1 =
+            q2(bf16_lo(w1.z), bf16_hi(w1.z), s) | (q2(bf16_lo(w1.w), bf16_hi(w1.w), s) << 16);
+        q1[p * n8 + c] = make_uint2(lo1, hi1);
+      }
     }
   }
 }
@@ -227,11 +243,12 @@ int grid_rows(long long rows, int num_sms) {
 cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                               long long src_rows, int n, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s, const int32_t* nvalid, const float* amax_part,
-                              int nt, uint16_t* copy) {
+                              int nt, uint16_t* copy, const uint16_t* in1, uint8_t* q1) {
   if (rows == 0 || src_rows == 0) return cudaSuccess;
   quant_rows_kernel<<<grid_rows(rows, num_sms), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(in), idx, div, rows, src_rows, nvalid, n / 8,
-      reinterpret_cast<uint2*>(q), scale, amax_part, nt, reinterpret_cast<uint4*>(copy));
+      reinterpret_cast<uint2*>(q), scale, amax_part, nt, reinterpret_cast<uint4*>(copy),
+      reinterpret_cast<const uint4*>(in1), reinterpret_cast<uint2*>(q1));
   return launched();
 }
 

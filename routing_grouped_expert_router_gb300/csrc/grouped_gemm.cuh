@@ -52,6 +52,18 @@ int gemm_fc1_col_tiles(int f);
 //   O = sh * s2 * (Hq W2q): Hq [rows, f]; W2q [E, h, f]; s2 [E, h]; sh [rows].
 cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& p, const void* Hq, const float* sh,
                              const void* W2q, const float* s2, void* O, cudaStream_t s);
+// FP8 data gradients:
+//   [dA, dB] from dH = sdo * s2r * (dOq W2r^T) as in gemm_fc2_dgrad, with
+//   ab_amax [rows, gemm_col_tiles(f)] = amax of |dA|, |dB| per 256-column tile;
+//   dOq [rows, h], W2r [E, f, h] e4m3, s2r [E, f], sdo [rows].
+cudaError_t gemm_fc2_dgrad_fp8(const GemmProblem& p, const void* dOq, const float* sdo,
+                               const void* W2r, const float* s2r, const void* A, const void* B,
+                               void* dA, void* dB, float* ab_amax, cudaStream_t s);
+//   dX = sab * s13r * (dAq W1r^T + dBq W3r^T), fp32 [rows, h]; dAq, dBq
+//   [rows, f], W1r, W3r [E, h, f] e4m3, s13r [E, h], sab [rows].
+cudaError_t gemm_fc1_dgrad_fp8(const GemmProblem& p, const void* dAq, const void* dBq,
+                               const float* sab, const void* W1r, const void* W3r,
+                               const float* s13r, float* dX, cudaStream_t s);
 // Output-column tiles of the M-grouped matmuls for n columns.
 int gemm_col_tiles(int n);
 // dX_perm = dA W1^T + dB W3^T (K = 2f), fp32 [rows, h].

@@ -62,12 +62,15 @@ cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, 
 // row, q row stride n bytes.
 // With amax_part [rows, nt] (fp32 partial maxima of |row|), the amax is taken
 // from it, rounded to bf16, and the row is read once.  With copy, the bf16
-// source rows are also written to copy [rows, n] (a fused permute).
+// source rows are also written to copy [rows, n] (a fused permute).  With in1
+// and q1, the same rows of in1 are quantised into q1 with a shared per-row
+// scale (amax over both rows).
 cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                               long long src_rows, int n, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s, const int32_t* nvalid = nullptr,
                               const float* amax_part = nullptr, int nt = 0,
-                              uint16_t* copy = nullptr);
+                              uint16_t* copy = nullptr, const uint16_t* in1 = nullptr,
+                              uint8_t* q1 = nullptr);
 // Columns of expert weights W [E, K, N]: scale[e, n] = amax_k |W[e, k, n]| / 448;
 // codes written K-major to row e * rows_per_e + (n / 128) * group_stride +
 // slot * 128 + n % 128 of q (K bytes per row).

@@ -223,3 +223,88 @@ def test_fp8_fullsize_sampled(lib):
             O_rows[key] = f8["O"][i]
     y_ref = np.stack([sum(gates[t, j] * O_rows[(int(t), j)] for j in range(k)) for t in toks])
     assert rel_l2(run.y[torch.from_numpy(toks)].double().cpu().numpy(), y_ref) <= 5e-3
+
+
+# --------------------------------------------------------- FP8 data gradients
+
+def _bwd_weights(d, dev):
+    qwb = torch.zeros(mb.moe_fp8_bwd_weight_bytes(d), dtype=torch.uint8, device="cuda")
+    mb.moe_quantize_weights_fp8_bwd(d, dev["W1"], dev["W3"], dev["W2"], qwb)
+    return qwb
+
+
+def _bview(d, qwb, name, shape, dtype):
+    off = mb.moe_fp8_bwd_weight_view(d, qwb, name) - qwb.data_ptr()
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    return qwb[off:off + n].view(dtype).view(shape)
+
+
+def test_bwd_weight_codes_and_scales_bit_exact(lib):
+    cfg = small_config(name="wqb", T=8, h=384, f=640, E=3, k=2, seed=23)
+    inp = conditioned_inputs(cfg)
+    d = mb.dims_of(cfg, has_bias=False)
+    qwb = _bwd_weights(d, _to(inp, "cuda"))
+    torch.cuda.synchronize()
+    E, h, f = cfg.E, cfg.h, cfg.f
+    W2r = _codes(_bview(d, qwb, "W2r", (E, f, h), torch.uint8))
+    W1r = _codes(_bview(d, qwb, "W1r", (E, h, f), torch.uint8))
+    W3r = _codes(_bview(d, qwb, "W3r", (E, h, f), torch.uint8))
+    s2r = _bview(d, qwb, "s2r", (E, f), torch.float32).cpu().numpy()
+    s13r = _bview(d, qwb, "s13r", (E, h), torch.float32).cpu().numpy()
+    for e in range(E):
+        q, s = oracle.quantize_rows_e4m3(oracle.as_f64(inp["W2"][e]))
+        np.testing.assert_array_equal(W2r[e], q)
+        np.testing.assert_array_equal(s2r[e], s)
+        q1, q3, s13 = oracle.quantize_rows_joint_e4m3(oracle.as_f64(inp["W1"][e]),
+                                                      oracle.as_f64(inp["W3"][e]))
+        np.testing.assert_array_equal(W1r[e], q1)
+        np.testing.assert_array_equal(W3r[e], q3)
+        np.testing.assert_array_equal(s13r[e], s13)
+
+
+@pytest.mark.parametrize("name,fwd8", [("tiny", False), ("mixtral_mid", True),
+                                       ("internal_mid_zipf", False), ("deepseek_mid", True),
+                                       ("hunyuan_mid", True), ("one_token", False),
+                                       ("ragged_tokens", True)])
+def test_fp8_backward_matches_fp8_oracle(lib, name, fwd8):
+    cfg = small_config(name=name, **CASES[name])
+    inp = conditioned_inputs(cfg)
+    fwd = oracle.layer_fwd_fp8 if fwd8 else oracle.layer_fwd
+    y, ctx = fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"], cfg.k)
+    g = oracle.layer_bwd_fp8(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    dev = _to(inp, "cuda")
+    d = mb.dims_of(cfg, has_bias=cfg.zipf_s > 0)
+    run = LayerRun(d)
+    b = dev["b"] if d.has_bias else None
+    if fwd8:
+        qw = _quant_weights(d, dev)
+        mb.moe_layer_fwd_fp8(d, dev["x"], dev["Wg"], b, qw, run.y, run.saved,
+                             workspace(d, mb.OP_LAYER_FWD_FP8))
+    else:
+        run.fwd(dev)
+    qwb = _bwd_weights(d, dev)
+    wsb = workspace(d, mb.OP_LAYER_BWD_FP8)
+    mb.moe_layer_bwd_fp8(d, dev["x"], dev["dy"], dev["Wg"], qwb, run.saved, run.dx, run.dWg,
+                         run.dW1, run.dW3, run.dW2, wsb)
+    torch.cuda.synchronize()
+    assert mb.moe_read_device_status(wsb) == mb.MOE_OK and run.status() == mb.MOE_OK
+    out = run.outputs()
+    assert rel_l2(out["y"].double().numpy(), y) <= TOL_Y
+    assert rel_l2(out["dx"].double().numpy(), g["dx"]) <= TOL_Y
+    for key in ("dW1", "dW3", "dW2", "dWg"):
+        assert rel_l2(out[key].numpy(), g[key]) <= TOL_W, key
+    if cfg.k == 1:
+        assert torch.all(out["dWg"] == 0)
+
+
+def test_fp8_backward_rejects_sar(lib):
+    cfg = small_config(name="sarb", T=64, h=128, f=128, E=4, k=2, seed=3)
+    d = mb.dims_of(cfg, has_bias=False, sar=True)
+    dev = _to(conditioned_inputs(cfg), "cuda")
+    run = LayerRun(d)
+    qwb = _bwd_weights(mb.dims_of(cfg, has_bias=False), dev)
+    with pytest.raises(mb.MoeError) as err:
+        mb.moe_layer_bwd_fp8(d, dev["x"], dev["dy"], dev["Wg"], qwb, run.saved, run.dx, run.dWg,
+                             run.dW1, run.dW3, run.dW2,
+                             workspace(mb.dims_of(cfg, has_bias=False), mb.OP_LAYER_BWD_FP8))
+    assert err.value.status == mb.MOE_ERR_UNSUPPORTED
