@@ -50,7 +50,7 @@ __all__ = [
     "expert_wgrad_columns", "condition_router_margins", "router_margin",
     "gemm_macs_fwd", "dispatch_bytes_per_token", "activation_bytes",
     "E4M3_MAX", "e4m3_round", "bf16_round", "quantize_rows_e4m3", "quantize_cols_e4m3",
-    "expert_ffn_fwd_fp8", "layer_fwd_fp8", "quantize_rows_joint_e4m3", "fc2_dgrad_fp8",
+    "expert_ffn_fwd_fp8", "layer_fwd_fp8", "quantize_rows_joint_e4m3",
     "fc1_dgrad_fp8", "expert_ffn_bwd_fp8", "layer_bwd_fp8",
 ]
 
@@ -588,18 +588,19 @@ def layer_fwd_fp8(x, Wg, b, W1, W3, W2, k, capacity=None):
     return y, ctx
 
 
-# ----------------------------------------------------- FP8 (e4m3) dgrads ---
+# ------------------------------------------------------ FP8 (e4m3) dgrad ---
 #
-# The backward's two data-gradient matmuls on e4m3 codes, with the same
+# The backward's FC1 data-gradient matmul on e4m3 codes, with the same
 # per-token reading as the forward: the left operand's rows get one scale each
 # and the weights' output rows one scale each (amax over the contraction
 # dimension), so the scales again factor out of the sums.
-#   FC2 dgrad  dH = dO W2^T:  dO per row (its bf16 copy, dO = bf16(g * dy) in
-#              float32); W2[e] per row f (over h).
 #   FC1 dgrad  dX = dA W1^T + dB W3^T, one contraction over both halves: a row
 #              of dA and the same row of dB share one scale (amax over both
 #              bf16 rows), and row n of W1[e] and row n of W3[e] share one.
-# The weight gradients stay bf16 matmuls on the bf16 dO, dA, dB.
+# FC2 dgrad (dH = dO W2^T with the SwiGLU backward) stays bf16: its time is
+# the fused SwiGLU-backward epilogue, which e4m3 operands do not shorten.  The
+# weight gradients stay bf16 matmuls on the bf16 dO, dA, dB; dO is the bf16
+# value of g * dy (product in float32).
 
 def quantize_rows_joint_e4m3(X0, X1):
     """Row i of X0 and row i of X1 quantised with one shared float32 scale
@@ -613,13 +614,6 @@ def quantize_rows_joint_e4m3(X0, X1):
     return q0, q1, s
 
 
-def fc2_dgrad_fp8(dO, W2e):
-    """dH = dO W2e^T on e4m3 codes: dO [n, h] per row, W2e [f, h] per row."""
-    dOq, sd = quantize_rows_e4m3(dO)
-    Wq, sw = quantize_rows_e4m3(W2e)
-    return (dOq @ Wq.T) * sd[:, None].astype(np.float64) * sw[None, :].astype(np.float64)
-
-
 def fc1_dgrad_fp8(dA, dB, W1e, W3e):
     """dX = dA W1e^T + dB W3e^T on e4m3 codes: rows of dA and dB [n, f] share a
     scale; rows n of W1e and W3e ([h, f]) share a scale."""
@@ -630,7 +624,7 @@ def fc1_dgrad_fp8(dA, dB, W1e, W3e):
 
 
 def expert_ffn_bwd_fp8(dO, x_perm, offsets, W1, W3, W2, A, B, H):
-    """expert_ffn_bwd with both dgrads on e4m3 codes (recipe above).  dO must
+    """expert_ffn_bwd with the FC1 dgrad on e4m3 codes (recipe above).  dO must
     be the bf16 values of g * dy.  The activations are taken as stored, in
     bf16 (A, B, H are rounded here): the e4m3 codes of dA and dB are integer
     decisions, so they are made from the same values the layer keeps.  dA and
@@ -647,7 +641,7 @@ def expert_ffn_bwd_fp8(dO, x_perm, offsets, W1, W3, W2, A, B, H):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi == lo:
             continue
-        dH = fc2_dgrad_fp8(dO[lo:hi], W2[e])
+        dH = dO[lo:hi] @ W2[e].T
         a = A[lo:hi]
         sg = _sigmoid(a)
         dA[lo:hi] = bf16_round(dH * B[lo:hi] * sg * (1.0 + a * (1.0 - sg)))
@@ -660,7 +654,7 @@ def expert_ffn_bwd_fp8(dO, x_perm, offsets, W1, W3, W2, A, B, H):
 
 
 def layer_bwd_fp8(dy, x, Wg, W1, W3, W2, ctx):
-    """layer_bwd with the expert dgrads of expert_ffn_bwd_fp8; dO = bf16(g dy)
+    """layer_bwd with the expert dgrad of expert_ffn_bwd_fp8; dO = bf16(g dy)
     with the product in float32, dg = <dy, O> in float64."""
     k = ctx["k"]
     dy64 = as_f64(dy)
