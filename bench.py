@@ -34,7 +34,7 @@ from routing_grouped_expert_router_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s fwd+bwd; GroupedGEMM TFLOP/s as % of GB300 BF16 peak"
 GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc1_fwd_swiglu_fp8", "gg_fc2_fwd_fp8",
-         "gg_fc2_dgrad_swiglu_bwd", "gg_fc2_dgrad_swiglu_bwd_fp8", "gg_fc1_dgrad_fp8",
+         "gg_fc2_dgrad_swiglu_bwd", "gg_fc1_dgrad_fp8",
          "gg_fc2_dgrad_swiglu_bwd_sar", "gg_fc2_wgrad", "gg_fc1_dgrad", "gg_fc1_wgrad")
 
 
@@ -62,7 +62,7 @@ def parse():
     p.add_argument("--fp8", action="store_true",
                    help="e4m3 expert forward (weights quantised inside every step)")
     p.add_argument("--fp8-dgrad", action="store_true",
-                   help="e4m3 data-gradient matmuls in the backward (weights quantised every step)")
+                   help="e4m3 FC1 data-gradient matmul in the backward (weights quantised every step)")
     return p.parse_args()
 
 
@@ -233,9 +233,9 @@ class Layer:
         dy = inp["dy"] if dy is None else dy
         if self.fp8_dgrad:
             mb = self.mb
-            mb.moe_quantize_weights_fp8_bwd(self.d, inp["W1"], inp["W3"], inp["W2"], self.qwb)
-            mb.moe_layer_bwd_fp8(self.d, x, dy, inp["Wg"], self.qwb, self.saved, self.dx,
-                                 self.dWg, self.dW1, self.dW3, self.dW2, self.ws_b)
+            mb.moe_quantize_weights_fp8_bwd(self.d, inp["W1"], inp["W3"], self.qwb)
+            mb.moe_layer_bwd_fp8(self.d, x, dy, inp["Wg"], inp["W2"], self.qwb, self.saved,
+                                 self.dx, self.dWg, self.dW1, self.dW3, self.dW2, self.ws_b)
             return
         self.mb.moe_layer_bwd(self.d, x, dy, inp["Wg"], inp["W1"], inp["W3"], inp["W2"],
                               self.saved, self.dx, self.dWg, self.dW1, self.dW3, self.dW2,
@@ -541,7 +541,7 @@ def main():
                    "top_k": cfg.k, "tokens_per_gpu_per_step": cfg.T,
                    "parallelism": f"replicas{n}" if n > 1 else "single",
                    "variant": ("fp8 forward, " if args.fp8 else "")
-                   + ("fp8 dgrads, " if args.fp8_dgrad else "")
+                   + ("fp8 FC1 dgrad, " if args.fp8_dgrad else "")
                    + ("sar" if args.sar else "default")
                    + (f", capacity factor {args.capacity_factor}" if args.capacity_factor else
                       ", dropless"),

@@ -307,35 +307,37 @@ moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x,
                              moe_bf16* y, void* saved, void* ws,
                              size_t ws_bytes, moe_stream_t stream);
 
-/* FP8 data gradients of the backward, with the same per-token reading: the
- * FC2 dgrad dH = dO W2^T takes dO per row (its bf16 copy, g * dy rounded)
- * and W2 per output row f; the FC1 dgrad dX = dA W1^T + dB W3^T is one
- * contraction over both halves, so a row of dA and the same row of dB share
- * one scale (taken from the FC2 dgrad's epilogue), and row n of W1 and row n
- * of W3 share one.  The weight gradients stay bf16 matmuls on the bf16 dO,
- * dA, dB.  Requires h, f multiples of 128 and dims.sar = 0.
+/* FP8 data gradient of the backward, with the same per-token reading: the
+ * FC1 dgrad dX = dA W1^T + dB W3^T runs on e4m3 codes as one contraction
+ * over both halves, so a row of dA and the same row of dB share one scale
+ * (their amax is recorded by the FC2 dgrad's epilogue) and row n of W1[e] and
+ * row n of W3[e] share one.  FC2 dgrad stays bf16: its cost is the fused
+ * SwiGLU backward in its epilogue, which e4m3 operands do not shorten
+ * (measured).  The weight gradients stay bf16 matmuls on the bf16 dO, dA,
+ * dB.  Requires h, f multiples of 128 and dims.sar = 0.
  *
  * moe_quantize_weights_fp8_bwd writes into `qwb` (256-byte aligned,
- * moe_fp8_bwd_weight_bytes): "W2r" [E, f, h] e4m3 (row f of W2[e] over h),
- * "W1r", "W3r" [E, h, f] e4m3 (row n of W1[e] and of W3[e] with one shared
- * scale), "s2r" [E, f] and "s13r" [E, h] float32; moe_fp8_bwd_weight_view
- * gives each part's address.  Call it after every weight update. */
+ * moe_fp8_bwd_weight_bytes): "W1r", "W3r" [E, h, f] e4m3 (row n of W1[e] and
+ * of W3[e] with one shared scale) and "s13r" [E, h] float32;
+ * moe_fp8_bwd_weight_view gives each part's address.  Call it after every
+ * weight update. */
 size_t moe_fp8_bwd_weight_bytes(const moe_dims* dims);
 moe_status moe_quantize_weights_fp8_bwd(const moe_dims* dims,
                                         const moe_bf16* W1, const moe_bf16* W3,
-                                        const moe_bf16* W2, void* qwb,
-                                        moe_stream_t stream);
+                                        void* qwb, moe_stream_t stream);
 void* moe_fp8_bwd_weight_view(const moe_dims* dims, void* qwb,
                               const char* name);
 
-/* moe_layer_bwd with the FP8 data gradients above, from a `saved` context of
- * moe_layer_fwd or moe_layer_fwd_fp8 (sar = 0).  Same outputs as
- * moe_layer_bwd.  Workspace: moe_workspace_bytes(dims, MOE_OP_LAYER_BWD_FP8). */
+/* moe_layer_bwd with the FP8 FC1 data gradient above, from a `saved` context
+ * of moe_layer_fwd or moe_layer_fwd_fp8 (sar = 0).  W2 (bf16) feeds the FC2
+ * dgrad.  Same outputs as moe_layer_bwd.  Workspace:
+ * moe_workspace_bytes(dims, MOE_OP_LAYER_BWD_FP8). */
 moe_status moe_layer_bwd_fp8(const moe_dims* dims, const moe_bf16* x,
                              const moe_bf16* dy, const float* Wg,
-                             const void* qwb, const void* saved, moe_bf16* dx,
-                             float* dWg, float* dW1, float* dW3, float* dW2,
-                             void* ws, size_t ws_bytes, moe_stream_t stream);
+                             const moe_bf16* W2, const void* qwb,
+                             const void* saved, moe_bf16* dx, float* dWg,
+                             float* dW1, float* dW3, float* dW2, void* ws,
+                             size_t ws_bytes, moe_stream_t stream);
 
 /* Whole layer backward from `saved`: writes dx [T,h] bf16 and the fp32
  * gradients dWg, dW1, dW3, dW2.  The router bias gets no gradient. */

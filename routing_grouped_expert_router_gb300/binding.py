@@ -92,9 +92,9 @@ _SIGS = {
                                    ctypes.c_int64, _P, _P, _P]),
     "moe_layer_fwd_fp8": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_fp8_bwd_weight_bytes": (_SZ, [_D]),
-    "moe_quantize_weights_fp8_bwd": (_I, [_D, _P, _P, _P, _P, _P]),
+    "moe_quantize_weights_fp8_bwd": (_I, [_D, _P, _P, _P, _P]),
     "moe_fp8_bwd_weight_view": (_P, [_D, _P, ctypes.c_char_p]),
-    "moe_layer_bwd_fp8": (_I, [_D] + [_P] * 10 + [_P, _SZ, _P]),
+    "moe_layer_bwd_fp8": (_I, [_D] + [_P] * 11 + [_P, _SZ, _P]),
     "moe_version": (ctypes.c_char_p, []),
 }
 
@@ -309,8 +309,8 @@ def moe_fp8_bwd_weight_bytes(d) -> int:
     return int(load().moe_fp8_bwd_weight_bytes(ctypes.byref(d)))
 
 
-def moe_quantize_weights_fp8_bwd(d, W1, W3, W2, qwb, stream=None):
-    _check(load().moe_quantize_weights_fp8_bwd(ctypes.byref(d), _addr(W1), _addr(W3), _addr(W2),
+def moe_quantize_weights_fp8_bwd(d, W1, W3, qwb, stream=None):
+    _check(load().moe_quantize_weights_fp8_bwd(ctypes.byref(d), _addr(W1), _addr(W3),
                                                _addr(qwb), _stream(stream)),
            "moe_quantize_weights_fp8_bwd")
 
@@ -322,10 +322,11 @@ def moe_fp8_bwd_weight_view(d, qwb, name: str) -> int:
     return int(p)
 
 
-def moe_layer_bwd_fp8(d, x, dy, Wg, qwb, saved, dx, dWg, dW1, dW3, dW2, ws, ws_bytes=None,
+def moe_layer_bwd_fp8(d, x, dy, Wg, W2, qwb, saved, dx, dWg, dW1, dW3, dW2, ws, ws_bytes=None,
                       stream=None):
     ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
-    _check(load().moe_layer_bwd_fp8(ctypes.byref(d), _addr(x), _addr(dy), _addr(Wg), _addr(qwb),
+    _check(load().moe_layer_bwd_fp8(ctypes.byref(d), _addr(x), _addr(dy), _addr(Wg), _addr(W2),
+                                    _addr(qwb),
                                     _addr(saved), _addr(dx), _addr(dWg), _addr(dW1), _addr(dW3),
                                     _addr(dW2), _addr(ws), ws_bytes, _stream(stream)),
            "moe_layer_bwd_fp8")

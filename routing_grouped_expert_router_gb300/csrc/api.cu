@@ -108,18 +108,17 @@ Fp8WeightLayout fp8_weight_layout(const moe_dims& d) {
 }
 bool fp8_shape_ok(const moe_dims& d) { return d.h % 128 == 0 && d.f % 128 == 0; }
 
-// The backward's quantised weights: per output row of each dgrad matmul.
+// The backward's quantised weights: FC1 dgrad's B operand, per output row h
+// of W1[e] and W3[e] with one shared scale.
 struct Fp8BwdWeightLayout {
-  size_t W2r, W1r, W3r, s2r, s13r, total;
+  size_t W1r, W3r, s13r, total;
 };
 Fp8BwdWeightLayout fp8_bwd_weight_layout(const moe_dims& d) {
   const size_t E = d.E, h = d.h, f = d.f;
   Carve c;
   Fp8BwdWeightLayout L;
-  L.W2r = c.take(E * f * h);
   L.W1r = c.take(E * h * f);
   L.W3r = c.take(E * h * f);
-  L.s2r = c.take(E * f * 4);
   L.s13r = c.take(E * h * 4);
   L.total = c.off;
   return L;
@@ -167,7 +166,7 @@ struct WsLayout {
   size_t gH = 0, gate_rows = 0, dg_part = 0;  // sar backward
   size_t Xq = 0, sx = 0, Hq = 0, sh = 0;     // fp8 forward
   size_t h_amax = 0;                         // fp8 forward: per-tile amax of H
-  size_t dOq = 0, sdo = 0, dAq = 0, dBq = 0, sab = 0, ab_amax = 0;  // fp8 backward
+  size_t dAq = 0, dBq = 0, sab = 0, ab_amax = 0;  // fp8 backward
   size_t total = 0;
 };
 WsLayout ws_layout(const moe_dims& d, int op) {
@@ -218,8 +217,6 @@ WsLayout ws_layout(const moe_dims& d, int op) {
     case MOE_OP_LAYER_BWD:
     case MOE_OP_LAYER_BWD_FP8:
       if (op == MOE_OP_LAYER_BWD_FP8) {
-        L.dOq = c.take(R * d.h);
-        L.sdo = c.take(R * 4);
         L.dAq = c.take(R * d.f);
         L.dBq = c.take(R * d.f);
         L.sab = c.take(R * 4);
@@ -807,29 +804,22 @@ void* moe_fp8_bwd_weight_view(const moe_dims* dims, void* qwb, const char* name)
   struct {
     const char* n;
     size_t off;
-  } tab[] = {{"W2r", L.W2r}, {"W1r", L.W1r}, {"W3r", L.W3r}, {"s2r", L.s2r}, {"s13r", L.s13r}};
+  } tab[] = {{"W1r", L.W1r}, {"W3r", L.W3r}, {"s13r", L.s13r}};
   for (auto& e : tab)
     if (strcmp(e.n, name) == 0) return at<uint8_t>(qwb, e.off);
   return nullptr;
 }
 
 moe_status moe_quantize_weights_fp8_bwd(const moe_dims* dims, const moe_bf16* W1,
-                                        const moe_bf16* W3, const moe_bf16* W2, void* qwb,
-                                        moe_stream_t stream_) {
+                                        const moe_bf16* W3, void* qwb, moe_stream_t stream_) {
   moe_status st = check_dims(dims, false);
   if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
   if (!fp8_shape_ok(d)) return MOE_ERR_UNSUPPORTED;
-  if (!ptr_ok(W1) || !ptr_ok(W3) || !ptr_ok(W2) || !qwb || !aligned(qwb, kAlign))
-    return MOE_ERR_INVALID_ARG;
+  if (!ptr_ok(W1) || !ptr_ok(W3) || !qwb || !aligned(qwb, kAlign)) return MOE_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const Fp8BwdWeightLayout L = fp8_bwd_weight_layout(d);
-  const long long Ef = static_cast<long long>(d.E) * d.f;
   const long long Eh = static_cast<long long>(d.E) * d.h;
-  // W2 [E, f, h]: rows f, scale over h
-  MOE_RUN(moe::launch_quant_rows(W2, nullptr, 1, Ef, Ef, d.h, at<uint8_t>(qwb, L.W2r),
-                                 at<float>(qwb, L.s2r), num_sms(), stream),
-          "quant_w2_rows");
   // W1, W3 [E, h, f]: rows h, one scale over both matrices' rows
   MOE_RUN(moe::launch_quant_rows(W1, nullptr, 1, Eh, Eh, d.f, at<uint8_t>(qwb, L.W1r),
                                  at<float>(qwb, L.s13r), num_sms(), stream, nullptr, nullptr, 0,
@@ -839,7 +829,8 @@ moe_status moe_quantize_weights_fp8_bwd(const moe_dims* dims, const moe_bf16* W1
 }
 
 moe_status moe_layer_bwd_fp8(const moe_dims* dims, const moe_bf16* x, const moe_bf16* dy,
-                             const float* Wg, const void* qwb, const void* saved, moe_bf16* dx,
+                             const float* Wg, const moe_bf16* W2, const void* qwb,
+                             const void* saved, moe_bf16* dx,
                              float* dWg, float* dW1, float* dW3, float* dW2, void* ws,
                              size_t ws_bytes, moe_stream_t stream_) {
   moe_status st = check_dims(dims, true);
@@ -847,7 +838,8 @@ moe_status moe_layer_bwd_fp8(const moe_dims* dims, const moe_bf16* x, const moe_
   const moe_dims& d = *dims;
   if (!fp8_shape_ok(d) || d.sar) return MOE_ERR_UNSUPPORTED;
   const size_t T = d.T;
-  if (!buf_ok(x, T) || !buf_ok(dy, T) || !ptr_ok(Wg) || !qwb || !aligned(qwb, kAlign) ||
+  if (!buf_ok(x, T) || !buf_ok(dy, T) || !ptr_ok(Wg) || !ptr_ok(W2) || !qwb ||
+      !aligned(qwb, kAlign) ||
       !saved || !aligned(saved, kAlign) || !buf_ok(dx, T) || !ptr_ok(dWg) || !ptr_ok(dW1) ||
       !ptr_ok(dW3) || !ptr_ok(dW2))
     return MOE_ERR_INVALID_ARG;
@@ -878,14 +870,11 @@ moe_status moe_layer_bwd_fp8(const moe_dims* dims, const moe_bf16* x, const moe_
     MOE_RUN(cudaMemsetAsync(dW2, 0, wbytes, stream), "zero_dW2");
   } else {
     const GemmProblem g = problem(d, offsets, ws);
-    MOE_RUN(moe::launch_quant_rows(dO, nullptr, 1, R, R, d.h, at<uint8_t>(ws, L.dOq),
-                                   at<float>(ws, L.sdo), num_sms(), stream, nvalid),
-            "quant_dO");
-    MOE_RUN(moe::gemm_fc2_dgrad_fp8(g, at<uint8_t>(ws, L.dOq), at<float>(ws, L.sdo),
-                                    at<uint8_t>(qwb, Q.W2r), at<float>(qwb, Q.s2r),
-                                    at<uint16_t>(saved, S.A), at<uint16_t>(saved, S.B), dA, dB,
-                                    at<float>(ws, L.ab_amax), stream),
-            "gg_fc2_dgrad_swiglu_bwd_fp8");
+    // FC2 dgrad stays bf16 (its cost is the fused SwiGLU-backward epilogue);
+    // it also records the per-tile amax of dA and dB for their e4m3 scale
+    MOE_RUN(moe::gemm_fc2_dgrad(g, dO, W2, at<uint16_t>(saved, S.A), at<uint16_t>(saved, S.B), dA,
+                                dB, stream, at<float>(ws, L.ab_amax)),
+            moe::kGemmNames[2]);
     MOE_RUN(moe::launch_quant_rows(dA, nullptr, 1, R, R, d.f, at<uint8_t>(ws, L.dAq),
                                    at<float>(ws, L.sab), num_sms(), stream, nvalid,
                                    at<float>(ws, L.ab_amax), moe::gemm_col_tiles(d.f), nullptr,

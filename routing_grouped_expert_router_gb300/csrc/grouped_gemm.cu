@@ -75,20 +75,17 @@ enum Epi {
   EPI_SWIGLU_BWD_SAR = 5,  // SwiGLU backward that rebuilds H from A, B (no saved H or O)
   EPI_SWIGLU_F8 = 6,       // EPI_SWIGLU on e4m3 operands: sums rescaled by row x column scales
   EPI_BF16_F8 = 7,         // EPI_BF16 on e4m3 operands, likewise
-  EPI_SWIGLU_BWD_F8 = 8,   // EPI_SWIGLU_BWD on e4m3 operands (+ amax of dA, dB per tile)
-  EPI_F32_F8 = 9           // EPI_F32 on e4m3 operands
+  EPI_F32_F8 = 8           // EPI_F32 on e4m3 operands
 };
 __host__ __device__ constexpr bool is_f8(int epi) {
-  return epi == EPI_SWIGLU_F8 || epi == EPI_BF16_F8 || epi == EPI_SWIGLU_BWD_F8 ||
-         epi == EPI_F32_F8;
+  return epi == EPI_SWIGLU_F8 || epi == EPI_BF16_F8 || epi == EPI_F32_F8;
 }
 // The epilogue an FP8 matmul runs after rescaling its sums.
 __host__ __device__ constexpr int base_epi(int epi) {
-  return epi == EPI_SWIGLU_F8       ? EPI_SWIGLU
-         : epi == EPI_BF16_F8       ? EPI_BF16
-         : epi == EPI_SWIGLU_BWD_F8 ? EPI_SWIGLU_BWD
-         : epi == EPI_F32_F8        ? EPI_F32
-                                    : epi;
+  return epi == EPI_SWIGLU_F8 ? EPI_SWIGLU
+         : epi == EPI_BF16_F8 ? EPI_BF16
+         : epi == EPI_F32_F8  ? EPI_F32
+                              : epi;
 }
 
 struct Params {
@@ -107,7 +104,8 @@ struct Params {
   const void* in1;
   const float* in2;  // EPI_SWIGLU_BWD_SAR: gate of each permuted row
   float* part;       // EPI_SWIGLU_BWD_SAR: per-(row, n-tile) partial sums of <H, dY W2^T>;
-                     // EPI_SWIGLU_F8: per-(row, n-tile) amax of H
+                     // EPI_SWIGLU_F8: per-(row, n-tile) amax of H;
+                     // EPI_SWIGLU_BWD (optional): per-(row, n-tile) amax of dA and dB
   int part_ld;       // n-tiles per row of `part`
   const float* row_scale;   // FP8: scale of each A row (permuted row)
   const float* col_scale0;  // FP8: [E, N] scales of the B columns (first operand)
@@ -312,7 +310,7 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, int grow, int 
   unpack_bf16x32(ra, av);
   unpack_bf16x32(rb, bv);
   float da[32], db[32];
-  if (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_F8) {
+  if (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float a = av[i];
@@ -321,7 +319,7 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, int grow, int 
       da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
       db[i] = dh * a * sg;
     }
-    if (EPI == EPI_SWIGLU_BWD_F8) {  // amax of the row's dA and dB for their shared e4m3 scale
+    if (p.part) {  // amax of the row's dA and dB, for their shared e4m3 scale downstream
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc = fmaxf(acc, fmaxf(fabsf(da[i]), fabsf(db[i])));
     }
@@ -617,8 +615,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int grow = tl.row0 + r;                        // M-grouped row
       const bool row_ok = GROUP_K ? (tl.mb * BM + r < p.M) : (grow < tl.row_end);
       float acc = 0.f;
-      if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR ||
-                    EPI == EPI_SWIGLU_BWD_F8) {
+      if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
         // A and B of chunk ch + 1 are in flight while chunk ch is computed
         const size_t o0 = static_cast<size_t>(grow) * p.ldo + tl.nb * BNB;
         uint4 ra[4], rb[4];
@@ -637,7 +634,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float v0[32];
           tmem_ld32(tbase + ch * 32, v0);
           if (!row_ok || col >= p.N) continue;
-          if (is_f8(EPI)) rescale_f8<NUM_B>(p, tl, grow, col, v0, v0);
           swiglu_bwd_chunk<EPI>(p, grow, col, v0, ca, cb, acc);
         }
       } else {
@@ -653,8 +649,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1, acc);
         }
       }
-      if ((EPI == EPI_SWIGLU_BWD_SAR || EPI == EPI_SWIGLU_F8 || EPI == EPI_SWIGLU_BWD_F8) &&
-          row_ok)
+      if ((EPI == EPI_SWIGLU_BWD_SAR || EPI == EPI_SWIGLU_F8 ||
+           (EPI == EPI_SWIGLU_BWD && p.part)) && row_ok)
         p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
       tc_fence_before();
       mbar_arrive(smem_u32(&c.tempty[buf]));
@@ -988,7 +984,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           epilogue_chunk<NUM_B, EPI>(p, tl, grow, orow, col, v0, v1, acc);
         }
       }
-      if (EPI == EPI_SWIGLU_BWD_SAR && row_ok)
+      if ((EPI == EPI_SWIGLU_BWD_SAR || (EPI == EPI_SWIGLU_BWD && p.part)) && row_ok)
         p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
       tc_fence_before();
       __syncwarp();
@@ -1185,7 +1181,7 @@ cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, vo
 }
 
 cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2, const void* A,
-                           const void* B, void* dA, void* dB, cudaStream_t s) {
+                           const void* B, void* dA, void* dB, cudaStream_t s, float* ab_amax) {
   Maps m;
   memset(&m, 0, sizeof(m));
   // B operand: W2[e] viewed as [f rows (N), h (K)] -- K-major
@@ -1203,6 +1199,8 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.out0 = dA;
   p.out1 = dB;
   p.ldo = g.f;
+  p.part = ab_amax;
+  p.part_ld = gemm_col_tiles(g.f);
   return launch<false, false, 1, EPI_SWIGLU_BWD, false>(p, m, mgrouped_tiles(g, EPI_SWIGLU_BWD, g.f, BN),
                                                          g.num_sms, s);
 }
@@ -1211,34 +1209,6 @@ int gemm_col_tiles(int n) { return (n + BN - 1) / BN; }
 int gemm_fc1_col_tiles(int f) { return (f + BN / 2 - 1) / (BN / 2); }
 
 // FP8 data gradients (one-CTA kernel, e4m3 K-major operands).
-cudaError_t gemm_fc2_dgrad_fp8(const GemmProblem& g, const void* dOq, const float* sdo,
-                               const void* W2r, const float* s2r, const void* A, const void* B,
-                               void* dA, void* dB, float* ab_amax, cudaStream_t s) {
-  Maps m;
-  memset(&m, 0, sizeof(m));
-  // A: dOq [rows, h];  B: W2r [E * f rows (N), h (K)]
-  if (!make_map(&m.a0, dOq, g.h, g.rows, 2 * BK, BM, true) ||
-      !make_map(&m.b0, W2r, g.h, static_cast<uint64_t>(g.E) * g.f, 2 * BK, BN, true))
-    return cudaErrorInvalidValue;
-  m.a1 = m.a0;
-  m.b1 = m.b0;
-  Params p = base_params(g);
-  p.N = g.f;
-  p.kblocks = g.h / (2 * BK);
-  p.b_rows = g.f;
-  p.in0 = A;
-  p.in1 = B;
-  p.row_scale = sdo;
-  p.col_scale0 = s2r;
-  p.part = ab_amax;
-  p.part_ld = gemm_col_tiles(g.f);
-  p.out0 = dA;
-  p.out1 = dB;
-  p.ldo = g.f;
-  return launch<false, false, 1, EPI_SWIGLU_BWD_F8, false>(
-      p, m, mgrouped_tiles(g, EPI_SWIGLU_BWD_F8, g.f, BN), g.num_sms, s);
-}
-
 cudaError_t gemm_fc1_dgrad_fp8(const GemmProblem& g, const void* dAq, const void* dBq,
                                const float* sab, const void* W1r, const void* W3r,
                                const float* s13r, float* dX, cudaStream_t s) {

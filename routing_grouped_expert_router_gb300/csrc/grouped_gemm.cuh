@@ -27,9 +27,12 @@ cudaError_t gemm_fc1_fwd(const GemmProblem& p, const void* x_perm, const void* W
 cudaError_t gemm_fc2_fwd(const GemmProblem& p, const void* H, const void* W2, void* O,
                          cudaStream_t s);
 // dH = dO W2^T, fused with the SwiGLU backward: dA = dH * B * s (1 + A (1 - s)),
-// dB = dH * silu(A).  dO: [rows, h]; A, B, dA, dB: [rows, f] bf16.
+// dB = dH * silu(A).  dO: [rows, h]; A, B, dA, dB: [rows, f] bf16.  With
+// ab_amax [rows, gemm_col_tiles(f)], also the amax of |dA|, |dB| (fp32, before
+// the bf16 store) over each 256-column tile of a row.
 cudaError_t gemm_fc2_dgrad(const GemmProblem& p, const void* dO, const void* W2,
-                           const void* A, const void* B, void* dA, void* dB, cudaStream_t s);
+                           const void* A, const void* B, void* dA, void* dB, cudaStream_t s,
+                           float* ab_amax = nullptr);
 // The same matmul for selective activation rematerialisation, where neither H
 // nor O was kept: the A operand is the ungated dy_perm [rows, h], and with
 // u = dy_perm W2^T, g = gate_rows[row] and H = silu(A) * B rebuilt here:
@@ -52,13 +55,7 @@ int gemm_fc1_col_tiles(int f);
 //   O = sh * s2 * (Hq W2q): Hq [rows, f]; W2q [E, h, f]; s2 [E, h]; sh [rows].
 cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& p, const void* Hq, const float* sh,
                              const void* W2q, const float* s2, void* O, cudaStream_t s);
-// FP8 data gradients:
-//   [dA, dB] from dH = sdo * s2r * (dOq W2r^T) as in gemm_fc2_dgrad, with
-//   ab_amax [rows, gemm_col_tiles(f)] = amax of |dA|, |dB| per 256-column tile;
-//   dOq [rows, h], W2r [E, f, h] e4m3, s2r [E, f], sdo [rows].
-cudaError_t gemm_fc2_dgrad_fp8(const GemmProblem& p, const void* dOq, const float* sdo,
-                               const void* W2r, const float* s2r, const void* A, const void* B,
-                               void* dA, void* dB, float* ab_amax, cudaStream_t s);
+// FP8 FC1 data gradient:
 //   dX = sab * s13r * (dAq W1r^T + dBq W3r^T), fp32 [rows, h]; dAq, dBq
 //   [rows, f], W1r, W3r [E, h, f] e4m3, s13r [E, h], sab [rows].
 cudaError_t gemm_fc1_dgrad_fp8(const GemmProblem& p, const void* dAq, const void* dBq,

@@ -27,7 +27,6 @@ def kernel_work(T: int, h: int, f: int, E: int, k: int) -> dict:
         "gg_fc2_dgrad_swiglu_bwd_sar": 2 * R * h * f,
         "gg_fc1_fwd_swiglu_fp8": 2 * 2 * R * h * f,
         "gg_fc2_fwd_fp8": 2 * R * f * h,
-        "gg_fc2_dgrad_swiglu_bwd_fp8": 2 * R * h * f,
         "gg_fc1_dgrad_fp8": 2 * 2 * R * f * h,
         "gg_fc2_wgrad": 2 * R * f * h,
         "gg_fc1_dgrad": 2 * 2 * R * f * h,
@@ -49,9 +48,7 @@ def kernel_work(T: int, h: int, f: int, E: int, k: int) -> dict:
         "quant_w1": E * h * f * (2 + 1) + E * f * 4,
         "quant_w3": E * h * f * (2 + 1) + E * f * 4,
         "quant_w2": E * h * f * (2 + 1) + E * h * 4,
-        "quant_w2_rows": E * h * f * (2 + 1) + E * f * 4,
         "quant_w13_rows": 2 * E * h * f * (2 + 1) + E * h * 4,
-        "quant_dO": R * h * 3 + R * 4,
         "quant_dAdB": 2 * R * f * 3 + R * 4,
         "transpose_wg": 2 * h * E * 4,
         "token_grad": R * h * 4 + T * h * 2 + E * h * 4 + R * 16 + T * E * 4,
