@@ -113,6 +113,8 @@ struct Params {
   int ldo;           // row stride (elements) of M-grouped outputs and inputs
   int* status;
   int ktiles;        // K-grouped: tiles in total
+  int raster_n;      // tile order: 0 = groups of m-tiles, 1 = groups of n-tiles
+  int group;         // tiles per group along that dimension
 };
 
 struct Maps {
@@ -126,20 +128,31 @@ struct Tile {
   int nkb;      // K blocks
 };
 
-// Tile order inside one expert's MT x NT tile grid: groups of GM m-tiles,
-// and within a group n-major, m fastest.  The ~152 tiles in flight at once then
-// cover about GM m-tiles x (152 / GM) n-tiles, so the A row-blocks and B
-// column-slabs they stream stay shared in L2 instead of the whole A operand
-// being streamed again for every column of tiles.
-constexpr int GM = 16;
-
-__device__ __forceinline__ void raster(int local, int MT, int& mb, int& nb, int NT) {
-  const int g = local / (GM * NT);
-  const int base = g * GM;
-  const int gsz = min(GM, MT - base);
-  const int r = local - g * GM * NT;
-  nb = r / gsz;
-  mb = base + r % gsz;
+// Tile order inside one expert's MT x NT tile grid.  raster_n = 0: groups of
+// `group` m-tiles, and within a group n-major, m fastest; raster_n = 1: the
+// same with the roles of m and n swapped.  The ~152 tiles in flight at once
+// then share the slabs of the grouped operand, which stay in L2 while the
+// group sweeps the other operand once.  The host picks the orientation and the
+// group so that, where one operand of an expert fits in L2, that operand stays
+// resident and the other streams from DRAM exactly once.
+__device__ __forceinline__ void raster(const Params& p, int local, int MT, int NT, int& mb,
+                                       int& nb) {
+  const int G = p.group;
+  if (!p.raster_n) {
+    const int g = local / (G * NT);
+    const int base = g * G;
+    const int gsz = min(G, MT - base);
+    const int r = local - g * G * NT;
+    nb = r / gsz;
+    mb = base + r % gsz;
+  } else {
+    const int g = local / (G * MT);
+    const int base = g * G;
+    const int gsz = min(G, NT - base);
+    const int r = local - g * G * MT;
+    mb = r / gsz;
+    nb = base + r % gsz;
+  }
 }
 
 // Tile t of the launch -> expert, m-tile, n-tile and K range.  TM = rows per
@@ -157,7 +170,7 @@ __device__ __forceinline__ bool decode(const Params& p, const int* off, const in
     const int local = t - NT * cum[e];
     const int mt = cum[e + 1] - cum[e];
     tl.e = e;
-    raster(local, mt, tl.mb, tl.nb, NT);
+    raster(p, local, mt, NT, tl.mb, tl.nb);
     tl.row0 = off[e] + tl.mb * TM;
     tl.row_end = off[e + 1];
     tl.nkb = p.kblocks * p.kconcat;
@@ -167,7 +180,7 @@ __device__ __forceinline__ bool decode(const Params& p, const int* off, const in
     const int per = MT * NT;
     const int e = t / per;
     tl.e = e;
-    raster(t - e * per, MT, tl.mb, tl.nb, NT);
+    raster(p, t - e * per, MT, NT, tl.mb, tl.nb);
     tl.row0 = off[e];
     tl.row_end = off[e + 1];
     tl.nkb = (tl.row_end - tl.row0 + BK - 1) / BK;
@@ -486,25 +499,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tma_load_2d(b_dst, second ? &maps.b1 : &maps.b0, kx,
                           tl.e * p.b_rows + tl.nb * (F8 ? BN : BNB), full);
             } else {
+              // MN-major: one 3-D copy fills the BNB / 64 column chunks of an operand
 #pragma unroll
               for (int i = 0; i < NUM_B; ++i)
-#pragma unroll
-                for (int ch = 0; ch < BNB / 64; ++ch)
-                  tma_load_2d(b_dst + i * (B_BYTES / NUM_B) + ch * CHUNK_BYTES,
-                              i ? &maps.b1 : &maps.b0, tl.nb * BNB + ch * 64,
-                              tl.e * p.b_rows + kx, full);
+                tma_load_3d(b_dst + i * (B_BYTES / NUM_B), i ? &maps.b1 : &maps.b0, 0,
+                            tl.e * p.b_rows + kx, tl.nb * (BNB / 64), full);
             }
           } else {
             const int ky = tl.row0 + kb * BK;
-#pragma unroll
-            for (int ch = 0; ch < BM / 64; ++ch)
-              tma_load_2d(a_dst + ch * CHUNK_BYTES, &maps.a0, tl.mb * BM + ch * 64, ky, full);
+            tma_load_3d(a_dst, &maps.a0, 0, ky, tl.mb * (BM / 64), full);
 #pragma unroll
             for (int i = 0; i < NUM_B; ++i)
-#pragma unroll
-              for (int ch = 0; ch < BNB / 64; ++ch)
-                tma_load_2d(b_dst + i * (B_BYTES / NUM_B) + ch * CHUNK_BYTES,
-                            i ? &maps.b1 : &maps.b0, tl.nb * BNB + ch * 64, ky, full);
+              tma_load_3d(b_dst + i * (B_BYTES / NUM_B), i ? &maps.b1 : &maps.b0, 0, ky,
+                          tl.nb * (BNB / 64), full);
           }
         }
       }
@@ -804,6 +811,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else
               tma_load_2d(dst, m, x, y, bar);
           };
+          // MN-major operands: one 3-D copy of two 64-column chunks
+          auto load_mn = [&](uint32_t dst, const CUtensorMap* m, int y, int chunk) {
+            if (cross)
+              tma_load_3d_pair(dst, m, 0, y, chunk, bar);
+            else
+              tma_load_3d(dst, m, 0, y, chunk, bar);
+          };
           const uint32_t a_dst = smem_u32(smem + s * STAGE2_BYTES);
           const uint32_t b_dst = a_dst + A2_BYTES;
           // B columns of this CTA: the second operand for NUM_B = 2 (W3 / dB),
@@ -818,18 +832,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               load(b_dst, second ? &maps.b1 : &maps.b0, kx,
                    tl.e * p.b_rows + tl.nb * BN + 128 * static_cast<int>(rank));
             } else {
-#pragma unroll
-              for (int ch = 0; ch < 2; ++ch)
-                load(b_dst + ch * CHUNK_BYTES, bmap, bcol + ch * 64, tl.e * p.b_rows + kx);
+              load_mn(b_dst, bmap, tl.e * p.b_rows + kx, bcol / 64);
             }
           } else {
             const int ky = tl.row0 + kb * BK;
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch)
-              load(a_dst + ch * CHUNK_BYTES, &maps.a0,
-                   tl.mb * PM + 128 * static_cast<int>(rank) + ch * 64, ky);
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) load(b_dst + ch * CHUNK_BYTES, bmap, bcol + ch * 64, ky);
+            load_mn(a_dst, &maps.a0, ky, (tl.mb * PM + 128 * static_cast<int>(rank)) / 64);
+            load_mn(b_dst, bmap, ky, bcol / 64);
           }
         }
       }
@@ -1035,6 +1043,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MN-major operand: bf16 matrix [outer, inner] (row-major, inner a multiple of
+// 64) viewed as {64, outer, inner / 64}, so that one box of {64, box_outer,
+// chunks} copies `chunks` 64-column chunks of box_outer rows, 128B swizzle.
+bool make_map_mn(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                 uint32_t box_outer, uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || inner % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, outer, inner / 64};
+  cuuint64_t strides[2] = {inner * 2, 128};
+  cuuint32_t box[3] = {64, box_outer, chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Which kernel runs each matmul.  Measured on GB300 (Mixtral-8x7B-shaped
 // layer): the CTA pair is faster for the two dgrads (K-major operands, 5-6%),
 // the one-CTA kernel for the forward and wgrad matmuls (MN-major operands).
@@ -1117,10 +1141,53 @@ Params base_params(const GemmProblem& g) {
   p.rows = g.rows;
   p.status = g.status;
   p.kconcat = 1;
+  p.raster_n = 0;
+  p.group = 16;
   return p;
 }
 
 int tile_rows(int epi) { return pair_for(epi) ? PM : BM; }
+
+// Tile order of one launch (see raster).  Per expert, operand A (the tiled-M
+// side) holds a_bytes and operand B (the tiled-N side) b_bytes; one m-tile
+// reads slab_a bytes of A over the whole K loop, one n-tile slab_b of B.  When
+// the smaller operand fits the L2 budget, its tiles form one group, so it is
+// read from DRAM once and the larger one streams past it once.  Otherwise both
+// stream, in groups of 16 m-tiles.
+// MOE_GEMM_RASTER=m<G> or n<G> forces one order and group size on every
+// matmul (for tests and measurement).
+constexpr long long kL2ResidentBytes = 48ll << 20;
+void set_raster(Params& p, long long a_bytes, long long b_bytes, long long slab_a,
+                long long slab_b) {
+  static const int forced = [] {
+    const char* e = getenv("MOE_GEMM_RASTER");
+    if (!e || (e[0] != 'm' && e[0] != 'n')) return 0;
+    const int g = atoi(e + 1);
+    return (g >= 1 && g <= 4096) ? (e[0] == 'n' ? -g : g) : 0;
+  }();
+  if (forced) {
+    p.raster_n = forced < 0;
+    p.group = forced < 0 ? -forced : forced;
+    return;
+  }
+  auto group_of = [](long long slab) {
+    const long long g = slab > 0 ? kL2ResidentBytes / slab : 1;
+    return static_cast<int>(g < 1 ? 1 : (g > 4096 ? 4096 : g));
+  };
+  if (a_bytes <= kL2ResidentBytes && a_bytes <= b_bytes) {
+    p.raster_n = 0;
+    p.group = group_of(slab_a);
+  } else if (b_bytes <= kL2ResidentBytes) {
+    p.raster_n = 1;
+    p.group = group_of(slab_b);
+  } else {
+    p.raster_n = 0;
+    p.group = 16;
+  }
+}
+
+// Average rows per expert (the K extent of a wgrad, the M extent of the rest).
+long long rows_per_expert(const GemmProblem& g) { return (g.rows + g.E - 1) / g.E; }
 
 // Upper bound of an M-grouped tile count without reading the offsets.
 long long mgrouped_tiles(const GemmProblem& g, int epi, int N, int bnb) {
@@ -1138,6 +1205,11 @@ long long kgrouped_tiles(const GemmProblem& g, int epi, int M, int N, int bnb) {
 // half of it (pair).
 uint32_t kmajor_b_rows(int epi) { return pair_for(epi) ? 128 : BN; }
 
+// 64-column chunks per MN-major B copy: an operand's columns of one tile (one
+// CTA), or this CTA's 128 of them (pair).  An MN-major A copy is this CTA's
+// 128 rows of the tile in both kernels: BM / 64 chunks.
+uint32_t mn_chunks(int epi, int num_b) { return pair_for(epi) ? 2 : BN / num_b / 64; }
+
 }  // namespace
 
 cudaError_t gemm_fc1_fwd(const GemmProblem& g, const void* x_perm, const void* W1,
@@ -1145,8 +1217,8 @@ cudaError_t gemm_fc1_fwd(const GemmProblem& g, const void* x_perm, const void* W
   Maps m;
   memset(&m, 0, sizeof(m));
   if (!make_map(&m.a0, x_perm, g.h, g.rows, BK, BM) ||
-      !make_map(&m.b0, W1, g.f, static_cast<uint64_t>(g.E) * g.h, 64, BK) ||
-      !make_map(&m.b1, W3, g.f, static_cast<uint64_t>(g.E) * g.h, 64, BK))
+      !make_map_mn(&m.b0, W1, g.f, static_cast<uint64_t>(g.E) * g.h, BK, mn_chunks(EPI_SWIGLU, 2)) ||
+      !make_map_mn(&m.b1, W3, g.f, static_cast<uint64_t>(g.E) * g.h, BK, mn_chunks(EPI_SWIGLU, 2)))
     return cudaErrorInvalidValue;
   m.a1 = m.a0;
   Params p = base_params(g);
@@ -1157,6 +1229,8 @@ cudaError_t gemm_fc1_fwd(const GemmProblem& g, const void* x_perm, const void* W
   p.out1 = B;
   p.out2 = H;
   p.ldo = g.f;
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.h * 2, 2ll * g.h * 2 * g.f, 1ll * tile_rows(EPI_SWIGLU) * g.h * 2, 1ll * BN * g.h * 2);
   return launch<false, true, 2, EPI_SWIGLU, false>(p, m, mgrouped_tiles(g, EPI_SWIGLU, g.f, BN / 2),
                                                     g.num_sms, s);
 }
@@ -1166,7 +1240,7 @@ cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, vo
   Maps m;
   memset(&m, 0, sizeof(m));
   if (!make_map(&m.a0, H, g.f, g.rows, BK, BM) ||
-      !make_map(&m.b0, W2, g.h, static_cast<uint64_t>(g.E) * g.f, 64, BK))
+      !make_map_mn(&m.b0, W2, g.h, static_cast<uint64_t>(g.E) * g.f, BK, mn_chunks(EPI_BF16, 1)))
     return cudaErrorInvalidValue;
   m.a1 = m.a0;
   m.b1 = m.b0;
@@ -1176,6 +1250,8 @@ cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, vo
   p.b_rows = g.f;
   p.out0 = O;
   p.ldo = g.h;
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.f * 2, 2ll * g.f * g.h, 1ll * tile_rows(EPI_BF16) * g.f * 2, 1ll * BN * g.f * 2);
   return launch<false, true, 1, EPI_BF16, false>(p, m, mgrouped_tiles(g, EPI_BF16, g.h, BN),
                                                 g.num_sms, s);
 }
@@ -1201,6 +1277,8 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.ldo = g.f;
   p.part = ab_amax;
   p.part_ld = gemm_col_tiles(g.f);
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.h * 2, 2ll * g.h * g.f, 1ll * tile_rows(EPI_SWIGLU_BWD) * g.h * 2, 1ll * BN * g.h * 2);
   return launch<false, false, 1, EPI_SWIGLU_BWD, false>(p, m, mgrouped_tiles(g, EPI_SWIGLU_BWD, g.f, BN),
                                                          g.num_sms, s);
 }
@@ -1229,6 +1307,8 @@ cudaError_t gemm_fc1_dgrad_fp8(const GemmProblem& g, const void* dAq, const void
   p.col_scale0 = s13r;
   p.out0 = dX;
   p.ldo = g.h;
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * 2 * g.f, 2ll * g.f * g.h, 1ll * BM * 2 * g.f, 1ll * BN * 2 * g.f);
   return launch<false, false, 1, EPI_F32_F8, false>(p, m, mgrouped_tiles(g, EPI_F32_F8, g.h, BN),
                                                     g.num_sms, s);
 }
@@ -1259,6 +1339,8 @@ cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& g, const void* Xq, const float* 
   p.out1 = B;
   p.out2 = H;
   p.ldo = g.f;
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.h, 2ll * g.h * g.f, 1ll * BM * g.h, 1ll * BN * g.h);
   return launch<false, false, 2, EPI_SWIGLU_F8, false>(
       p, m, mgrouped_tiles(g, EPI_SWIGLU_F8, g.f, BN / 2), g.num_sms, s);
 }
@@ -1281,6 +1363,8 @@ cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& g, const void* Hq, const float* 
   p.col_scale0 = s2;
   p.out0 = O;
   p.ldo = g.h;
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.f, 1ll * g.f * g.h, 1ll * BM * g.f, 1ll * BN * g.f);
   return launch<false, false, 1, EPI_BF16_F8, false>(p, m, mgrouped_tiles(g, EPI_BF16_F8, g.h, BN),
                                                      g.num_sms, s);
 }
@@ -1309,6 +1393,8 @@ cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& g, const void* dy_perm, const 
   p.out1 = dB;
   p.out2 = gH;
   p.ldo = g.f;
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.h * 2, 2ll * g.h * g.f, 1ll * tile_rows(EPI_SWIGLU_BWD_SAR) * g.h * 2, 1ll * BN * g.h * 2);
   return launch<false, false, 1, EPI_SWIGLU_BWD_SAR, false>(
       p, m, mgrouped_tiles(g, EPI_SWIGLU_BWD_SAR, g.f, BN), g.num_sms, s);
 }
@@ -1329,6 +1415,8 @@ cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB,
   p.b_rows = g.h;
   p.out0 = dX;
   p.ldo = g.h;
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * 2 * g.f * 2, 4ll * g.f * g.h, 1ll * tile_rows(EPI_F32) * 2 * g.f * 2, 1ll * BN * 2 * g.f * 2);
   return launch<false, false, 1, EPI_F32, false>(p, m, mgrouped_tiles(g, EPI_F32, g.h, BN),
                                                  g.num_sms, s);
 }
@@ -1337,7 +1425,8 @@ cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, 
                            cudaStream_t s) {
   Maps m;
   memset(&m, 0, sizeof(m));
-  if (!make_map(&m.a0, H, g.f, g.rows, 64, BK) || !make_map(&m.b0, dO, g.h, g.rows, 64, BK))
+  if (!make_map_mn(&m.a0, H, g.f, g.rows, BK, BM / 64) ||
+      !make_map_mn(&m.b0, dO, g.h, g.rows, BK, mn_chunks(EPI_WGRAD, 1)))
     return cudaErrorInvalidValue;
   m.a1 = m.a0;
   m.b1 = m.b0;
@@ -1346,6 +1435,8 @@ cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, 
   p.N = g.h;
   p.out0 = dW2;
   p.ktiles = static_cast<int>(kgrouped_tiles(g, EPI_WGRAD, g.f, g.h, BN));
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.f * 2, R * g.h * 2, tile_rows(EPI_WGRAD) * R * 2, BN * R * 2);
   return launch<true, true, 1, EPI_WGRAD, true>(p, m, p.ktiles, g.num_sms, s);
 }
 
@@ -1353,8 +1444,9 @@ cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void*
                            const void* dB, float* dW1, float* dW3, cudaStream_t s) {
   Maps m;
   memset(&m, 0, sizeof(m));
-  if (!make_map(&m.a0, x_perm, g.h, g.rows, 64, BK) || !make_map(&m.b0, dA, g.f, g.rows, 64, BK) ||
-      !make_map(&m.b1, dB, g.f, g.rows, 64, BK))
+  if (!make_map_mn(&m.a0, x_perm, g.h, g.rows, BK, BM / 64) ||
+      !make_map_mn(&m.b0, dA, g.f, g.rows, BK, mn_chunks(EPI_WGRAD, 2)) ||
+      !make_map_mn(&m.b1, dB, g.f, g.rows, BK, mn_chunks(EPI_WGRAD, 2)))
     return cudaErrorInvalidValue;
   m.a1 = m.a0;
   Params p = base_params(g);
@@ -1363,6 +1455,8 @@ cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void*
   p.out0 = dW1;
   p.out1 = dW3;
   p.ktiles = static_cast<int>(kgrouped_tiles(g, EPI_WGRAD, g.h, g.f, BN / 2));
+  const long long R = rows_per_expert(g);
+  set_raster(p, R * g.h * 2, R * 2 * g.f * 2, tile_rows(EPI_WGRAD) * R * 2, BN * R * 2);
   return launch<true, true, 2, EPI_WGRAD, true>(p, m, p.ktiles, g.num_sms, s);
 }
 
