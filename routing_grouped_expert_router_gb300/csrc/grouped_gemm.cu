@@ -64,7 +64,12 @@ struct alignas(8) Ctrl {
   int off[MAX_E + 1];   // expert offsets
   int cum[MAX_E + 1];   // M-grouped: prefix of m-tiles per expert
 };
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + static_cast<int>(sizeof(Ctrl));
+// Each epilogue warp owns two 4 KiB staging blocks between the stage ring and
+// the control words: 32 x 32 fp32 tiles on their way to global memory (see
+// store_f32_block).
+constexpr int EPI_STAGE_BYTES = 32 * 32 * 4;
+constexpr int EPI_SMEM_BYTES = 4 * 2 * EPI_STAGE_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_SMEM_BYTES + static_cast<int>(sizeof(Ctrl));
 
 enum Epi {
   EPI_SWIGLU = 0,
@@ -119,6 +124,9 @@ struct Params {
 
 struct Maps {
   CUtensorMap a0, a1, b0, b1;
+  // Outputs written by TMA from the epilogue's staging blocks (32 x 32 boxes):
+  // fp32 (EPI_WGRAD, EPI_F32; 128B swizzle) or bf16 (the rest; 64B swizzle).
+  CUtensorMap o0, o1, o2;
 };
 
 struct Tile {
@@ -203,36 +211,121 @@ __device__ __forceinline__ void store_bf16x32(void* dst, const float* v) {
                       pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
 }
 
-__device__ __forceinline__ void load_bf16x32(const void* src, float* v) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 q = __ldg(s + i);
-    uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-  }
-}
-
 __device__ __forceinline__ void store_f32x32(void* dst, const float* v) {
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
   for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-// One 32-column chunk of the epilogue for one accumulator row.
-//   grow: M-grouped output row (permuted row);  orow: K-grouped output row.
-//   v0 (and v1 for two B operands): the fp32 accumulator values.
+// A warp's 32 consecutive rows x 32 fp32 columns (lane i holds row i in v) to
+// global memory.  Written straight from the registers, every store
+// instruction would touch 32 rows with 16 bytes each; instead the block goes
+// to shared memory in the 128-byte-swizzled layout (16-byte piece j of row i
+// in slot j ^ (i & 7), which also keeps the writes free of bank conflicts),
+// and one TMA copy (map, box origin x, y) writes it out as whole rows while
+// the warp goes on.  Two staging blocks alternate: before one is refilled,
+// the copy that last read it must be done reading.  A block with rows that
+// must stay untouched (bit clear in `ok`: past the expert's rows) is written
+// by the warp itself instead, row i at dst0 + i * ld, four whole rows per
+// instruction.
+__device__ __forceinline__ void store_f32_block(float4* stage, int& nblk, const float* v,
+                                                const CUtensorMap* map, int x, int y, float* dst0,
+                                                size_t ld, unsigned ok, int lane) {
+  float4* buf = stage + (nblk & 1) * (EPI_STAGE_BYTES / 16);
+  ++nblk;
+  if (lane == 0) bulk_wait_read_1();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    buf[lane * 8 + (j ^ (lane & 7))] =
+        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  if (ok == 0xffffffffu) {
+    fence_proxy_async_smem();  // the generic-proxy writes, seen by the copy
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, smem_u32(buf), x, y);
+      bulk_commit();
+    }
+    return;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const int c = lane & 7;
+    const float4 q = buf[r * 8 + (c ^ (r & 7))];
+    if ((ok >> r) & 1u) reinterpret_cast<float4*>(dst0 + static_cast<size_t>(r) * ld)[c] = q;
+  }
+  __syncwarp();
+}
+
+// Lane i's 32 values as bf16 into row i of a 32 x 32 block (2 KiB) in the
+// layout of a TMA box {32, 32} with 64-byte swizzle: 16-byte piece j of row i
+// in slot j ^ ((i >> 1) & 3), which also keeps the writes free of bank
+// conflicts.
+__device__ __forceinline__ void stage_bf16(uint4* buf, const float* v, int lane) {
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    buf[lane * 4 + (j ^ sw)] =
+        make_uint4(pack_bf16(v[8 * j + 0], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                   pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+}
+
+// NOUT bf16 outputs (x0 -> out0 / o0, x1 -> out1 / o1, x2 -> out2 / o2) of one
+// 32-column chunk of a warp's 32 rows, lane i holding row grow0 + i.  With all
+// 32 rows in range the blocks go through the warp's staging area and one TMA
+// copy per output writes each (a store instruction from the registers would
+// touch 32 rows with 16 bytes each); the warp does not wait for the copies,
+// only, before it refills a staging set, for the copies that last read it.
+// Otherwise (rows past the expert's end, which belong to the next expert)
+// each lane in range stores its own row.
+template <int NOUT>
+__device__ __forceinline__ void store_bf16_chunk(const Params& p, const Maps& maps, uint4* stage,
+                                                 int& nblk, int grow0, int col, bool row_ok,
+                                                 const float* x0, const float* x1,
+                                                 const float* x2, int lane) {
+  const unsigned ok = __ballot_sync(0xffffffffu, row_ok);
+  if (ok == 0xffffffffu) {
+    constexpr int NSETS = NOUT <= 2 ? 2 : 1;  // staging sets in the warp's 8 KiB
+    uint4* buf = stage + (nblk % NSETS) * (NOUT * 128);
+    ++nblk;
+    if (lane == 0) {
+      if (NSETS == 2)
+        bulk_wait_read_1();
+      else
+        bulk_wait_read_0();
+    }
+    __syncwarp();
+    stage_bf16(buf, x0, lane);
+    if (NOUT > 1) stage_bf16(buf + 128, x1, lane);
+    if (NOUT > 2) stage_bf16(buf + 256, x2, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&maps.o0, smem_u32(buf), col, grow0);
+      if (NOUT > 1) tma_store_2d(&maps.o1, smem_u32(buf + 128), col, grow0);
+      if (NOUT > 2) tma_store_2d(&maps.o2, smem_u32(buf + 256), col, grow0);
+      bulk_commit();
+    }
+  } else if (row_ok) {
+    const size_t o = static_cast<size_t>(grow0 + lane) * p.ldo + col;
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, x0);
+    if (NOUT > 1) store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, x1);
+    if (NOUT > 2) store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, x2);
+  }
+}
+
+// The bf16-output forward epilogues (EPI_SWIGLU, EPI_BF16 and their FP8
+// forms) on one 32-column chunk of a warp's 32 rows; v0 (and v1 for two B
+// operands) are lane i's fp32 accumulator values for row grow0 + i.
 template <int NUM_B, int EPI_>
-__device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, int grow, int orow,
-                                               int col, const float* v0, const float* v1,
-                                               float& acc) {
+__device__ __forceinline__ void bf16_chunk(const Params& p, const Maps& maps, uint4* stage,
+                                           int& nblk, int grow0, int col, bool row_ok,
+                                           const float* v0, const float* v1, float& acc,
+                                           int lane) {
   constexpr int EPI = base_epi(EPI_);
-  if (EPI == EPI_SWIGLU) {
-    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+  if constexpr (EPI == EPI_SWIGLU) {
     float hv[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) hv[i] = silu_f(v0[i]) * v1[i];
@@ -240,61 +333,10 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const Tile& tl, 
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc = fmaxf(acc, fabsf(hv[i]));
     }
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, v1);
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, hv);
-  } else if (EPI == EPI_BF16) {
-    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, v0);
-  } else if (EPI == EPI_SWIGLU_BWD) {
-    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-    float av[32], bv[32];
-    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in0) + o, av);
-    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in1) + o, bv);
-    float da[32], db[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float a = av[i];
-      const float sg = 1.0f / (1.0f + expf(-a));
-      const float dh = v0[i];
-      da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
-      db[i] = dh * a * sg;
-    }
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
-  } else if (EPI == EPI_SWIGLU_BWD_SAR) {
-    // The accumulator holds u = dy_perm W2^T without the gate.  With the row's
-    // gate g and H = silu(A) * B rebuilt from the kept A, B:
-    //   dH = g u;  dA, dB as in EPI_SWIGLU_BWD;  gH = g H (FC2 wgrad's operand,
-    //   since dW2 = H^T (g dy) = (g H)^T dy);  dg += <H, u> (= <dy, O>).
-    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-    float av[32], bv[32];
-    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in0) + o, av);
-    load_bf16x32(static_cast<const __nv_bfloat16*>(p.in1) + o, bv);
-    const float g = __ldg(p.in2 + grow);
-    float da[32], db[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float a = av[i];
-      const float sg = 1.0f / (1.0f + expf(-a));
-      const float sl = a * sg;
-      const float hh = sl * bv[i];
-      const float dh = g * v0[i];
-      acc = fmaf(hh, v0[i], acc);
-      da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
-      db[i] = dh * sl;
-      av[i] = g * hh;  // gH
-    }
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, av);
-  } else if (EPI == EPI_F32) {
-    const size_t o = static_cast<size_t>(grow) * p.ldo + col;
-    store_f32x32(static_cast<float*>(p.out0) + o, v0);
-  } else {  // EPI_WGRAD
-    const size_t o = (static_cast<size_t>(tl.e) * p.M + orow) * p.N + col;
-    store_f32x32(static_cast<float*>(p.out0) + o, v0);
-    if (NUM_B == 2) store_f32x32(static_cast<float*>(p.out1) + o, v1);
+    store_bf16_chunk<3>(p, maps, stage, nblk, grow0, col, row_ok, v0, v1, hv, lane);
+  } else {
+    static_assert(EPI == EPI_BF16, "bf16_chunk serves the forward epilogues only");
+    store_bf16_chunk<1>(p, maps, stage, nblk, grow0, col, row_ok, v0, v0, v0, lane);
   }
 }
 
@@ -311,14 +353,19 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&q)[4], float* v) {
   }
 }
 
-// The SwiGLU-backward epilogues on a 32-column chunk whose A and B values
-// were loaded ahead (raw bf16).  EPI_SWIGLU_BWD: v0 = dH.  EPI_SWIGLU_BWD_SAR:
-// v0 = dy W2^T without the gate (see epilogue_chunk).
+// The SwiGLU-backward epilogues on a 32-column chunk of a warp's 32 rows (lane
+// i: row grow0 + i) whose A and B values were loaded ahead (raw bf16).
+//   EPI_SWIGLU_BWD: v0 = dH;  dA = dH * B * s (1 + A (1 - s)), dB = dH * silu(A)
+//   with s = sigmoid(A); with p.part, acc = the amax of the row's dA and dB.
+//   EPI_SWIGLU_BWD_SAR: v0 = u = dy_perm W2^T without the gate.  With the
+//   row's gate g and H = silu(A) * B rebuilt from the kept A, B: dH = g u;
+//   dA, dB as above; gH = g H (FC2 wgrad's operand, since dW2 = H^T (g dy) =
+//   (g H)^T dy); acc += <H, u> (= <dy, O>).
 template <int EPI>
-__device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, int grow, int col,
+__device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, const Maps& maps, uint4* stage,
+                                                 int& nblk, int grow0, int col, bool row_ok,
                                                  const float* v0, const uint4 (&ra)[4],
-                                                 const uint4 (&rb)[4], float& acc) {
-  const size_t o = static_cast<size_t>(grow) * p.ldo + col;
+                                                 const uint4 (&rb)[4], float& acc, int lane) {
   float av[32], bv[32];
   unpack_bf16x32(ra, av);
   unpack_bf16x32(rb, bv);
@@ -332,12 +379,13 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, int grow, int 
       da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
       db[i] = dh * a * sg;
     }
-    if (p.part) {  // amax of the row's dA and dB, for their shared e4m3 scale downstream
+    if (p.part) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc = fmaxf(acc, fmaxf(fabsf(da[i]), fabsf(db[i])));
     }
+    store_bf16_chunk<2>(p, maps, stage, nblk, grow0, col, row_ok, da, db, db, lane);
   } else {
-    const float g = __ldg(p.in2 + grow);
+    const float g = row_ok ? __ldg(p.in2 + grow0 + lane) : 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float a = av[i];
@@ -350,10 +398,8 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, int grow, int 
       db[i] = dh * sl;
       av[i] = g * hh;  // gH
     }
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out2) + o, av);
+    store_bf16_chunk<3>(p, maps, stage, nblk, grow0, col, row_ok, da, db, av, lane);
   }
-  store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
-  store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
 }
 
 // The next chunk's A and B pieces (nothing for rows or columns out of range).
@@ -415,13 +461,38 @@ __device__ __forceinline__ void zero_a_tail(uint8_t* a_tile, int kv, int lane) {
   __syncwarp();
 }
 
+// The fp32 epilogues (EPI_WGRAD, EPI_F32) on one 32-column chunk of a warp's
+// 32 rows.  grow0 / orow0: the M-grouped / K-grouped output row of lane 0.
+// The output maps view dW as [E * M, N] and dX as [rows, ldo].
+template <int NUM_B, int EPI>
+__device__ __forceinline__ void fp32_rows_chunk(const Params& p, const Maps& maps, const Tile& tl,
+                                                float4* stage, int& nblk, int grow0, int orow0,
+                                                int col, bool row_ok, const float* v0,
+                                                const float* v1, int lane) {
+  const unsigned ok = __ballot_sync(0xffffffffu, row_ok);
+  if (ok == 0u) return;
+  if (EPI == EPI_WGRAD) {
+    const int y = tl.e * p.M + orow0;
+    const size_t o = static_cast<size_t>(y) * p.N + col;
+    store_f32_block(stage, nblk, v0, &maps.o0, col, y, static_cast<float*>(p.out0) + o, p.N, ok,
+                    lane);
+    if (NUM_B == 2)
+      store_f32_block(stage, nblk, v1, &maps.o1, col, y, static_cast<float*>(p.out1) + o, p.N,
+                      ok, lane);
+  } else {
+    const size_t o = static_cast<size_t>(grow0) * p.ldo + col;
+    store_f32_block(stage, nblk, v0, &maps.o0, col, grow0, static_cast<float*>(p.out0) + o,
+                    p.ldo, ok, lane);
+  }
+}
+
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gg_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES + EPI_SMEM_BYTES);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr int BNB = BN / NUM_B;  // accumulator columns per B operand
@@ -602,10 +673,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;
+    float4* stage =
+        reinterpret_cast<float4*>(smem + STAGES * STAGE_BYTES + (warp - 2) * 2 * EPI_STAGE_BYTES);
+    int nblk = 0;  // fp32 blocks this warp has staged
     int it = 0;
     Tile tl;
     for (int t = blockIdx.x; decode<BM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += gridDim.x) {
-      if (*abort_flag) break;
+      // every decision to stop is taken by the whole warp: the TMEM loads and
+      // the staged stores below are warp-collective
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       if (GROUP_K && tl.nkb == 0) {  // expert without tokens: zero weight gradient
         zero_wgrad_row<NUM_B>(p, tl, tl.mb * BM + r);
         continue;
@@ -613,7 +689,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int buf = it & 1;
       const uint32_t u = (it >> 1) & 1;
       ++it;
-      if (!mbar_wait(smem_u32(&c.tfull[buf]), u, p.status, kTimeoutCode)) {
+      const bool filled = mbar_wait(smem_u32(&c.tfull[buf]), u, p.status, kTimeoutCode);
+      if (!__all_sync(0xffffffffu, filled)) {
         *abort_flag = 1;
         break;
       }
@@ -640,8 +717,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             load_ab_chunk(p, row_ok && col + 32 < p.N, o0 + (ch + 1) * 32, ra, rb);
           float v0[32];
           tmem_ld32(tbase + ch * 32, v0);
-          if (!row_ok || col >= p.N) continue;
-          swiglu_bwd_chunk<EPI>(p, grow, col, v0, ca, cb, acc);
+          if (col >= p.N) continue;  // the same for the whole warp
+          swiglu_bwd_chunk<EPI>(p, maps, reinterpret_cast<uint4*>(stage), nblk, grow - lane, col,
+                                row_ok, v0, ca, cb, acc, lane);
         }
       } else {
 #pragma unroll 1
@@ -651,9 +729,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tbase + ch * 32, v0);
           if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
           const int col = tl.nb * BNB + ch * 32;
-          if (!row_ok || col >= p.N) continue;
-          if (is_f8(EPI)) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
-          epilogue_chunk<NUM_B, EPI>(p, tl, grow, tl.mb * BM + r, col, v0, v1, acc);
+          if constexpr (EPI == EPI_WGRAD || base_epi(EPI) == EPI_F32) {
+            if (col >= p.N) continue;  // the same for the whole warp
+            if (is_f8(EPI) && row_ok) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
+            fp32_rows_chunk<NUM_B, EPI>(p, maps, tl, stage, nblk, grow - lane,
+                                        tl.mb * BM + quarter * 32, col, row_ok, v0, v1, lane);
+          } else {
+            if (col >= p.N) continue;  // the same for the whole warp
+            if (is_f8(EPI) && row_ok) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
+            bf16_chunk<NUM_B, EPI>(p, maps, reinterpret_cast<uint4*>(stage), nblk, grow - lane,
+                                   col, row_ok, v0, v1, acc, lane);
+          }
         }
       }
       if ((EPI == EPI_SWIGLU_BWD_SAR || EPI == EPI_SWIGLU_F8 ||
@@ -662,6 +748,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&c.tempty[buf]));
     }
+    if (lane == 0) bulk_wait_all();  // staged fp32 blocks written out before the CTA ends
   }
 
   // ------------------------------------------------------------ teardown
@@ -707,7 +794,8 @@ struct alignas(8) Ctrl2 {
   int off[MAX_E + 1];
   int cum[MAX_E + 1];
 };
-constexpr int SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + static_cast<int>(sizeof(Ctrl2));
+constexpr int SMEM2_BYTES =
+    1024 + STAGES2 * STAGE2_BYTES + EPI_SMEM_BYTES + static_cast<int>(sizeof(Ctrl2));
 static_assert(SMEM2_BYTES <= 232448, "pair kernel exceeds the 227 KiB shared-memory limit");
 static_assert(SMEM_BYTES <= 232448, "one-CTA kernel exceeds the 227 KiB shared-memory limit");
 
@@ -717,7 +805,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Ctrl2& c = *reinterpret_cast<Ctrl2*>(smem + STAGES2 * STAGE2_BYTES);
+  Ctrl2& c = *reinterpret_cast<Ctrl2*>(smem + STAGES2 * STAGE2_BYTES + EPI_SMEM_BYTES);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();     // 0: issues the MMAs of the pair
@@ -938,10 +1026,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;             // TMEM lane = row within this CTA's half
     const int half = 128 * static_cast<int>(rank);
+    float4* stage = reinterpret_cast<float4*>(smem + STAGES2 * STAGE2_BYTES +
+                                              (warp - 2) * 2 * EPI_STAGE_BYTES);
+    int nblk = 0;
     int it = 0;
     Tile tl;
     for (int t = cid; decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
-      if (*abort_flag) break;
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-wide, as above
       const int orow = tl.mb * PM + half + r;       // K-grouped output row
       if (GROUP_K && tl.nkb == 0) {
         zero_wgrad_row<NUM_B>(p, tl, orow);
@@ -950,7 +1041,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int buf = it & 1;
       const uint32_t u = (it >> 1) & 1;
       ++it;
-      if (!mbar_wait(smem_u32(&c.tfull[buf]), u, p.status, kTimeoutCode)) {
+      const bool filled = mbar_wait(smem_u32(&c.tfull[buf]), u, p.status, kTimeoutCode);
+      if (!__all_sync(0xffffffffu, filled)) {
         give_up();
         break;
       }
@@ -977,8 +1069,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             load_ab_chunk(p, row_ok && col + 32 < p.N, o0 + (ch + 1) * 32, ra, rb);
           float v0[32];
           tmem_ld32(tbase + ch * 32, v0);
-          if (!row_ok || col >= p.N) continue;
-          swiglu_bwd_chunk<EPI>(p, grow, col, v0, ca, cb, acc);
+          if (col >= p.N) continue;  // the same for the whole warp
+          swiglu_bwd_chunk<EPI>(p, maps, reinterpret_cast<uint4*>(stage), nblk, grow - lane, col,
+                                row_ok, v0, ca, cb, acc, lane);
         }
       } else {
 #pragma unroll 1
@@ -988,8 +1081,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(tbase + ch * 32, v0);
           if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
           const int col = tl.nb * BNB + ch * 32;
-          if (!row_ok || col >= p.N) continue;
-          epilogue_chunk<NUM_B, EPI>(p, tl, grow, orow, col, v0, v1, acc);
+          if constexpr (EPI == EPI_WGRAD || EPI == EPI_F32) {
+            if (col >= p.N) continue;  // the same for the whole warp
+            fp32_rows_chunk<NUM_B, EPI>(p, maps, tl, stage, nblk, grow - lane, orow - lane, col,
+                                        row_ok, v0, v1, lane);
+          } else {
+            if (col >= p.N) continue;  // the same for the whole warp
+            bf16_chunk<NUM_B, EPI>(p, maps, reinterpret_cast<uint4*>(stage), nblk, grow - lane,
+                                   col, row_ok, v0, v1, acc, lane);
+          }
         }
       }
       if ((EPI == EPI_SWIGLU_BWD_SAR || (EPI == EPI_SWIGLU_BWD && p.part)) && row_ok)
@@ -998,6 +1098,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&c.tempty[buf]), 0));
     }
+    if (lane == 0) bulk_wait_all();  // staged fp32 blocks written out before the CTA ends
   }
 
   // ------------------------------------------------------------ teardown
@@ -1059,10 +1160,39 @@ bool make_map_mn(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 output [outer, inner] (row-major) for the epilogue's TMA stores: 32 x 32
+// boxes, 128B swizzle (one 128-byte row of 32 floats per box row).
+bool make_map_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 output [outer, inner] (row-major) for the epilogue's TMA stores: 32 x 32
+// boxes, 64B swizzle (one 64-byte row of 32 values per box row).
+bool make_map_out_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Which kernel runs each matmul.  Measured on GB300 (Mixtral-8x7B-shaped
-// layer): the CTA pair is faster for the two dgrads (K-major operands, 5-6%),
-// the one-CTA kernel for the forward and wgrad matmuls (MN-major operands).
-// MOE_GEMM_CTAS=1 or =2 forces one kind for every matmul (for measurement).
+// layer): the CTA pair is as fast or faster for every matmul but FC1 forward
+// (wgrads 2-3%, FC2 forward 1%), whose three-output epilogue runs 2% faster on
+// the one-CTA kernel.  MOE_GEMM_CTAS=1 or =2 forces one kind for every matmul
+// (for measurement).
 int forced_ctas() {
   static const int v = [] {
     const char* e = getenv("MOE_GEMM_CTAS");
@@ -1073,7 +1203,7 @@ int forced_ctas() {
 bool pair_for(int epi) {
   if (is_f8(epi)) return false;  // the FP8 matmuls run on the one-CTA kernel only
   if (forced_ctas()) return forced_ctas() == 2;
-  return epi == EPI_SWIGLU_BWD || epi == EPI_SWIGLU_BWD_SAR || epi == EPI_F32;
+  return epi != EPI_SWIGLU;
 }
 
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
@@ -1229,6 +1359,9 @@ cudaError_t gemm_fc1_fwd(const GemmProblem& g, const void* x_perm, const void* W
   p.out1 = B;
   p.out2 = H;
   p.ldo = g.f;
+  if (!make_map_out_bf16(&m.o0, A, g.f, g.rows) || !make_map_out_bf16(&m.o1, B, g.f, g.rows) ||
+      !make_map_out_bf16(&m.o2, H, g.f, g.rows))
+    return cudaErrorInvalidValue;
   const long long R = rows_per_expert(g);
   set_raster(p, R * g.h * 2, 2ll * g.h * 2 * g.f, 1ll * tile_rows(EPI_SWIGLU) * g.h * 2, 1ll * BN * g.h * 2);
   return launch<false, true, 2, EPI_SWIGLU, false>(p, m, mgrouped_tiles(g, EPI_SWIGLU, g.f, BN / 2),
@@ -1250,6 +1383,7 @@ cudaError_t gemm_fc2_fwd(const GemmProblem& g, const void* H, const void* W2, vo
   p.b_rows = g.f;
   p.out0 = O;
   p.ldo = g.h;
+  if (!make_map_out_bf16(&m.o0, O, g.h, g.rows)) return cudaErrorInvalidValue;
   const long long R = rows_per_expert(g);
   set_raster(p, R * g.f * 2, 2ll * g.f * g.h, 1ll * tile_rows(EPI_BF16) * g.f * 2, 1ll * BN * g.f * 2);
   return launch<false, true, 1, EPI_BF16, false>(p, m, mgrouped_tiles(g, EPI_BF16, g.h, BN),
@@ -1275,6 +1409,8 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.out0 = dA;
   p.out1 = dB;
   p.ldo = g.f;
+  if (!make_map_out_bf16(&m.o0, dA, g.f, g.rows) || !make_map_out_bf16(&m.o1, dB, g.f, g.rows))
+    return cudaErrorInvalidValue;
   p.part = ab_amax;
   p.part_ld = gemm_col_tiles(g.f);
   const long long R = rows_per_expert(g);
@@ -1307,6 +1443,7 @@ cudaError_t gemm_fc1_dgrad_fp8(const GemmProblem& g, const void* dAq, const void
   p.col_scale0 = s13r;
   p.out0 = dX;
   p.ldo = g.h;
+  if (!make_map_out(&m.o0, dX, g.h, g.rows)) return cudaErrorInvalidValue;
   const long long R = rows_per_expert(g);
   set_raster(p, R * 2 * g.f, 2ll * g.f * g.h, 1ll * BM * 2 * g.f, 1ll * BN * 2 * g.f);
   return launch<false, false, 1, EPI_F32_F8, false>(p, m, mgrouped_tiles(g, EPI_F32_F8, g.h, BN),
@@ -1339,6 +1476,9 @@ cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& g, const void* Xq, const float* 
   p.out1 = B;
   p.out2 = H;
   p.ldo = g.f;
+  if (!make_map_out_bf16(&m.o0, A, g.f, g.rows) || !make_map_out_bf16(&m.o1, B, g.f, g.rows) ||
+      !make_map_out_bf16(&m.o2, H, g.f, g.rows))
+    return cudaErrorInvalidValue;
   const long long R = rows_per_expert(g);
   set_raster(p, R * g.h, 2ll * g.h * g.f, 1ll * BM * g.h, 1ll * BN * g.h);
   return launch<false, false, 2, EPI_SWIGLU_F8, false>(
@@ -1363,6 +1503,7 @@ cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& g, const void* Hq, const float* 
   p.col_scale0 = s2;
   p.out0 = O;
   p.ldo = g.h;
+  if (!make_map_out_bf16(&m.o0, O, g.h, g.rows)) return cudaErrorInvalidValue;
   const long long R = rows_per_expert(g);
   set_raster(p, R * g.f, 1ll * g.f * g.h, 1ll * BM * g.f, 1ll * BN * g.f);
   return launch<false, false, 1, EPI_BF16_F8, false>(p, m, mgrouped_tiles(g, EPI_BF16_F8, g.h, BN),
@@ -1393,6 +1534,9 @@ cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& g, const void* dy_perm, const 
   p.out1 = dB;
   p.out2 = gH;
   p.ldo = g.f;
+  if (!make_map_out_bf16(&m.o0, dA, g.f, g.rows) || !make_map_out_bf16(&m.o1, dB, g.f, g.rows) ||
+      !make_map_out_bf16(&m.o2, gH, g.f, g.rows))
+    return cudaErrorInvalidValue;
   const long long R = rows_per_expert(g);
   set_raster(p, R * g.h * 2, 2ll * g.h * g.f, 1ll * tile_rows(EPI_SWIGLU_BWD_SAR) * g.h * 2, 1ll * BN * g.h * 2);
   return launch<false, false, 1, EPI_SWIGLU_BWD_SAR, false>(
@@ -1415,6 +1559,7 @@ cudaError_t gemm_fc1_dgrad(const GemmProblem& g, const void* dA, const void* dB,
   p.b_rows = g.h;
   p.out0 = dX;
   p.ldo = g.h;
+  if (!make_map_out(&m.o0, dX, g.h, g.rows)) return cudaErrorInvalidValue;
   const long long R = rows_per_expert(g);
   set_raster(p, R * 2 * g.f * 2, 4ll * g.f * g.h, 1ll * tile_rows(EPI_F32) * 2 * g.f * 2, 1ll * BN * 2 * g.f * 2);
   return launch<false, false, 1, EPI_F32, false>(p, m, mgrouped_tiles(g, EPI_F32, g.h, BN),
@@ -1434,6 +1579,7 @@ cudaError_t gemm_fc2_wgrad(const GemmProblem& g, const void* H, const void* dO, 
   p.M = g.f;
   p.N = g.h;
   p.out0 = dW2;
+  if (!make_map_out(&m.o0, dW2, g.h, static_cast<uint64_t>(g.E) * g.f)) return cudaErrorInvalidValue;
   p.ktiles = static_cast<int>(kgrouped_tiles(g, EPI_WGRAD, g.f, g.h, BN));
   const long long R = rows_per_expert(g);
   set_raster(p, R * g.f * 2, R * g.h * 2, tile_rows(EPI_WGRAD) * R * 2, BN * R * 2);
@@ -1454,6 +1600,9 @@ cudaError_t gemm_fc1_wgrad(const GemmProblem& g, const void* x_perm, const void*
   p.N = g.f;
   p.out0 = dW1;
   p.out1 = dW3;
+  if (!make_map_out(&m.o0, dW1, g.f, static_cast<uint64_t>(g.E) * g.h) ||
+      !make_map_out(&m.o1, dW3, g.f, static_cast<uint64_t>(g.E) * g.h))
+    return cudaErrorInvalidValue;
   p.ktiles = static_cast<int>(kgrouped_tiles(g, EPI_WGRAD, g.h, g.f, BN / 2));
   const long long R = rows_per_expert(g);
   set_raster(p, R * g.h * 2, R * 2 * g.f * 2, tile_rows(EPI_WGRAD) * R * 2, BN * R * 2);
