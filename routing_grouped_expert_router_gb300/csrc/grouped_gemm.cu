@@ -127,6 +127,9 @@ struct Maps {
   // Outputs written by TMA from the epilogue's staging blocks (32 x 32 boxes):
   // fp32 (EPI_WGRAD, EPI_F32; 128B swizzle) or bf16 (the rest; 64B swizzle).
   CUtensorMap o0, o1, o2;
+  // EPI_SWIGLU_BWD(_SAR): A and B [rows, f] bf16, 256 x 32 boxes, for the L2
+  // prefetch of the next tile's rows
+  CUtensorMap i0, i1;
 };
 
 struct Tile {
@@ -400,6 +403,16 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, const Maps& ma
     }
     store_bf16_chunk<3>(p, maps, stage, nblk, grow0, col, row_ok, da, db, av, lane);
   }
+}
+
+// The SwiGLU-backward epilogue reads A and B of its tile's rows straight from
+// DRAM one chunk ahead, which does not cover DRAM latency; so while tile t is
+// in its epilogue, each warp asks the TMA unit to bring its 32 rows of the
+// CTA's next tile into L2 (the main loop of that tile gives them time to land).
+template <int BNB>
+__device__ __forceinline__ void prefetch_ab_rows(const Maps& maps, const Tile& tn, int row_off) {
+  tma_prefetch_l2_2d(&maps.i0, tn.nb * BNB, tn.row0 + row_off);
+  tma_prefetch_l2_2d(&maps.i1, tn.nb * BNB, tn.row0 + row_off);
 }
 
 // The next chunk's A and B pieces (nothing for rows or columns out of range).
@@ -678,10 +691,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int nblk = 0;  // fp32 blocks this warp has staged
     int it = 0;
     Tile tl;
+    if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
+      Tile tn;
+      if (lane == 0 && decode<BM, GROUP_K, NUM_B>(p, c.off, c.cum, blockIdx.x, tn))
+        prefetch_ab_rows<BNB>(maps, tn, quarter * 32);
+    }
     for (int t = blockIdx.x; decode<BM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += gridDim.x) {
       // every decision to stop is taken by the whole warp: the TMEM loads and
       // the staged stores below are warp-collective
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
+        Tile tn;
+        if (lane == 0 && decode<BM, GROUP_K, NUM_B>(p, c.off, c.cum, t + gridDim.x, tn))
+          prefetch_ab_rows<BNB>(maps, tn, quarter * 32);
+      }
       if (GROUP_K && tl.nkb == 0) {  // expert without tokens: zero weight gradient
         zero_wgrad_row<NUM_B>(p, tl, tl.mb * BM + r);
         continue;
@@ -1031,8 +1054,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int nblk = 0;
     int it = 0;
     Tile tl;
+    if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
+      Tile tn;
+      if (lane == 0 && decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, cid, tn))
+        prefetch_ab_rows<BNB>(maps, tn, half + quarter * 32);
+    }
     for (int t = cid; decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-wide, as above
+      if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
+        Tile tn;
+        if (lane == 0 && decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t + ncl, tn))
+          prefetch_ab_rows<BNB>(maps, tn, half + quarter * 32);
+      }
       const int orow = tl.mb * PM + half + r;       // K-grouped output row
       if (GROUP_K && tl.nkb == 0) {
         zero_wgrad_row<NUM_B>(p, tl, orow);
@@ -1186,6 +1219,19 @@ bool make_map_out_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [outer, inner] for L2 prefetches of 256 x 32 boxes.
+bool make_map_prefetch(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(inner < 256 ? inner : 256), 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Which kernel runs each matmul.  Measured on GB300 (Mixtral-8x7B-shaped
@@ -1406,6 +1452,8 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.b_rows = g.f;
   p.in0 = A;
   p.in1 = B;
+  if (!make_map_prefetch(&m.i0, A, g.f, g.rows) || !make_map_prefetch(&m.i1, B, g.f, g.rows))
+    return cudaErrorInvalidValue;
   p.out0 = dA;
   p.out1 = dB;
   p.ldo = g.f;
@@ -1527,6 +1575,8 @@ cudaError_t gemm_fc2_dgrad_sar(const GemmProblem& g, const void* dy_perm, const 
   p.b_rows = g.f;
   p.in0 = A;
   p.in1 = B;
+  if (!make_map_prefetch(&m.i0, A, g.f, g.rows) || !make_map_prefetch(&m.i1, B, g.f, g.rows))
+    return cudaErrorInvalidValue;
   p.in2 = gate_rows;
   p.part = dg_part;
   p.part_ld = gemm_col_tiles(g.f);
