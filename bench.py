@@ -93,10 +93,10 @@ def workload_desc(cfg):
             + (f" zipf{cfg.zipf_s}" if cfg.zipf_s else ""))
 
 
-# DRAM traffic of the dominant GroupedGEMM, from an ncu capture summarised in
+# DRAM traffic of each GroupedGEMM, from an ncu capture summarised in
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of one launch).  It
 # is reported only while the GEMM sources are the ones it was captured from.
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "dram_traffic_gg_fc1_wgrad_mixtral8x7b.md")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "dram_traffic_gemms_mixtral8x7b.md")
 GEMM_SOURCES = ("grouped_gemm.cu", "grouped_gemm.cuh", "ptx.cuh")
 
 
@@ -117,10 +117,11 @@ def measured_traffic(kernel: str, workload: str):
                         if line.startswith("    ") and ": " in line)
     except OSError:
         return None
-    if (vals.get("kernel") != kernel or vals.get("workload") != workload
+    key = "dram_bytes_per_launch." + kernel
+    if (key not in vals or vals.get("workload") != workload
             or vals.get("source_sha256") != gemm_source_hash()):
         return None
-    return float(vals["dram_bytes_per_launch"])
+    return float(vals[key])
 
 
 def load_peaks():
