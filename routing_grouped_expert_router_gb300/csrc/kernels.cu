@@ -279,6 +279,172 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
   cp_async_wait<0>();
 }
 
+// ---- E <= 8 with the whole of Wg in shared memory (h <= kRouterA1MaxH): one
+// launch routes every token, with no partial logits and no select kernel.
+// Work items are TOK tokens, dealt round-robin to all warps of the grid; TOK
+// is picked at launch so that T / TOK items spread evenly over the warps.
+// Within an item the lanes split the columns (8 per lane per 256-column
+// step) and keep all TOK x 8 partial logits, as in router_a_kernel: a bf16x2
+// word of x and two weights of one expert feed one packed fp32x2 FMA.  Each
+// warp streams its item's x through its own ring of NST cp.async stages, so
+// it needs warp-level syncs only.  At the end of an item a reduce-scatter
+// over the lanes (5 exchange rounds on halving halves, 62 shuffles instead of
+// 320 for a full butterfly) leaves lane l with sums 2l and 2l + 1 of the
+// TOK x 8 (token, expert) logits; they meet in shared memory, where lane u
+// selects token u's top-k.
+constexpr int kRouterA1Threads = 256;
+constexpr int kRouterA1Warps = kRouterA1Threads / 32;
+constexpr int kRouterA1Step = 256;  // columns per stage
+constexpr int kRouterA1NStage = 3;
+constexpr int kRouterA1MaxH = 4096;
+constexpr size_t router_a1_smem(int h, int tok) {
+  return static_cast<size_t>((h + 7) / 8) * kRouterASlice * 4 +
+         static_cast<size_t>(kRouterA1Warps) * kRouterA1NStage * tok * kRouterA1Step * 2 +
+         static_cast<size_t>(kRouterA1Warps) * 64 * 4;
+}
+
+template <int TOK>
+__global__ void __launch_bounds__(kRouterA1Threads, 1) router_a1_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ Wg, const float* __restrict__ b,
+    int T, int h, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ gates) {
+  constexpr int EP = 8, SLICE = kRouterASlice, NST = kRouterA1NStage, SC = kRouterA1Step;
+  constexpr int XSTAGE = TOK * SC;  // bf16 per stage of one warp
+  extern __shared__ float sw[];
+  const int nslice = (h + 7) / 8;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sw + nslice * SLICE) + warp * NST * XSTAGE;
+  float* lg = sw + nslice * SLICE + kRouterA1Warps * NST * XSTAGE / 2 + warp * 64;
+
+  const int nsteps = (h + SC - 1) / SC;
+  const int nitems = (T + TOK - 1) / TOK;
+  const int gw = blockIdx.x * kRouterA1Warps + warp;
+  const int nw = gridDim.x * kRouterA1Warps;
+  const int my_items = gw < nitems ? (nitems - gw + nw - 1) / nw : 0;
+  const int total = my_items * nsteps;
+
+  // the warp's stream of (item, step) stages; slot g % NST
+  int is_item = gw, is_step = 0, is_slot = 0;
+  auto issue = [&](int g) {
+    if (g < total) {
+      const int t0 = is_item * TOK;
+      const int c = is_step * SC + 8 * lane;
+      const uint32_t base = smem_addr(xs + is_slot * XSTAGE + 8 * lane);
+#pragma unroll
+      for (int i = 0; i < TOK; ++i) {
+        const bool ok = t0 + i < T && c < h;
+        const uint16_t* src = ok ? x + static_cast<size_t>(t0 + i) * h + c : x;
+        cp_async16(base + i * SC * 2, src, ok);
+      }
+      if (++is_step == nsteps) {
+        is_step = 0;
+        is_item += nw;
+      }
+      if (++is_slot == NST) is_slot = 0;
+    }
+    cp_async_commit();  // an empty group keeps the group count uniform
+  };
+#pragma unroll
+  for (int g = 0; g < NST - 1; ++g) issue(g);
+  // the weights are staged while the first x stages are in flight
+  if (E == EP) {
+    for (int lr = 2 * threadIdx.x; lr < h; lr += 2 * kRouterA1Threads) {
+      const float4* src = reinterpret_cast<const float4*>(Wg + static_cast<size_t>(lr) * EP);
+      const float4 a0 = __ldg(src), a1 = __ldg(src + 1), b0 = __ldg(src + 2), b1 = __ldg(src + 3);
+      float4* dst = reinterpret_cast<float4*>(sw + (lr >> 3) * SLICE + ((lr & 7) >> 1) * (2 * EP));
+      dst[0] = make_float4(a0.x, b0.x, a0.y, b0.y);
+      dst[1] = make_float4(a0.z, b0.z, a0.w, b0.w);
+      dst[2] = make_float4(a1.x, b1.x, a1.y, b1.y);
+      dst[3] = make_float4(a1.z, b1.z, a1.w, b1.w);
+    }
+  } else {
+    for (int q = threadIdx.x; q < h * EP; q += kRouterA1Threads) {
+      const int lr = q / EP;
+      const int e = q - lr * EP;
+      sw[(lr >> 3) * SLICE + ((lr & 7) >> 1) * (2 * EP) + 2 * e + (lr & 1)] =
+          (e < E) ? __ldg(Wg + static_cast<size_t>(lr) * E + e) : 0.f;
+    }
+  }
+  __syncthreads();  // weights staged
+
+  float2 acc2[TOK][EP];  // (even-column, odd-column) partial sums
+  int item = gw, step = 0, slot = 0;
+  for (int g = 0; g < total; ++g) {
+    issue(g + NST - 1);
+    cp_async_wait<NST - 1>();
+    __syncwarp();  // stage g landed for every lane's copies (the warp's own rows)
+    if (step == 0) {
+#pragma unroll
+      for (int u = 0; u < TOK; ++u)
+#pragma unroll
+        for (int e = 0; e < EP; ++e) acc2[u][e] = make_float2(0.f, 0.f);
+    }
+    const int lc = step * SC + 8 * lane;
+    if (lc < h) {
+      const uint16_t* xt = xs + slot * XSTAGE + 8 * lane;
+      uint4 xq[TOK];
+#pragma unroll
+      for (int u = 0; u < TOK; ++u) xq[u] = *reinterpret_cast<const uint4*>(xt + u * SC);
+      const float4* wb = reinterpret_cast<const float4*>(sw + (lc >> 3) * SLICE);
+#pragma unroll
+      for (int j2 = 0; j2 < 4; ++j2) {
+        float2 xp[TOK];
+#pragma unroll
+        for (int u = 0; u < TOK; ++u) {
+          const uint32_t w = j2 == 0 ? xq[u].x : j2 == 1 ? xq[u].y : j2 == 2 ? xq[u].z : xq[u].w;
+          xp[u] = make_float2(bf16_lo(w), bf16_hi(w));
+        }
+#pragma unroll
+        for (int e2 = 0; e2 < EP / 2; ++e2) {
+          const float4 w4 = wb[j2 * (EP / 2) + e2];
+          const float2 wa = make_float2(w4.x, w4.y);
+          const float2 wc = make_float2(w4.z, w4.w);
+#pragma unroll
+          for (int u = 0; u < TOK; ++u) {
+            acc2[u][2 * e2] = __ffma2_rn(xp[u], wa, acc2[u][2 * e2]);
+            acc2[u][2 * e2 + 1] = __ffma2_rn(xp[u], wc, acc2[u][2 * e2 + 1]);
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane is done with the slot before it is refilled
+    if (++slot == NST) slot = 0;
+    if (++step == nsteps) {
+      // reduce-scatter of v[u * 8 + e] (u < TOK, e < 8; zero-padded to 64)
+      float v[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = (i / EP < TOK) ? acc2[i / EP][i % EP].x + acc2[i / EP][i % EP].y : 0.f;
+#pragma unroll
+      for (int sft = 16, n = 64; sft >= 1; sft >>= 1, n >>= 1) {
+        const bool upper = (lane & sft) != 0;
+        const int half = n / 2;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float keep = upper ? v[half + i] : v[i];
+          const float give = upper ? v[i] : v[half + i];
+          v[i] = keep + __shfl_xor_sync(kFull, give, sft);
+        }
+      }
+      lg[2 * lane] = v[0];  // sums 2 lane and 2 lane + 1
+      lg[2 * lane + 1] = v[1];
+      __syncwarp();
+      const int t = item * TOK + lane;
+      if (lane < TOK && t < T) {
+        float l[EP];
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+          l[e] = (e < E) ? lg[lane * EP + e] + (b ? __ldg(b + e) : 0.f) : 0.f;
+        select_topk<EP>(l, E, k, topk_idx + static_cast<size_t>(t) * k,
+                        gates + static_cast<size_t>(t) * k);
+      }
+      __syncwarp();  // the scratch is read before the next item overwrites it
+      step = 0;
+      item += nw;
+    }
+  }
+  cp_async_wait<0>();
+}
+
 // ---- E > 8: lanes own experts.  A group of GL = EP / 4 lanes handles TOK
 // tokens; lane i of a group owns the four consecutive experts 4i .. 4i + 3,
 // whose weights for one column are one conflict-free 16-byte shared-memory
@@ -419,8 +585,55 @@ int router_padded_e(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : 6
 
 int router_chunks(int h, int E) {
   const int ep = router_padded_e(E);
+  if (ep == 8 && h <= kRouterA1MaxH) return 1;  // router_a1_kernel holds all of Wg
   const int ch = ep == 8 ? kRouterACh : 32768 / ep;
   return (h + ch - 1) / ch;
+}
+
+// router_a1_kernel<TOK>: the TOK whose items spread most evenly over the
+// grid's warps (fewest token slots on the busiest warp; ties to the larger
+// TOK), within the shared-memory limit.
+template <int TOK>
+cudaError_t router_a1_launch(const uint16_t* x, const float* Wg, const float* b, int T, int h,
+                             int E, int k, int32_t* idx, float* gates, int blocks,
+                             cudaStream_t s) {
+  const size_t smem = router_a1_smem(h, TOK);
+  static int attr_smem = 0;
+  if (attr_smem < static_cast<int>(smem)) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        router_a1_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_smem = static_cast<int>(smem);
+  }
+  router_a1_kernel<TOK><<<blocks, kRouterA1Threads, smem, s>>>(x, Wg, b, T, h, E, k, idx, gates);
+  return launched();
+}
+
+cudaError_t router_a1_dispatch(const uint16_t* x, const float* Wg, const float* b, int T, int h,
+                               int E, int k, int32_t* idx, float* gates, int num_sms,
+                               cudaStream_t s) {
+  const long long nw = static_cast<long long>(num_sms) * kRouterA1Warps;
+  int best = 4;
+  long long best_slots = -1;
+  for (int tok = 4; tok <= 7; ++tok) {
+    if (router_a1_smem(h, tok) > 232448) continue;
+    const long long items = (T + tok - 1) / tok;
+    const long long slots = (items + nw - 1) / nw * tok;
+    if (best_slots < 0 || slots <= best_slots) {
+      best = tok;
+      best_slots = slots;
+    }
+  }
+  // blocks: enough warps for the items, at most one block per SM
+  const long long items = (T + best - 1) / best;
+  int blocks = static_cast<int>((items + kRouterA1Warps - 1) / kRouterA1Warps);
+  if (blocks > num_sms) blocks = num_sms;
+  switch (best) {
+    case 4: return router_a1_launch<4>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
+    case 5: return router_a1_launch<5>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
+    case 6: return router_a1_launch<6>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
+    default: return router_a1_launch<7>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
+  }
 }
 
 template <int EP>
@@ -896,6 +1109,7 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
   const int ep = router_padded_e(E);
   const int nch = router_chunks(h, E);
   cudaError_t err;
+  if (ep == 8 && nch == 1) return router_a1_dispatch(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
   if (ep == 8) {
     static bool attr = false;
     if (!attr) {
