@@ -199,7 +199,12 @@ __device__ __forceinline__ bool decode(const Params& p, const int* off, const in
   return true;
 }
 
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+// sigmoid and silu for the SwiGLU epilogues, with CUDA's fast exponential and
+// division intrinsics: their few-ulp error in fp32 is far below the bf16
+// rounding of every value these epilogues store.  (For a < -88, __expf(-a)
+// overflows to inf and both give 0, the limit.)
+__device__ __forceinline__ float sigmoid_f(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -377,7 +382,7 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, const Maps& ma
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float a = av[i];
-      const float sg = 1.0f / (1.0f + expf(-a));
+      const float sg = sigmoid_f(a);
       const float dh = v0[i];
       da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
       db[i] = dh * a * sg;
@@ -392,7 +397,7 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, const Maps& ma
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float a = av[i];
-      const float sg = 1.0f / (1.0f + expf(-a));
+      const float sg = sigmoid_f(a);
       const float sl = a * sg;
       const float hh = sl * bv[i];
       const float dh = g * v0[i];
