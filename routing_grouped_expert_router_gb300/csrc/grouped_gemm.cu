@@ -799,21 +799,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // Synchronisation: the even CTA's `full` barrier counts both CTAs' bytes: its
 // own loads signal it directly, and the odd CTA's loads signal it across the
 // pair (TMA .cta_group::2).  The exception is the last K block of a wgrad tile
-// whose rows run into the next expert: the odd CTA then loads against its own
-// barrier, and its warp 1 waits for the bytes, clears the stale k-rows and
-// arrives on the even CTA's barrier (count 2 = the even producer's arrivals
-// plus, for such a block, that relay).  The issuer's commits are multicast to
-// the `empty` and `tfull` barriers of both CTAs; all eight epilogue warps
-// arrive on the even CTA's `tempty` barrier.
+// whose rows run into the next expert: each CTA then loads it against its own
+// `tailbar`, and its relay warp (warp 6) waits for the bytes, clears the
+// stale k-rows and arrives on the even CTA's `full` (count 2: the even
+// producer's two arrivals for a plain block, the two relays for such a
+// block).  Clearing there, rather than in the issuer, keeps the issuer's
+// stream of MMAs free of stores and proxy fences: measured on GB300, the
+// issuer-side clearing cost the wgrads about 5%.  The issuer's commits are
+// multicast to the `empty` and `tfull` barriers of both CTAs; all eight
+// epilogue warps arrive on the even CTA's `tempty` barrier.
 constexpr int PM = 256;                           // rows of a pair tile
 constexpr int STAGES2 = 6;
 constexpr int A2_BYTES = 128 * BK * 2;            // this CTA's 128 rows: 16 KiB
 constexpr int B2_BYTES = 128 * BK * 2;            // this CTA's 128 columns: 16 KiB
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;  // 32 KiB
+constexpr int NUM_THREADS2 = NUM_THREADS + 32;     // the one-CTA roles plus the relay warp
 
 struct alignas(8) Ctrl2 {
   uint64_t full[STAGES2];
   uint64_t empty[STAGES2];
+  uint64_t tailbar[STAGES2];  // wgrad K blocks that run past the expert (see above)
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -828,7 +833,7 @@ static_assert(SMEM2_BYTES <= 232448, "pair kernel exceeds the 227 KiB shared-mem
 static_assert(SMEM_BYTES <= 232448, "one-CTA kernel exceeds the 227 KiB shared-memory limit");
 
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS2, 1)
     gg2_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -846,6 +851,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES2; ++s) {
       mbar_init(smem_u32(&c.full[s]), rank == 0 ? 2 : 1);
       mbar_init(smem_u32(&c.empty[s]), 1);
+      mbar_init(smem_u32(&c.tailbar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&c.tfull[b]), 1);
@@ -862,7 +868,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish2();
     tc_fence_before();
   }
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
     for (int e = threadIdx.x - 64; e <= p.E; e += 128) {
       const int o = __ldg(p.offsets + e);
       c.off[e] = o < 0 ? 0 : (o > p.rows ? p.rows : o);
@@ -906,17 +912,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const bool tail = GROUP_K && tl.row_end - (tl.row0 + kb * BK) < BK;
           const uint32_t own_full = smem_u32(&c.full[s]);
           uint32_t bar;  // where this CTA's loads complete
-          if (rank == 0) {
+          if (tail) {
+            bar = smem_u32(&c.tailbar[s]);  // the relay warp takes it from here
+            mbar_expect_tx(bar, STAGE2_BYTES);
+          } else if (rank == 0) {
             bar = own_full;
-            if (tail) {
-              mbar_expect_tx(own_full, STAGE2_BYTES);      // + the relay's arrival
-            } else {
-              mbar_expect_tx(own_full, 2 * STAGE2_BYTES);  // both CTAs' bytes
-              mbar_arrive(own_full);
-            }
-          } else if (tail) {
-            bar = own_full;
-            mbar_expect_tx(own_full, STAGE2_BYTES);
+            mbar_expect_tx(own_full, 2 * STAGE2_BYTES);  // both CTAs' bytes
+            mbar_arrive(own_full);
           } else {
             bar = mapa_shared(own_full, 0);
           }
@@ -997,10 +999,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           uint8_t* a_tile = smem + s * STAGE2_BYTES;
-          if (GROUP_K) {
-            const int kv = tl.row_end - (tl.row0 + kb * BK);
-            if (kv < BK) zero_a_tail(a_tile, kv, lane);
-          }
           if (lane == 0) {
             tc_fence_after();
             const uint32_t a_base = smem_u32(a_tile);
@@ -1022,31 +1020,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_wait(smem_u32(&c.drain), 0, p.status, kTimeoutCode);
       }
       __syncwarp();
-    } else {
-      // ----------------------------------------------- relay (odd CTA)
-      // Only wgrad tiles whose last K block runs into the next expert need it:
-      // that block was loaded against this CTA's own `full` barrier.
-      if (GROUP_K) {
-        int q = 0;
-        uint32_t phase_bits = 0;  // completed phases of each own `full` barrier
-        Tile tl;
-        for (int t = cid; decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
-          if (tl.nkb == 0) continue;
-          const int last = q + tl.nkb - 1;
-          q += tl.nkb;
-          const int kv = tl.row_end - (tl.row0 + (tl.nkb - 1) * BK);
-          if (kv >= BK) continue;
-          const int s = last % STAGES2;
-          const uint32_t ph = (phase_bits >> s) & 1u;
-          phase_bits ^= 1u << s;
-          if (*abort_flag || !mbar_wait(smem_u32(&c.full[s]), ph, p.status, kTimeoutCode)) {
-            give_up();
-            break;
-          }
-          zero_a_tail(smem + s * STAGE2_BYTES, kv, lane);
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&c.full[s]), 0));
-          __syncwarp();
+    }
+  } else if (warp == 6) {
+    // ----------------------------------------------- relay (both CTAs)
+    // Only wgrad tiles whose last K block runs into the next expert need it:
+    // that block was loaded against this CTA's `tailbar`.
+    if (GROUP_K) {
+      int q = 0;
+      uint32_t phase_bits = 0;  // completed phases of each `tailbar`
+      Tile tl;
+      const uint32_t full0 = rank == 0 ? 0u : 1u;  // 0: arrive locally
+      for (int t = cid; decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
+        if (tl.nkb == 0) continue;
+        const int last = q + tl.nkb - 1;
+        q += tl.nkb;
+        const int kv = tl.row_end - (tl.row0 + (tl.nkb - 1) * BK);
+        if (kv >= BK) continue;
+        const int s = last % STAGES2;
+        const uint32_t ph = (phase_bits >> s) & 1u;
+        phase_bits ^= 1u << s;
+        if (*abort_flag || !mbar_wait(smem_u32(&c.tailbar[s]), ph, p.status, kTimeoutCode)) {
+          give_up();
+          break;
         }
+        zero_a_tail(smem + s * STAGE2_BYTES, kv, lane);
+        if (lane == 0) {
+          if (full0 == 0)
+            mbar_arrive(smem_u32(&c.full[s]));
+          else
+            mbar_arrive_cluster(mapa_shared(smem_u32(&c.full[s]), 0));
+        }
+        __syncwarp();
       }
     }
   } else {
@@ -1287,7 +1291,7 @@ cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num
     }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS2, 1, 1);
     cfg.dynamicSmemBytes = SMEM2_BYTES;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

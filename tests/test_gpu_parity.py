@@ -34,6 +34,8 @@ CASES = {
     "k8": dict(T=100, h=128, f=128, E=16, k=8, seed=6),
     "one_token": dict(T=1, h=64, f=128, E=4, k=2, seed=7),
     "ragged": dict(T=777, h=192, f=320, E=5, k=3, seed=8),
+    # E <= 8 with h > 4096: the router's chunked kernel and its select kernel
+    "wide_h": dict(T=300, h=4160, f=192, E=6, k=2, seed=9),
 }
 
 
