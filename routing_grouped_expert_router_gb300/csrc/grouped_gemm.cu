@@ -845,6 +845,9 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(cluster_count_x());
   constexpr int BNB = BN / NUM_B;
+  constexpr bool F8 = is_f8(EPI);  // e4m3 operands (K-major only): 128 per 128-byte row
+  constexpr int BKE = F8 ? 2 * BK : BK;  // K elements per stage
+  static_assert(!F8 || (!A_MN && !B_MN && !GROUP_K), "FP8 matmuls take K-major operands");
 
   // ------------------------------------------------------------ set-up
   if (warp == 0 && lane == 0) {
@@ -944,7 +947,7 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
           const int bcol = NUM_B == 2 ? tl.nb * BNB : tl.nb * BN + 128 * static_cast<int>(rank);
           if (!GROUP_K) {
             const bool second = p.kconcat == 2 && kb >= p.kblocks;
-            const int kx = (second ? kb - p.kblocks : kb) * BK;
+            const int kx = (second ? kb - p.kblocks : kb) * BKE;
             load(a_dst, second ? &maps.a1 : &maps.a0, kx, tl.row0 + 128 * static_cast<int>(rank));
             if (!B_MN) {
               load(b_dst, second ? &maps.b1 : &maps.b0, kx,
@@ -970,7 +973,7 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
   } else if (warp == 1) {
     if (rank == 0) {
       // ----------------------------------------------- MMA issuer (even CTA)
-      constexpr uint32_t IDESC = idesc_bf16(PM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = F8 ? idesc_e4m3(PM, BN) : idesc_bf16(PM, BN, A_MN, B_MN);
       constexpr uint32_t A_LBO = A_MN ? CHUNK_BYTES : 16;
       constexpr uint32_t B_LBO = B_MN ? CHUNK_BYTES : 16;
       constexpr uint32_t A_KSTEP = A_MN ? 2048 : 32;
@@ -1004,9 +1007,14 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
             const uint32_t a_base = smem_u32(a_tile);
             const uint32_t b_base = a_base + A2_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              umma2_bf16(acc, smem_desc(a_base + kk * A_KSTEP, A_LBO, 1024),
-                         smem_desc(b_base + kk * B_KSTEP, B_LBO, 1024), IDESC, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = smem_desc(a_base + kk * A_KSTEP, A_LBO, 1024);
+              const uint64_t bd = smem_desc(b_base + kk * B_KSTEP, B_LBO, 1024);
+              if (F8)
+                umma2_e4m3(acc, ad, bd, IDESC, (kb | kk) != 0);
+              else
+                umma2_bf16(acc, ad, bd, IDESC, (kb | kk) != 0);
+            }
             umma2_commit_mc(smem_u32(&c.empty[s]), 0x3);
           }
           __syncwarp();
@@ -1123,18 +1131,21 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
           tmem_ld32(tbase + ch * 32, v0);
           if (NUM_B == 2) tmem_ld32(tbase + BNB + ch * 32, v1);
           const int col = tl.nb * BNB + ch * 32;
-          if constexpr (EPI == EPI_WGRAD || EPI == EPI_F32) {
+          if constexpr (EPI == EPI_WGRAD || base_epi(EPI) == EPI_F32) {
             if (col >= p.N) continue;  // the same for the whole warp
+            if (is_f8(EPI) && row_ok) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
             fp32_rows_chunk<NUM_B, EPI>(p, maps, tl, stage, nblk, grow - lane, orow - lane, col,
                                         row_ok, v0, v1, lane);
           } else {
             if (col >= p.N) continue;  // the same for the whole warp
+            if (is_f8(EPI) && row_ok) rescale_f8<NUM_B>(p, tl, grow, col, v0, v1);
             bf16_chunk<NUM_B, EPI>(p, maps, reinterpret_cast<uint4*>(stage), nblk, grow - lane,
                                    col, row_ok, v0, v1, acc, lane);
           }
         }
       }
-      if ((EPI == EPI_SWIGLU_BWD_SAR || (EPI == EPI_SWIGLU_BWD && p.part)) && row_ok)
+      if ((EPI == EPI_SWIGLU_BWD_SAR || EPI == EPI_SWIGLU_F8 ||
+           (EPI == EPI_SWIGLU_BWD && p.part)) && row_ok)
         p.part[static_cast<size_t>(grow) * p.part_ld + tl.nb] = acc;
       tc_fence_before();
       __syncwarp();
@@ -1245,9 +1256,10 @@ bool make_map_prefetch(CUtensorMap* m, const void* base, uint64_t inner, uint64_
 
 // Which kernel runs each matmul.  Measured on GB300 (Mixtral-8x7B-shaped
 // layer): the CTA pair is as fast or faster for every matmul but FC1 forward
-// (wgrads 2-3%, FC2 forward 1%), whose three-output epilogue runs 2% faster on
-// the one-CTA kernel.  MOE_GEMM_CTAS=1 or =2 forces one kind for every matmul
-// (for measurement).
+// (bf16: wgrads 2-3%, FC2 forward 1%; e4m3: FC1 dgrad 3.5%, FC2 forward 2%).
+// FC1 forward runs 2-3% faster on the one-CTA kernel, in bf16 and e4m3: its
+// 256-row pair tiles waste more rows at each expert's end.  MOE_GEMM_CTAS=1
+// or =2 forces one kind for every matmul (for measurement).
 int forced_ctas() {
   static const int v = [] {
     const char* e = getenv("MOE_GEMM_CTAS");
@@ -1256,16 +1268,15 @@ int forced_ctas() {
   return v;
 }
 bool pair_for(int epi) {
-  if (is_f8(epi)) return false;  // the FP8 matmuls run on the one-CTA kernel only
   if (forced_ctas()) return forced_ctas() == 2;
-  return epi != EPI_SWIGLU;
+  return epi != EPI_SWIGLU && epi != EPI_SWIGLU_F8;
 }
 
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
 cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num_sms,
                    cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
-  if (is_f8(EPI) || !pair_for(EPI)) {
+  if (!pair_for(EPI)) {
     auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -1278,9 +1289,7 @@ cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(prm, maps);
     return launched();
   }
-  if constexpr (is_f8(EPI)) {
-    return cudaErrorInvalidValue;
-  } else {
+  {
     auto kern = gg2_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
     static bool attr2_set = false;
     if (!attr2_set) {
@@ -1488,8 +1497,8 @@ cudaError_t gemm_fc1_dgrad_fp8(const GemmProblem& g, const void* dAq, const void
   // A: dAq then dBq [rows, f] (K concatenated);  B: W1r then W3r [E * h rows (N), f (K)]
   if (!make_map(&m.a0, dAq, g.f, g.rows, 2 * BK, BM, true) ||
       !make_map(&m.a1, dBq, g.f, g.rows, 2 * BK, BM, true) ||
-      !make_map(&m.b0, W1r, g.f, static_cast<uint64_t>(g.E) * g.h, 2 * BK, BN, true) ||
-      !make_map(&m.b1, W3r, g.f, static_cast<uint64_t>(g.E) * g.h, 2 * BK, BN, true))
+      !make_map(&m.b0, W1r, g.f, static_cast<uint64_t>(g.E) * g.h, 2 * BK, kmajor_b_rows(EPI_F32_F8), true) ||
+      !make_map(&m.b1, W3r, g.f, static_cast<uint64_t>(g.E) * g.h, 2 * BK, kmajor_b_rows(EPI_F32_F8), true))
     return cudaErrorInvalidValue;
   Params p = base_params(g);
   p.N = g.h;
@@ -1516,7 +1525,7 @@ cudaError_t gemm_fc1_fwd_fp8(const GemmProblem& g, const void* Xq, const float* 
   memset(&m, 0, sizeof(m));
   // A: Xq [rows, h];  B: W13q viewed as [E * 2f rows (N), h (K)], 256-row tiles
   if (!make_map(&m.a0, Xq, g.h, g.rows, 2 * BK, BM, true) ||
-      !make_map(&m.b0, W13q, g.h, static_cast<uint64_t>(g.E) * 2 * g.f, 2 * BK, BN, true))
+      !make_map(&m.b0, W13q, g.h, static_cast<uint64_t>(g.E) * 2 * g.f, 2 * BK, kmajor_b_rows(EPI_SWIGLU_F8), true))
     return cudaErrorInvalidValue;
   m.a1 = m.a0;
   m.b1 = m.b0;
@@ -1548,7 +1557,7 @@ cudaError_t gemm_fc2_fwd_fp8(const GemmProblem& g, const void* Hq, const float* 
   memset(&m, 0, sizeof(m));
   // A: Hq [rows, f];  B: W2q viewed as [E * h rows (N), f (K)]
   if (!make_map(&m.a0, Hq, g.f, g.rows, 2 * BK, BM, true) ||
-      !make_map(&m.b0, W2q, g.f, static_cast<uint64_t>(g.E) * g.h, 2 * BK, BN, true))
+      !make_map(&m.b0, W2q, g.f, static_cast<uint64_t>(g.E) * g.h, 2 * BK, kmajor_b_rows(EPI_BF16_F8), true))
     return cudaErrorInvalidValue;
   m.a1 = m.a0;
   m.b1 = m.b0;
