@@ -118,6 +118,92 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
   }
 }
 
+// The same operation as quant_rows_kernel with a 256-thread block per row (or
+// row pair), the whole row held in registers: NPT 16-byte pieces per thread and
+// row, every load issued before any arithmetic, the amax a block reduction.
+// The row is read from memory once whatever the amax source, and a block has
+// its full row (28 KB for 14336 bf16 values, twice that for a pair) in flight
+// at once; the warp-per-row kernel kept one 16-byte load per lane in flight
+// and read two-pass rows twice from DRAM.  The codes and scales are the same
+// (the amax is a max, whatever the order).
+constexpr int kQrThreads = 256;
+constexpr int kQrMaxNpt = 8;  // rows up to 8 * 256 * 8 = 16384 values
+
+template <int NPT, bool PAIR>
+__global__ void __launch_bounds__(kQrThreads) quant_rows_reg_kernel(
+    const uint4* __restrict__ in, const int32_t* __restrict__ idx, int div, long long rows,
+    long long src_rows, const int32_t* __restrict__ nvalid, int n8, uint2* __restrict__ q,
+    float* __restrict__ scale, const float* __restrict__ amax_part, int nt,
+    uint4* __restrict__ copy, const uint4* __restrict__ in1, uint2* __restrict__ q1) {
+  __shared__ float red[kQrThreads / 32];
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  if (nvalid) {
+    const long long nv = __ldg(nvalid);
+    rows = nv < rows ? (nv < 0 ? 0 : nv) : rows;
+  }
+  for (long long p = blockIdx.x; p < rows; p += gridDim.x) {
+    long long src = idx ? __ldg(idx + p) / div : p;
+    src = src < 0 ? 0 : (src >= src_rows ? src_rows - 1 : src);
+    const uint4* r = in + src * n8;
+    const uint4* r1 = PAIR ? in1 + src * n8 : nullptr;
+    uint4 v[NPT];
+    uint4 v1[PAIR ? NPT : 1];
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) {
+      const int c = t + kQrThreads * j;
+      v[j] = c < n8 ? __ldg(r + c) : make_uint4(0, 0, 0, 0);
+      if constexpr (PAIR) v1[j] = c < n8 ? __ldg(r1 + c) : make_uint4(0, 0, 0, 0);
+    }
+    float amax = 0.f;
+    if (amax_part) {
+      for (int i = t; i < nt; i += kQrThreads) amax = fmaxf(amax, __ldg(amax_part + p * nt + i));
+    } else {
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
+        if constexpr (PAIR) {
+          const uint32_t u1[4] = {v1[j].x, v1[j].y, v1[j].z, v1[j].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u1[i])), fabsf(bf16_hi(u1[i]))));
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+    if (lane == 0) red[t >> 5] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kQrThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    if (amax_part) amax = __bfloat162float(__float2bfloat16_rn(amax));
+    const float s = scale_of(amax);
+    if (t == 0) scale[p] = s;
+    uint2* out = q + p * n8;
+    uint4* cp = copy ? copy + p * n8 : nullptr;
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) {
+      const int c = t + kQrThreads * j;
+      if (c < n8) {
+        const uint4 w = v[j];
+        if (cp) cp[c] = w;
+        out[c] = make_uint2(q2(bf16_lo(w.x), bf16_hi(w.x), s) | (q2(bf16_lo(w.y), bf16_hi(w.y), s) << 16),
+                            q2(bf16_lo(w.z), bf16_hi(w.z), s) | (q2(bf16_lo(w.w), bf16_hi(w.w), s) << 16));
+        if constexpr (PAIR) {
+          const uint4 w1 = v1[j];
+          q1[p * n8 + c] =
+              make_uint2(q2(bf16_lo(w1.x), bf16_hi(w1.x), s) | (q2(bf16_lo(w1.y), bf16_hi(w1.y), s) << 16),
+                         q2(bf16_lo(w1.z), bf16_hi(w1.z), s) | (q2(bf16_lo(w1.w), bf16_hi(w1.w), s) << 16));
+        }
+      }
+    }
+    __syncthreads();  // red is rewritten by the next row
+  }
+}
+
 // Expert weights W [E, K, N] bf16 (N contiguous) -> per-(e, n) scales and
 // K-major codes: output row of column n of expert e is
 //   e * rows_per_e + (n / 128) * group_stride + slot * 128 + n % 128,
@@ -245,6 +331,30 @@ cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, l
                               cudaStream_t s, const int32_t* nvalid, const float* amax_part,
                               int nt, uint16_t* copy, const uint16_t* in1, uint8_t* q1) {
   if (rows == 0 || src_rows == 0) return cudaSuccess;
+  const int n8 = n / 8;
+  const int need = (n8 + kQrThreads - 1) / kQrThreads;
+  if (need <= kQrMaxNpt) {
+    const int npt = need <= 2 ? need : (need <= 4 ? 4 : (need <= 7 ? 7 : 8));
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    const int grid = static_cast<int>(rows < cap ? rows : cap);
+    const uint4* i4 = reinterpret_cast<const uint4*>(in);
+    const uint4* i14 = reinterpret_cast<const uint4*>(in1);
+    uint2* q2p = reinterpret_cast<uint2*>(q);
+    uint2* q12p = reinterpret_cast<uint2*>(q1);
+    uint4* c4 = reinterpret_cast<uint4*>(copy);
+#define MOE_QR(NPT_)                                                                         \
+  if (npt == NPT_) {                                                                        \
+    if (in1)                                                                                \
+      quant_rows_reg_kernel<NPT_, true><<<grid, kQrThreads, 0, s>>>(                        \
+          i4, idx, div, rows, src_rows, nvalid, n8, q2p, scale, amax_part, nt, c4, i14, q12p); \
+    else                                                                                    \
+      quant_rows_reg_kernel<NPT_, false><<<grid, kQrThreads, 0, s>>>(                       \
+          i4, idx, div, rows, src_rows, nvalid, n8, q2p, scale, amax_part, nt, c4, i14, q12p); \
+    return launched();                                                                      \
+  }
+    MOE_QR(1) MOE_QR(2) MOE_QR(4) MOE_QR(7) MOE_QR(8)
+#undef MOE_QR
+  }
   quant_rows_kernel<<<grid_rows(rows, num_sms), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(in), idx, div, rows, src_rows, nvalid, n / 8,
       reinterpret_cast<uint2*>(q), scale, amax_part, nt, reinterpret_cast<uint4*>(copy),

@@ -84,8 +84,11 @@ def test_weight_codes_and_scales_bit_exact(lib):
     np.testing.assert_array_equal(W2, np.transpose(W2q, (0, 2, 1)))
 
 
-def test_row_codes_and_scales_bit_exact(lib):
-    cfg = small_config(name="xq", T=333, h=512, f=128, E=8, k=2, seed=22)
+# row lengths: a block row of 256 x 16-byte pieces or less, a ragged second
+# piece per thread, and rows above the register-held limit (16384 values)
+@pytest.mark.parametrize("h", [512, 2112, 17408])
+def test_row_codes_and_scales_bit_exact(lib, h):
+    cfg = small_config(name="xq", T=333, h=h, f=128, E=8, k=2, seed=22)
     inp = conditioned_inputs(cfg)
     inp["x"][17] = 0                               # a zero row: scale 1, codes 0
     _, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
@@ -239,8 +242,9 @@ def _bview(d, qwb, name, shape, dtype):
     return qwb[off:off + n].view(dtype).view(shape)
 
 
-def test_bwd_weight_codes_and_scales_bit_exact(lib):
-    cfg = small_config(name="wqb", T=8, h=384, f=640, E=3, k=2, seed=23)
+@pytest.mark.parametrize("f", [640, 4224, 16512])
+def test_bwd_weight_codes_and_scales_bit_exact(lib, f):
+    cfg = small_config(name="wqb", T=8, h=384, f=f, E=3, k=2, seed=23)
     inp = conditioned_inputs(cfg)
     d = mb.dims_of(cfg, has_bias=False)
     qwb = _bwd_weights(d, _to(inp, "cuda"))
