@@ -130,6 +130,10 @@ struct Maps {
   // EPI_SWIGLU_BWD(_SAR): A and B [rows, f] bf16, 256 x 32 boxes, for the L2
   // prefetch of the next tile's rows
   CUtensorMap i0, i1;
+  // EPI_SWIGLU_BWD on the CTA pair: A and B again, 32 x 32 boxes with 64B
+  // swizzle (the layout of the dA / dB staging blocks), loaded by TMA into the
+  // epilogue's staging sets
+  CUtensorMap l0, l1;
 };
 
 struct Tile {
@@ -361,6 +365,25 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&q)[4], float* v) {
   }
 }
 
+// dA = dH * B * s (1 + A (1 - s)), dB = dH * silu(A), s = sigmoid(A), on one
+// lane's 32 values; with p.part, acc = the amax of the row's dA and dB.
+__device__ __forceinline__ void swiglu_bwd_math(const Params& p, const float* v0, const float* av,
+                                                const float* bv, float* da, float* db,
+                                                float& acc) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float a = av[i];
+    const float sg = sigmoid_f(a);
+    const float dh = v0[i];
+    da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
+    db[i] = dh * a * sg;
+  }
+  if (p.part) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc = fmaxf(acc, fmaxf(fabsf(da[i]), fabsf(db[i])));
+  }
+}
+
 // The SwiGLU-backward epilogues on a 32-column chunk of a warp's 32 rows (lane
 // i: row grow0 + i) whose A and B values were loaded ahead (raw bf16).
 //   EPI_SWIGLU_BWD: v0 = dH;  dA = dH * B * s (1 + A (1 - s)), dB = dH * silu(A)
@@ -379,18 +402,7 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, const Maps& ma
   unpack_bf16x32(rb, bv);
   float da[32], db[32];
   if (EPI == EPI_SWIGLU_BWD) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float a = av[i];
-      const float sg = sigmoid_f(a);
-      const float dh = v0[i];
-      da[i] = dh * bv[i] * sg * (1.0f + a * (1.0f - sg));
-      db[i] = dh * a * sg;
-    }
-    if (p.part) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc = fmaxf(acc, fmaxf(fabsf(da[i]), fabsf(db[i])));
-    }
+    swiglu_bwd_math(p, v0, av, bv, da, db, acc);
     store_bf16_chunk<2>(p, maps, stage, nblk, grow0, col, row_ok, da, db, db, lane);
   } else {
     const float g = row_ok ? __ldg(p.in2 + grow0 + lane) : 0.f;
@@ -407,6 +419,45 @@ __device__ __forceinline__ void swiglu_bwd_chunk(const Params& p, const Maps& ma
       av[i] = g * hh;  // gH
     }
     store_bf16_chunk<3>(p, maps, stage, nblk, grow0, col, row_ok, da, db, av, lane);
+  }
+}
+
+// EPI_SWIGLU_BWD on the CTA pair.  A TMA load put the chunk's A and B blocks
+// (32 rows x 32 columns of bf16, 64B-swizzled) in the staging set `buf`: A at
+// buf, B at buf + 128.  Lane i reads row i of both, and dA and dB are written
+// over them (the same row, the same places, so no lane touches another's
+// data) and stored from there by TMA.  Rows past the expert's end are stored
+// by their lanes instead, and the set is then free at once.
+__device__ __forceinline__ void swiglu_bwd_chunk_staged(const Params& p, const Maps& maps,
+                                                        uint4* buf, int grow0, int col,
+                                                        bool row_ok, const float* v0, float& acc,
+                                                        int lane) {
+  const int sw = (lane >> 1) & 3;
+  uint4 ra[4], rb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    ra[j] = buf[lane * 4 + (j ^ sw)];
+    rb[j] = buf[128 + lane * 4 + (j ^ sw)];
+  }
+  float av[32], bv[32], da[32], db[32];
+  unpack_bf16x32(ra, av);
+  unpack_bf16x32(rb, bv);
+  swiglu_bwd_math(p, v0, av, bv, da, db, acc);
+  const unsigned ok = __ballot_sync(0xffffffffu, row_ok);
+  if (ok == 0xffffffffu) {
+    stage_bf16(buf, da, lane);
+    stage_bf16(buf + 128, db, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&maps.o0, smem_u32(buf), col, grow0);
+      tma_store_2d(&maps.o1, smem_u32(buf + 128), col, grow0);
+      bulk_commit();
+    }
+  } else if (row_ok) {
+    const size_t o = static_cast<size_t>(grow0 + lane) * p.ldo + col;
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + o, da);
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + o, db);
   }
 }
 
@@ -819,6 +870,7 @@ struct alignas(8) Ctrl2 {
   uint64_t full[STAGES2];
   uint64_t empty[STAGES2];
   uint64_t tailbar[STAGES2];  // wgrad K blocks that run past the expert (see above)
+  uint64_t abar[4][2];        // EPI_SWIGLU_BWD: A/B block loads into each epilogue warp's sets
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -859,6 +911,10 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&c.tfull[b]), 1);
       mbar_init(smem_u32(&c.tempty[b]), 8);
+    }
+    for (int w = 0; w < 4; ++w) {
+      mbar_init(smem_u32(&c.abar[w][0]), 1);
+      mbar_init(smem_u32(&c.abar[w][1]), 1);
     }
     mbar_init(smem_u32(&c.drain), 1);
     c.abort = 0;
@@ -1076,6 +1132,32 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
       if (lane == 0 && decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, cid, tn))
         prefetch_ab_rows<BNB>(maps, tn, half + quarter * 32);
     }
+    // EPI_SWIGLU_BWD: each chunk's A and B blocks come by TMA into one of the
+    // warp's two 4 KiB staging sets, one chunk ahead (the last chunk of a tile
+    // asks for the first of the CTA's next tile); see swiglu_bwd_chunk_staged.
+    // Load n goes to set n & 1 and completes phase (n >> 1) & 1 of its barrier.
+    constexpr bool kStagedAB = EPI == EPI_SWIGLU_BWD;
+    uint4* sets = reinterpret_cast<uint4*>(stage);
+    int lq = 0;  // A/B block loads issued
+    int lw = 0;  // and waited for
+    auto ab_bar = [&](int n) { return smem_u32(&c.abar[warp - 2][n & 1]); };
+    auto issue_ab = [&](int col, int row) {
+      fence_proxy_async_smem();  // the warp's reads of the set come before the refill
+      __syncwarp();
+      if (lane == 0) {
+        bulk_wait_read_0();  // and so does the TMA store that last read it
+        mbar_expect_tx(ab_bar(lq), 4096);
+        tma_load_2d(smem_u32(sets + (lq & 1) * 256), &maps.l0, col, row, ab_bar(lq));
+        tma_load_2d(smem_u32(sets + (lq & 1) * 256 + 128), &maps.l1, col, row, ab_bar(lq));
+      }
+      __syncwarp();
+      ++lq;
+    };
+    if constexpr (kStagedAB) {
+      Tile t0;
+      if (decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, cid, t0))
+        issue_ab(t0.nb * BNB, t0.row0 + half + quarter * 32);
+    }
     for (int t = cid; decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t, tl); t += ncl) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-wide, as above
       if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
@@ -1101,7 +1183,34 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
       const int grow = tl.row0 + half + r;           // M-grouped row
       const bool row_ok = GROUP_K ? (orow < p.M) : (grow < tl.row_end);
       float acc = 0.f;
-      if constexpr (EPI == EPI_SWIGLU_BWD || EPI == EPI_SWIGLU_BWD_SAR) {
+      if constexpr (kStagedAB) {
+        Tile tn;
+        const bool has_next = decode<PM, GROUP_K, NUM_B>(p, c.off, c.cum, t + ncl, tn);
+        bool lost = false;
+#pragma unroll 1
+        for (int ch = 0; ch < BNB / 32; ++ch) {
+          const int col = tl.nb * BNB + ch * 32;
+          const int n = lw++;
+          const bool got = mbar_wait(ab_bar(n), (n >> 1) & 1, p.status, kTimeoutCode);
+          if (!__all_sync(0xffffffffu, got)) {
+            lost = true;
+            break;
+          }
+          if (ch + 1 < BNB / 32)
+            issue_ab(col + 32, grow - lane);
+          else if (has_next)
+            issue_ab(tn.nb * BNB, tn.row0 + half + quarter * 32);
+          float v0[32];
+          tmem_ld32(tbase + ch * 32, v0);
+          if (col >= p.N) continue;  // the same for the whole warp
+          swiglu_bwd_chunk_staged(p, maps, sets + (n & 1) * 256, grow - lane, col, row_ok, v0,
+                                  acc, lane);
+        }
+        if (lost) {
+          give_up();
+          break;
+        }
+      } else if constexpr (EPI == EPI_SWIGLU_BWD_SAR) {
         // A and B of chunk ch + 1 are in flight while chunk ch is computed
         const size_t o0 = static_cast<size_t>(grow) * p.ldo + tl.nb * BNB;
         uint4 ra[4], rb[4];
@@ -1150,6 +1259,9 @@ __global__ void __launch_bounds__(NUM_THREADS2, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&c.tempty[buf]), 0));
+    }
+    if constexpr (kStagedAB) {  // an A/B load still in flight (after an abort)
+      while (lw < lq && mbar_wait(ab_bar(lw), (lw >> 1) & 1, p.status, kTimeoutCode)) ++lw;
     }
     if (lane == 0) bulk_wait_all();  // staged fp32 blocks written out before the CTA ends
   }
@@ -1227,8 +1339,9 @@ bool make_map_out(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 output [outer, inner] (row-major) for the epilogue's TMA stores: 32 x 32
-// boxes, 64B swizzle (one 64-byte row of 32 values per box row).
+// bf16 [outer, inner] (row-major) in 32 x 32 boxes, 64B swizzle (one 64-byte
+// row of 32 values per box row): the epilogue's TMA stores, and the A / B block
+// loads of the pair's SwiGLU-backward epilogue.
 bool make_map_out_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -1470,7 +1583,8 @@ cudaError_t gemm_fc2_dgrad(const GemmProblem& g, const void* dO, const void* W2,
   p.b_rows = g.f;
   p.in0 = A;
   p.in1 = B;
-  if (!make_map_prefetch(&m.i0, A, g.f, g.rows) || !make_map_prefetch(&m.i1, B, g.f, g.rows))
+  if (!make_map_prefetch(&m.i0, A, g.f, g.rows) || !make_map_prefetch(&m.i1, B, g.f, g.rows) ||
+      !make_map_out_bf16(&m.l0, A, g.f, g.rows) || !make_map_out_bf16(&m.l1, B, g.f, g.rows))
     return cudaErrorInvalidValue;
   p.out0 = dA;
   p.out1 = dB;
