@@ -36,6 +36,10 @@ CASES = {
     "ragged": dict(T=777, h=192, f=320, E=5, k=3, seed=8),
     # E <= 8 with h > 4096: the router's chunked kernel and its select kernel
     "wide_h": dict(T=300, h=4160, f=192, E=6, k=2, seed=9),
+    # degenerate routings: one expert (a plain SwiGLU FFN, every gate 1) and
+    # every token to every expert (k = E, the gates the full softmax)
+    "single_expert": dict(T=300, h=128, f=128, E=1, k=1, seed=10),
+    "k_equals_E": dict(T=200, h=128, f=192, E=4, k=4, seed=11),
 }
 
 
