@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "kernels.cuh"
 
@@ -209,38 +210,53 @@ __global__ void __launch_bounds__(kQrThreads) quant_rows_reg_kernel(
 //   e * rows_per_e + (n / 128) * group_stride + slot * 128 + n % 128,
 // row length K bytes.
 //
-// A persistent grid of two 512-thread blocks per SM walks slabs of 64 columns
-// of one expert.  Pass 1 reads the slab with 16-byte loads (8 threads per
-// 128-byte row segment, 64 rows at a time) and reduces each column's amax;
-// pass 2 reads the slab again -- mostly from L2, which holds most of the
-// slabs in flight at once (two per SM, K x 128 bytes each) -- in
-// chunks of 256 rows staged in shared memory, and writes each column's codes
-// as 32-byte runs of its K-major output row.  The next chunk's loads are
-// issued before the current chunk is written.
-constexpr int kQcCols = 64;        // columns per slab
+// A persistent grid of two 512-thread blocks per SM walks slabs of QC columns
+// (64 or 32) of one expert.  Pass 1 reads the slab with 16-byte loads (QC / 8
+// threads per row segment, 4096 / QC rows at a time) and reduces each
+// column's amax; pass 2 reads the slab again, in chunks of 16 * QC / 4 rows
+// staged in shared memory, and writes each column's codes as 32-byte runs of
+// its K-major output row (lane -> column, warp -> 32-row segment).  The next
+// chunk's loads are issued before the current chunk is written.  Pass 2's
+// read hits L2 when the slabs in flight (two per SM, K x 2 QC bytes each) fit
+// in it, which narrower slabs make more likely.
 constexpr int kQcThreads = 512;
-constexpr int kQcChunk = 256;      // K rows per pass-2 chunk (4 tiles of 64)
-constexpr int kQcPitch = kQcCols + 8;  // bf16 elements per staged row (144 bytes)
 
+template <int QC>
+struct QcShape {
+  static constexpr int TPR = QC / 8;                  // threads per row segment
+  static constexpr int RSTEP = kQcThreads / TPR;      // rows per load step
+  static constexpr int SEGS = QC == 64 ? 8 : 16;      // 32-row segments per chunk
+  static constexpr int CHUNK = 32 * SEGS;             // rows per pass-2 chunk
+  static constexpr int LOADS = CHUNK / RSTEP;         // 16-byte loads per thread per chunk
+  static constexpr int PITCH = QC + 8;                // bf16 per staged row
+  static constexpr int RED = RSTEP * (QC + 1) * 4;    // pass-1 reduction bytes
+  static constexpr int TILE = CHUNK * PITCH * 2;      // pass-2 staging bytes
+  static constexpr int SMEM = RED > TILE ? RED : TILE;
+  static_assert(QC == 64 || QC == 32, "slab width");
+  static_assert(kQcThreads / 32 == SEGS * (QC / 32), "one warp per (segment, 32 columns)");
+};
+
+template <int QC>
 __global__ void __launch_bounds__(kQcThreads, 2) quant_cols_kernel(
     const uint16_t* __restrict__ W, int E, int K, int N, int rows_per_e, int group_stride,
     int slot, uint8_t* __restrict__ q, float* __restrict__ scale) {
-  // pass 1 uses it as float [64][65], pass 2 as bf16 [256][kQcPitch]
-  __shared__ __align__(16) uint8_t smem[kQcChunk * kQcPitch * 2];
-  __shared__ float s_col[kQcCols];
+  using S = QcShape<QC>;
+  // pass 1 uses it as float [RSTEP][QC + 1], pass 2 as bf16 [CHUNK][PITCH]
+  __shared__ __align__(16) uint8_t smem[S::SMEM];
+  __shared__ float s_col[QC];
   float* red = reinterpret_cast<float*>(smem);
   uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
   const int t = threadIdx.x;
-  const int c8 = t & 7;      // 8-column group of the loads
-  const int rg = t >> 3;     // row within a 64-row step
+  const int c8 = t % S::TPR;  // 8-column group of the loads
+  const int rg = t / S::TPR;  // row within a load step
   const int warp = t >> 5;
   const int lane = t & 31;
-  const int nslab = (N + kQcCols - 1) / kQcCols;
+  const int nslab = (N + QC - 1) / QC;
   for (int slab = blockIdx.x; slab < E * nslab; slab += gridDim.x) {
     const int e = slab / nslab;
-    const int n0 = (slab - e * nslab) * kQcCols;
+    const int n0 = (slab - e * nslab) * QC;
     const uint16_t* We = W + static_cast<size_t>(e) * K * N + n0 + 8 * c8;
-    const bool col_ok = n0 + 8 * c8 < N;  // N is a multiple of 64: whole groups
+    const bool col_ok = n0 + 8 * c8 < N;  // N is a multiple of 8: whole groups
 
     // ---- pass 1: column amax
     float m[8];
@@ -248,7 +264,7 @@ __global__ void __launch_bounds__(kQcThreads, 2) quant_cols_kernel(
     for (int i = 0; i < 8; ++i) m[i] = 0.f;
     if (col_ok) {
 #pragma unroll 8
-      for (int k = rg; k < K; k += 64) {
+      for (int k = rg; k < K; k += S::RSTEP) {
         const uint4 w = __ldg(reinterpret_cast<const uint4*>(We + static_cast<size_t>(k) * N));
         const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -260,52 +276,51 @@ __global__ void __launch_bounds__(kQcThreads, 2) quant_cols_kernel(
     }
     __syncthreads();  // the previous slab's pass 2 is done with the buffer
 #pragma unroll
-    for (int i = 0; i < 8; ++i) red[rg * 65 + 8 * c8 + i] = m[i];
+    for (int i = 0; i < 8; ++i) red[rg * (QC + 1) + 8 * c8 + i] = m[i];
     __syncthreads();
-    if (t < kQcCols) {
+    if (t < QC) {
       float a = 0.f;
-      for (int r = 0; r < 64; ++r) a = fmaxf(a, red[r * 65 + t]);
+      for (int r = 0; r < S::RSTEP; ++r) a = fmaxf(a, red[r * (QC + 1) + t]);
       const float sc = scale_of(a);
       s_col[t] = sc;
       if (n0 + t < N) scale[static_cast<size_t>(e) * N + n0 + t] = sc;
     }
     __syncthreads();
 
-    // ---- pass 2: quantise and transpose, 256 rows at a time
-    // write-phase roles: lane -> column, warp -> 32-row segment of the chunk
-    const int wc = lane + 32 * (warp & 1);
-    const int seg = warp >> 1;  // 0..7
+    // ---- pass 2: quantise and transpose, CHUNK rows at a time
+    const int wc = lane + 32 * (warp % (QC / 32));  // column of the slab
+    const int seg = warp / (QC / 32);               // 32-row segment of the chunk
     const int n = n0 + wc;
     const float sc = s_col[wc];
     const size_t orow = static_cast<size_t>(e) * rows_per_e + (n / 128) * group_stride +
                         slot * 128 + n % 128;
-    uint4 v[4];
+    uint4 v[S::LOADS];
     auto load_chunk = [&](int k0) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int k = k0 + 64 * j + rg;
+      for (int j = 0; j < S::LOADS; ++j) {
+        const int k = k0 + S::RSTEP * j + rg;
         v[j] = (col_ok && k < K)
                    ? __ldg(reinterpret_cast<const uint4*>(We + static_cast<size_t>(k) * N))
                    : make_uint4(0, 0, 0, 0);
       }
     };
     load_chunk(0);
-    for (int k0 = 0; k0 < K; k0 += kQcChunk) {
+    for (int k0 = 0; k0 < K; k0 += S::CHUNK) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(tile + (64 * j + rg) * kQcPitch + 8 * c8) = v[j];
+      for (int j = 0; j < S::LOADS; ++j)
+        *reinterpret_cast<uint4*>(tile + (S::RSTEP * j + rg) * S::PITCH + 8 * c8) = v[j];
       __syncthreads();
-      if (k0 + kQcChunk < K) load_chunk(k0 + kQcChunk);  // in flight during the writes
+      if (k0 + S::CHUNK < K) load_chunk(k0 + S::CHUNK);  // in flight during the writes
       const int kk = k0 + 32 * seg;
       if (n < N && kk < K) {
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint16_t* col = tile + (32 * seg + 4 * i) * kQcPitch + wc;
+          const uint16_t* col = tile + (32 * seg + 4 * i) * S::PITCH + wc;
           const float x0 = __uint_as_float(static_cast<uint32_t>(col[0]) << 16);
-          const float x1 = __uint_as_float(static_cast<uint32_t>(col[kQcPitch]) << 16);
-          const float x2 = __uint_as_float(static_cast<uint32_t>(col[2 * kQcPitch]) << 16);
-          const float x3 = __uint_as_float(static_cast<uint32_t>(col[3 * kQcPitch]) << 16);
+          const float x1 = __uint_as_float(static_cast<uint32_t>(col[S::PITCH]) << 16);
+          const float x2 = __uint_as_float(static_cast<uint32_t>(col[2 * S::PITCH]) << 16);
+          const float x3 = __uint_as_float(static_cast<uint32_t>(col[3 * S::PITCH]) << 16);
           w[i] = q2(x0, x1, sc) | (q2(x2, x3, sc) << 16);
         }
         uint4* dst = reinterpret_cast<uint4*>(q + orow * K + kk);
@@ -362,14 +377,32 @@ cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, l
   return launched();
 }
 
+// Slab width of the weight quantiser.  Measured on GB300 (Mixtral-8x7B-shaped
+// weights, E = 8): W2 (K = 14336) took 0.59-0.60 ms with 32-column slabs
+// against 0.64 with 64; W1 and W3 (K = 4096) took 0.52 with 64 against 0.56
+// with 32.  MOE_QC_COLS=32 or =64 forces one width (for measurement).
+int qc_cols(int K) {
+  static const int forced = [] {
+    const char* e = getenv("MOE_QC_COLS");
+    return e ? atoi(e) : 0;
+  }();
+  if (forced == 32 || forced == 64) return forced;
+  return K > 8192 ? 32 : 64;
+}
+
 cudaError_t launch_quant_cols(const uint16_t* W, int E, int K, int N, int rows_per_e,
                               int group_stride, int slot, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s) {
   if (E == 0 || K == 0 || N == 0) return cudaSuccess;
-  const int slabs = E * ((N + kQcCols - 1) / kQcCols);
+  const int qc = qc_cols(K);
+  const int slabs = E * ((N + qc - 1) / qc);
   const int grid = slabs < 2 * num_sms ? slabs : 2 * num_sms;  // two blocks per SM
-  quant_cols_kernel<<<grid, kQcThreads, 0, s>>>(W, E, K, N, rows_per_e, group_stride, slot, q,
-                                                scale);
+  if (qc == 32)
+    quant_cols_kernel<32><<<grid, kQcThreads, 0, s>>>(W, E, K, N, rows_per_e, group_stride,
+                                                      slot, q, scale);
+  else
+    quant_cols_kernel<64><<<grid, kQcThreads, 0, s>>>(W, E, K, N, rows_per_e, group_stride,
+                                                      slot, q, scale);
   return launched();
 }
 

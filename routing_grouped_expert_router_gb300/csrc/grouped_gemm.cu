@@ -844,9 +844,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // [128 r, 128 r + 128) in its own shared memory; the even CTA's single issuer
 // thread runs the MMAs for both, and each CTA's TMEM holds its 128 rows of the
 // 256-column accumulator.  Per SM this halves the B bytes staged and read per
-// MAC (a 32 KiB stage feeds 128 x 256 x 64 MACs instead of 48 KiB), which is
-// what lets the tensor pipe run close to its peak rather than at the shared-
-// memory bandwidth limit of a one-SM 128 x 256 tile.
+// MAC (a 32 KiB stage feeds 128 x 256 x 64 MACs instead of 48 KiB), so the
+// same ring of stages covers more MMA time.  Measured on GB300, the pair is
+// 1-3.5% faster than the one-CTA kernel on every matmul but FC1 forward (see
+// pair_for below).
 // Synchronisation: the even CTA's `full` barrier counts both CTAs' bytes: its
 // own loads signal it directly, and the odd CTA's loads signal it across the
 // pair (TMA .cta_group::2).  The exception is the last K block of a wgrad tile

@@ -64,8 +64,11 @@ def _quant_weights(d, dev):
     return qw
 
 
-def test_weight_codes_and_scales_bit_exact(lib):
-    cfg = small_config(name="wq", T=8, h=384, f=640, E=3, k=2, seed=21)
+# f = 8320: W2's contraction dimension is above 8192, where the weight
+# quantiser switches from 64- to 32-column slabs
+@pytest.mark.parametrize("f", [640, 8320])
+def test_weight_codes_and_scales_bit_exact(lib, f):
+    cfg = small_config(name="wq", T=8, h=384, f=f, E=3, k=2, seed=21)
     inp = conditioned_inputs(cfg)
     d = mb.dims_of(cfg, has_bias=False)
     qw = _quant_weights(d, _to(inp, "cuda"))
