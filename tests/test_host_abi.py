@@ -47,6 +47,10 @@ def _d(**kw):
     (dict(k=5, E=4), mb.MOE_ERR_INVALID_ARG),
     (dict(E=65), mb.MOE_ERR_UNSUPPORTED),
     (dict(h=100), mb.MOE_ERR_UNSUPPORTED),
+    # h = 8 meets the ABI's h % 8 == 0, but the matmuls' 64-wide K blocks need
+    # h and h_ffn to be multiples of 64: declined, not computed wrongly
+    (dict(h=8), mb.MOE_ERR_UNSUPPORTED),
+    (dict(h=32), mb.MOE_ERR_UNSUPPORTED),
     (dict(f=72), mb.MOE_ERR_UNSUPPORTED),
     (dict(T=-1), mb.MOE_ERR_INVALID_ARG),
     (dict(T=1 << 29, k=8), mb.MOE_ERR_UNSUPPORTED),
