@@ -1,9 +1,10 @@
 """The benchmark's roofline bookkeeping on CPU: the DRAM traffic it reports
-per GroupedGEMM comes from the committed one-pass ncu summary, only for the
-workload and the GEMM sources that summary was captured from, and each figure
-is at least about the matmul's algorithmic bytes (every operand read once and
-every output written once)."""
-import re
+per GroupedGEMM comes from the committed one-pass ncu summary
+(profiles/dram_traffic_gemms.json), only for the workload and the GEMM sources
+that summary was captured from; each figure is the captured launch's bytes
+times the summary's stated scale, and at least about the matmul's algorithmic
+bytes (every operand read once and every output written once)."""
+import json
 
 import pytest
 
@@ -16,8 +17,7 @@ GEMMS = ("gg_fc1_fwd_swiglu", "gg_fc2_fwd", "gg_fc2_dgrad_swiglu_bwd", "gg_fc2_w
 
 def _recorded():
     with open(bench.TRAFFIC_PROFILE) as f:
-        text = f.read()
-    return dict(re.findall(r"^    ([\w.]+): (.+)$", text, re.M))
+        return json.load(f)
 
 
 def _algorithmic_bytes(cfg):
@@ -36,17 +36,21 @@ def _algorithmic_bytes(cfg):
 
 
 def test_summary_is_for_the_bench_workload():
-    assert _recorded()["workload"] == bench.workload_desc(CONFIGS["mixtral8x7b"])
+    rec = _recorded()
+    assert rec["workload"] == bench.workload_desc(CONFIGS["mixtral8x7b"])
+    assert set(GEMMS) <= set(rec["kernels"])
 
 
-def test_traffic_reported_for_the_recorded_sources(monkeypatch):
+def test_traffic_is_the_capture_scaled(monkeypatch):
     rec = _recorded()
     monkeypatch.setattr(bench, "gemm_source_hash", lambda: rec["source_sha256"])
     cfg = CONFIGS["mixtral8x7b"]
     alg = _algorithmic_bytes(cfg)
     for name in GEMMS:
+        ent = rec["kernels"][name]
         t = bench.measured_traffic(name, bench.workload_desc(cfg))
-        assert t == float(rec["dram_bytes_per_launch." + name])
+        assert t == pytest.approx(rec["scale"] * (ent["captured_read_bytes"]
+                                                  + ent["captured_write_bytes"]))
         # part of a kernel's output can still sit in L2 when it ends
         assert 0.95 * alg[name] <= t <= 5.0 * alg[name], name
 
@@ -80,3 +84,12 @@ def test_source_hash_covers_the_gemm_sources(tmp_path, monkeypatch):
 def test_job_throughput_counts_every_rank(tokens, ranks, steps, ms):
     assert bench.job_tokens_per_s(tokens, ranks, steps, ms) == pytest.approx(
         tokens * ranks * steps / (ms / 1e3))
+
+
+def test_oracle_leg_times_a_calibrated_sample():
+    """The CPU legs time the C++ oracle on a sample sized by a calibration run."""
+    import dataclasses
+    cfg = dataclasses.replace(CONFIGS["tiny"], T=64)
+    tps, n, dt, threads = bench.time_oracle(cfg, 0.05, 2, 1)
+    assert 8 <= n <= 64 and dt > 0 and threads >= 1
+    assert tps == pytest.approx(n * 2 / dt)

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.cref as ref
 from routing_grouped_expert_router_gb300 import binding as mb
 from routing_grouped_expert_router_gb300 import build as mbuild
 from tests.gpu_runner import LayerRun, workspace
@@ -53,9 +54,9 @@ def _case(name):
 @pytest.mark.parametrize("name", list(CASES))
 def test_layer_with_capacity_matches_oracle(lib, name):
     cfg, inp, cap = _case(name)
-    y, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
+    y, ctx = ref.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
                               cfg.k, capacity=cap)
-    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    g = ref.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
     n = int(ctx["offsets"][-1])
     if name != "cap_above_max":
         assert n < cfg.T * cfg.k, "the case must drop assignments"
@@ -124,13 +125,13 @@ def _local(d, idx, lo, hi, x, R, h):
 def test_permute_local_matches_oracle(lib, E, k, ranges, cap):
     cfg = small_config(name="local", T=900, h=128, f=128, E=E, k=k, seed=40 + E)
     inp = conditioned_inputs(cfg)
-    idx_np, _, _ = oracle.route(inp["x"], inp["Wg"], inp["b"], k)
+    idx_np, _, _ = ref.route(inp["x"], inp["Wg"], inp["b"], k)
     d = mb.dims_of(cfg, has_bias=False, capacity=cap)
     R = cfg.T * k
     idx = torch.from_numpy(np.ascontiguousarray(idx_np, dtype=np.int32)).cuda()
     x = inp["x"].cuda()
     for lo, hi in ranges:
-        counts, offsets, psrc, pdst = oracle.dispatch(idx_np, E, cap or None, (lo, hi))
+        counts, offsets, psrc, pdst = ref.dispatch(idx_np, E, cap or None, (lo, hi))
         g = _local(d, idx, lo, hi, x, R, cfg.h)
         torch.cuda.synchronize()
         n = int(offsets[-1])
@@ -139,7 +140,7 @@ def test_permute_local_matches_oracle(lib, E, k, ranges, cap):
         np.testing.assert_array_equal(g[2].cpu().numpy()[:n], psrc)
         np.testing.assert_array_equal(g[3].cpu().numpy(), pdst)
         np.testing.assert_array_equal(g[4][:n].cpu().double().numpy(),
-                                      oracle.permute_rows(oracle.as_f64(inp["x"]), psrc, k))
+                                      ref.permute_rows(oracle.as_f64(inp["x"]), psrc, k))
         # rows past the placed ones are left alone
         assert torch.all(g[4][n:] == 0)
 
@@ -149,7 +150,7 @@ def test_local_expert_ranges_sum_to_layer(lib):
     combine on each range; the partials summed in fp32 match the oracle."""
     cfg = small_config(name="local_sum", T=1024, h=256, f=512, E=8, k=4, seed=77)
     inp = conditioned_inputs(cfg)
-    y_ref, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
+    y_ref, ctx = ref.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
                                   inp["W2"], cfg.k)
     dev = _to(inp, "cuda")
     T, h, f, k = cfg.T, cfg.h, cfg.f, cfg.k
@@ -176,7 +177,7 @@ def test_local_expert_ranges_sum_to_layer(lib):
 def test_noalloc_with_capacity_equals_permute(lib):
     cfg = small_config(name="na", T=2000, h=64, f=64, E=16, k=2, seed=13)
     inp = conditioned_inputs(cfg)
-    idx_np, _, _ = oracle.route(inp["x"], inp["Wg"], inp["b"], cfg.k)
+    idx_np, _, _ = ref.route(inp["x"], inp["Wg"], inp["b"], cfg.k)
     cap = mb.capacity_for(cfg.T, cfg.k, cfg.E, 0.9)
     d = mb.dims_of(cfg, has_bias=False, capacity=cap)
     R = cfg.T * cfg.k
@@ -188,7 +189,7 @@ def test_noalloc_with_capacity_equals_permute(lib):
     mb.moe_permute(d, idx, None, *a, None, workspace(d, mb.OP_PERMUTE))
     mb.moe_permute_noalloc(d, idx, None, *b, None)
     torch.cuda.synchronize()
-    counts, offsets, psrc, pdst = oracle.dispatch(idx_np, cfg.E, cap)
+    counts, offsets, psrc, pdst = ref.dispatch(idx_np, cfg.E, cap)
     n = int(offsets[-1])
     assert n < R
     for got in (a, b):

@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.cref as ref
 from routing_grouped_expert_router_gb300 import binding as mb
 from routing_grouped_expert_router_gb300 import build as mbuild
 from tests.gpu_runner import LayerRun, workspace
@@ -47,7 +48,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(lib):
     assert mb.moe_read_device_status(ws) == mb.MOE_OK        # reading cleared it
     # the context is intact: a layer runs and matches the oracle
     cfg, inp, dev = _inputs()
-    y_ref, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
+    y_ref, ctx = ref.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
                                   inp["W2"], cfg.k)
     run = LayerRun(mb.dims_of(cfg, has_bias=False))
     run.fwd(dev)

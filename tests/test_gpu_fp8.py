@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.cref as ref
 from routing_grouped_expert_router_gb300 import binding as mb
 from routing_grouped_expert_router_gb300 import build as mbuild
 from tests.gpu_runner import LayerRun, workspace
@@ -74,9 +75,9 @@ def test_weight_codes_and_scales_bit_exact(lib, f):
     qw = _quant_weights(d, _to(inp, "cuda"))
     torch.cuda.synchronize()
     E, h, f = cfg.E, cfg.h, cfg.f
-    W1q, s1 = oracle.quantize_cols_e4m3(oracle.as_f64(inp["W1"]))
-    W3q, s3 = oracle.quantize_cols_e4m3(oracle.as_f64(inp["W3"]))
-    W2q, s2 = oracle.quantize_cols_e4m3(oracle.as_f64(inp["W2"]))
+    W1q, s1 = ref.quantize_cols_e4m3(oracle.as_f64(inp["W1"]))
+    W3q, s3 = ref.quantize_cols_e4m3(oracle.as_f64(inp["W3"]))
+    W2q, s2 = ref.quantize_cols_e4m3(oracle.as_f64(inp["W2"]))
     np.testing.assert_array_equal(_view(d, qw, "s1", (E, f), torch.float32).cpu().numpy(), s1)
     np.testing.assert_array_equal(_view(d, qw, "s3", (E, f), torch.float32).cpu().numpy(), s3)
     np.testing.assert_array_equal(_view(d, qw, "s2", (E, h), torch.float32).cpu().numpy(), s2)
@@ -94,7 +95,7 @@ def test_row_codes_and_scales_bit_exact(lib, h):
     cfg = small_config(name="xq", T=333, h=h, f=128, E=8, k=2, seed=22)
     inp = conditioned_inputs(cfg)
     inp["x"][17] = 0                               # a zero row: scale 1, codes 0
-    _, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
+    _, ctx = ref.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
                               cfg.k)
     R = cfg.T * cfg.k
     q = torch.empty(R, cfg.h, dtype=torch.uint8, device="cuda")
@@ -102,7 +103,7 @@ def test_row_codes_and_scales_bit_exact(lib, h):
     psrc = torch.from_numpy(ctx["perm_src"]).cuda()
     mb.moe_quantize_rows_fp8(inp["x"].cuda(), R, cfg.h, psrc, cfg.k, cfg.T, q, sc)
     torch.cuda.synchronize()
-    Xq, sx = oracle.quantize_rows_e4m3(ctx["x_perm"])
+    Xq, sx = ref.quantize_rows_e4m3(ctx["x_perm"])
     np.testing.assert_array_equal(sc.cpu().numpy(), sx)
     np.testing.assert_array_equal(_codes(q), Xq)
     assert np.sum(sx == 1.0) == cfg.k
@@ -112,9 +113,9 @@ def test_row_codes_and_scales_bit_exact(lib, h):
 def test_fp8_layer_matches_fp8_oracle(lib, name):
     cfg = small_config(name=name, **CASES[name])
     inp = conditioned_inputs(cfg)
-    y, ctx = oracle.layer_fwd_fp8(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
+    y, ctx = ref.layer_fwd_fp8(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
                                   inp["W2"], cfg.k)
-    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    g = ref.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
     dev = _to(inp, "cuda")
     d = mb.dims_of(cfg, has_bias=cfg.zipf_s > 0)
     qw = _quant_weights(d, dev)
@@ -141,9 +142,9 @@ def test_fp8_layer_with_capacity(lib):
     cfg = small_config(name="fp8_cap", T=1024, h=512, f=1024, E=8, k=2, seed=2)
     inp = conditioned_inputs(cfg)
     cap = mb.capacity_for(cfg.T, cfg.k, cfg.E, 1.0)
-    y, ctx = oracle.layer_fwd_fp8(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
+    y, ctx = ref.layer_fwd_fp8(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"],
                                   inp["W2"], cfg.k, capacity=cap)
-    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    g = ref.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
     assert int(ctx["offsets"][-1]) < cfg.T * cfg.k
     dev = _to(inp, "cuda")
     d = mb.dims_of(cfg, has_bias=False, capacity=cap)
@@ -191,8 +192,8 @@ def test_fp8_fullsize_sampled(lib):
     torch.cuda.synchronize()
     assert mb.moe_read_device_status(ws) == mb.MOE_OK and run.status() == mb.MOE_OK
 
-    idx, gates, _ = oracle.route(x_cpu, inp["Wg"].cpu(), inp["b"].cpu(), k)
-    counts, offsets, psrc, pdst = oracle.dispatch(idx, E)
+    idx, gates, _ = ref.route(x_cpu, inp["Wg"].cpu(), inp["b"].cpu(), k)
+    counts, offsets, psrc, pdst = ref.dispatch(idx, E)
     np.testing.assert_array_equal(run.saved_view("topk_idx").cpu().numpy(), idx)
     np.testing.assert_array_equal(run.saved_view("perm_src").cpu().numpy(), psrc)
 
@@ -212,7 +213,7 @@ def test_fp8_fullsize_sampled(lib):
     for e in pair:
         rows = [(int(t), j) for t in toks for j in range(k) if idx[t, j] == e]
         X = x64[[t for t, _ in rows]]
-        f8 = oracle.expert_ffn_fwd_fp8(X, np.array([0, len(rows)]), inp["W1"][e:e + 1].cpu(),
+        f8 = ref.expert_ffn_fwd_fp8(X, np.array([0, len(rows)]), inp["W1"][e:e + 1].cpu(),
                                        inp["W3"][e:e + 1].cpu(), inp["W2"][e:e + 1].cpu())
         # the expert's quantised weights, every code and scale
         np.testing.assert_array_equal(s1v[e], f8["s1"][0])
@@ -257,7 +258,7 @@ def test_bwd_weight_codes_and_scales_bit_exact(lib, f):
     W3r = _codes(_bview(d, qwb, "W3r", (E, h, f), torch.uint8))
     s13r = _bview(d, qwb, "s13r", (E, h), torch.float32).cpu().numpy()
     for e in range(E):
-        q1, q3, s13 = oracle.quantize_rows_joint_e4m3(oracle.as_f64(inp["W1"][e]),
+        q1, q3, s13 = ref.quantize_rows_joint_e4m3(oracle.as_f64(inp["W1"][e]),
                                                       oracle.as_f64(inp["W3"][e]))
         np.testing.assert_array_equal(W1r[e], q1)
         np.testing.assert_array_equal(W3r[e], q3)
@@ -271,9 +272,9 @@ def test_bwd_weight_codes_and_scales_bit_exact(lib, f):
 def test_fp8_backward_matches_fp8_oracle(lib, name, fwd8):
     cfg = small_config(name=name, **CASES[name])
     inp = conditioned_inputs(cfg)
-    fwd = oracle.layer_fwd_fp8 if fwd8 else oracle.layer_fwd
+    fwd = ref.layer_fwd_fp8 if fwd8 else ref.layer_fwd
     y, ctx = fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"], cfg.k)
-    g = oracle.layer_bwd_fp8(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    g = ref.layer_bwd_fp8(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
     dev = _to(inp, "cuda")
     d = mb.dims_of(cfg, has_bias=cfg.zipf_s > 0)
     run = LayerRun(d)

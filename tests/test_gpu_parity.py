@@ -12,6 +12,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.cref as ref
 from routing_grouped_expert_router_gb300 import binding as mb
 from routing_grouped_expert_router_gb300 import build as mbuild
 from routing_grouped_expert_router_gb300 import synth
@@ -64,9 +65,9 @@ def _to(inp, device):
 
 
 def _oracle(cfg, inp):
-    y, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
+    y, ctx = ref.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
                               cfg.k)
-    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    g = ref.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
     return y, ctx, g
 
 
@@ -222,7 +223,7 @@ def test_stage_entry_points(lib, name):
     g32 = torch.from_numpy(ctx["gates"]).float()
     y_syn = torch.empty(T, h, dtype=torch.bfloat16, device="cuda")
     mb.moe_combine(d, O_syn.cuda(), g32.cuda(), torch.from_numpy(ctx["perm_dst"]).cuda(), y_syn)
-    y_ref = oracle.combine(oracle.as_f64(O_syn), g32.double().numpy(), ctx["perm_dst"], T, k)
+    y_ref = ref.combine(oracle.as_f64(O_syn), g32.double().numpy(), ctx["perm_dst"], T, k)
     assert rel_l2(y_syn.cpu().double().numpy(), y_ref) <= 3e-3
 
     # expert FFN backward from the oracle's activations (rounded to bf16)

@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.cref as ref
 from routing_grouped_expert_router_gb300 import binding as mb
 from routing_grouped_expert_router_gb300 import build as mbuild
 from routing_grouped_expert_router_gb300 import synth
@@ -60,9 +61,9 @@ def test_sar_layer_matches_oracle(lib, name):
     shape, cap = CASES[name]
     cfg = small_config(name=name, **shape)
     inp = conditioned_inputs(cfg)
-    y, ctx = oracle.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
+    y, ctx = ref.layer_fwd(inp["x"], inp["Wg"], inp["b"], inp["W1"], inp["W3"], inp["W2"],
                               cfg.k, capacity=cap or None)
-    g = oracle.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    g = ref.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
     dev = _to(inp, "cuda")
     hb = cfg.zipf_s > 0
     out = _run(mb.dims_of(cfg, has_bias=hb, capacity=cap, sar=True), dev)
@@ -84,9 +85,9 @@ def test_sar_layer_matches_oracle(lib, name):
     for e in np.nonzero(ctx["counts"] == 0)[0]:
         assert torch.all(out["dW1"][e] == 0) and torch.all(out["dW2"][e] == 0)
     # same forward kernels as the default mode: y is bitwise the same
-    ref = _run(mb.dims_of(cfg, has_bias=hb, capacity=cap), dev)
-    assert torch.equal(out["y"].view(torch.int16), ref["y"].view(torch.int16))
-    assert torch.equal(out["A"].view(torch.int16), ref["A"].view(torch.int16))
+    base = _run(mb.dims_of(cfg, has_bias=hb, capacity=cap), dev)
+    assert torch.equal(out["y"].view(torch.int16), base["y"].view(torch.int16))
+    assert torch.equal(out["A"].view(torch.int16), base["A"].view(torch.int16))
 
 
 def test_sar_deterministic_and_empty(lib):
