@@ -50,7 +50,18 @@
  *     a status; nothing is launched then.  CUDA launch errors return
  *     MOE_ERR_CUDA.  Device code never traps or prints: a kernel whose bounded
  *     wait runs out records MOE_ERR_DEVICE_TIMEOUT in the status word at the
- *     start of `ws` and returns; moe_read_device_status() reports it.
+ *     start of `ws` and returns; moe_read_device_status() reports it.  A
+ *     kernel that reads an index from device memory (an expert id in
+ *     topk_idx, an entry of perm_src or perm_dst, an expert offset handed in
+ *     by the caller) checks it: one out of range is recorded as
+ *     MOE_ERR_DEVICE_INDEX in the same status word and that element is
+ *     skipped (an assignment not placed, a zero row, a slot that adds
+ *     nothing), so nothing is read or written out of bounds.  The calls that
+ *     take no workspace (moe_combine, moe_unpermute, moe_quantize_rows_fp8,
+ *     moe_permute_noalloc) record into one status word per device that the
+ *     library keeps (its address is looked up on the first such call on a
+ *     device and kept until the process exits); moe_read_device_status(NULL,
+ *     stream) reports that one.
  *   - Supported shapes: 1 <= k <= 8, E <= 64, T*k < 2^31, h and f multiples
  *     of 64 (the GEMMs' K blocks are 64 wide).  Calls that choose experts
  *     (moe_route, moe_layer_fwd/bwd, moe_saved_bytes) also need k <= E; the
@@ -76,7 +87,8 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,     /* shape outside the supported set */
   MOE_ERR_WORKSPACE = 3,       /* ws_bytes smaller than required */
   MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
-  MOE_ERR_DEVICE_TIMEOUT = 5   /* a kernel's bounded wait ran out */
+  MOE_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out */
+  MOE_ERR_DEVICE_INDEX = 6     /* an index read on the device was out of range */
 } moe_status;
 
 typedef struct {
@@ -101,6 +113,14 @@ typedef enum {
   MOE_OP_LAYER_FWD_FP8 = 7,
   MOE_OP_LAYER_BWD_FP8 = 8
 } moe_op;
+
+/* Per-expert capacity for a capacity factor: ceil(factor * T * k / E), the
+ * share of the T*k assignments an expert gets under perfect balance times the
+ * factor (the digest's per-GPU token dropping for load balance, §3.2 after
+ * Figure 7; the factor is the usual way to size it).  Returns the value for
+ * dims.capacity, or -1 when T < 0, k < 1, E < 1, factor <= 0 or the result
+ * does not fit an int32. */
+int32_t moe_capacity_for(int32_t T, int32_t k, int32_t E, double factor);
 
 /* Scratch bytes entry point `op` needs for `dims` (0 on invalid dims).  The
  * first 256 bytes of every workspace hold the device status word; zero the
@@ -154,8 +174,12 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx,
  * in the library's device memory (held by every GPU that loads the library
  * until exit), so it supports ceil(T*k / 1024) * E <= 131072 and returns
  * MOE_ERR_UNSUPPORTED beyond that.  The first call on a device looks up the
- * array's device address; make it before any stream capture.  All calls
- * share the array: calls that overlap on the GPU race.  Allocates nothing. */
+ * array's device address; make it before any stream capture.  The address is
+ * kept for the life of the process: after a cudaDeviceReset, restart the
+ * process before calling this again.  All calls share the array: calls that
+ * overlap on the GPU race.  Index errors (an expert id out of range) go to the
+ * per-device status word of the calls without a workspace.  Allocates
+ * nothing. */
 moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* topk_idx,
                                const moe_bf16* x, int32_t* counts,
                                int32_t* offsets, int32_t* perm_src,
@@ -182,7 +206,12 @@ moe_status moe_permute_local(const moe_dims* dims, const int32_t* topk_idx,
                              moe_stream_t stream);
 
 /* Inverse row move: rows_assign[a] = rows_perm[perm_dst[a]] for a < T*k, a
- * zero row where perm_dst[a] = -1.  rows_perm, rows_assign: [T*k, h] bf16. */
+ * zero row where perm_dst[a] = -1.  rows_perm, rows_assign: [T*k, h] bf16.
+ * It undoes the expert-major order of the dispatch (digest §3.3: token copies
+ * sorted by expert, then by source), taking rows back to assignment order
+ * a = t*k + j.  A perm_dst entry >= T*k gives a zero row and is recorded as
+ * MOE_ERR_DEVICE_INDEX in the per-device status word (no workspace; see
+ * moe_read_device_status). */
 moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst,
                          const moe_bf16* rows_perm, moe_bf16* rows_assign,
                          moe_stream_t stream);
@@ -358,10 +387,14 @@ void* moe_saved_view(const moe_dims* dims, void* saved, const char* name);
 const char* moe_status_string(moe_status status);
 
 /* Synchronises `stream`, returns the status word at the start of `ws` and
- * clears it.  MOE_ERR_CUDA if the synchronisation itself failed. */
+ * clears it.  ws = NULL: the status word of the calls that take no workspace
+ * (moe_combine, moe_unpermute, moe_quantize_rows_fp8, moe_permute_noalloc) on
+ * the current device.
+ * MOE_ERR_CUDA if the synchronisation itself failed. */
 moe_status moe_read_device_status(void* ws, moe_stream_t stream);
 
-/* Zeroes the status word at the start of `ws` (asynchronous). */
+/* Zeroes the status word at the start of `ws` (asynchronous); ws = NULL: the
+ * current device's status word of the calls without a workspace. */
 moe_status moe_clear_device_status(void* ws, moe_stream_t stream);
 
 /* Failure-path self test: launches one thread that waits on an mbarrier

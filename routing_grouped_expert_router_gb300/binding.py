@@ -9,7 +9,6 @@ library is absent: there is no fallback path.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import re
 
@@ -21,6 +20,7 @@ MOE_ERR_UNSUPPORTED = 2
 MOE_ERR_WORKSPACE = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
+MOE_ERR_DEVICE_INDEX = 6
 
 OP_ROUTE, OP_PERMUTE, OP_EXPERT_FFN_FWD, OP_EXPERT_FFN_BWD, OP_ROUTER_BWD, \
     OP_LAYER_FWD, OP_LAYER_BWD, OP_LAYER_FWD_FP8, OP_LAYER_BWD_FP8 = range(9)
@@ -51,9 +51,11 @@ def dims_of(cfg, has_bias=None, capacity=0, sar=False) -> moe_dims:
 
 
 def capacity_for(T, k, E, factor: float) -> int:
-    """Per-expert capacity ceil(factor * T * k / E): factor 1.0 is the share an
-    expert gets under perfect balance."""
-    return int(math.ceil(factor * T * k / E))
+    """moe_capacity_for: the per-expert capacity for a capacity factor."""
+    c = load().moe_capacity_for(int(T), int(k), int(E), float(factor))
+    if c < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_capacity_for")
+    return int(c)
 
 
 _LIB = None
@@ -96,6 +98,8 @@ _SIGS = {
     "moe_fp8_bwd_weight_view": (_P, [_D, _P, ctypes.c_char_p]),
     "moe_layer_bwd_fp8": (_I, [_D] + [_P] * 11 + [_P, _SZ, _P]),
     "moe_version": (ctypes.c_char_p, []),
+    "moe_capacity_for": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_double]),
 }
 
 

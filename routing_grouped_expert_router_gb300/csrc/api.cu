@@ -6,11 +6,14 @@
 // synchronises except moe_read_device_status.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 
 #include "../../include/moe.h"
+#include "api_internal.h"
 #include "grouped_gemm.cuh"
 #include "kernels.cuh"
 
@@ -67,16 +70,16 @@ bool routed_op(int op) {
 
 
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 // ------------------------------------------------------------- layouts
@@ -183,7 +186,7 @@ WsLayout ws_layout(const moe_dims& d, int op) {
   auto router_bwd = [&] {
     L.dl = c.take(static_cast<size_t>(d.T) * d.E * 4);
     L.WgT = c.take(static_cast<size_t>(d.E) * d.h * 4);
-    L.partial = c.take(static_cast<size_t>(moe::wgrad_router_chunks(d.T)) * d.h * d.E * 4);
+    L.partial = c.take(static_cast<size_t>(moe::wgrad_router_chunks(d.T, d.h, d.E)) * d.h * d.E * 4);
   };
   auto expert_bwd = [&](bool with_x) {
     if (with_x) L.x_perm = c.take(R * d.h * 2);
@@ -275,6 +278,16 @@ GemmProblem problem(const moe_dims& d, const int32_t* offsets, void* ws) {
   return p;
 }
 
+}  // namespace
+
+namespace moe_api {
+moe_status check_dims(const moe_dims* d, bool routed) { return ::check_dims(d, routed); }
+int num_sms() { return ::num_sms(); }
+bool note(cudaStream_t s, const char* name) { return ::note(s, name); }
+}  // namespace moe_api
+
+namespace {
+
 // --------------------------------------------------------- the steps
 moe_status do_route(const moe_dims& d, const uint16_t* x, const float* Wg, const float* b,
                     int32_t* idx, float* gates, void* ws, const WsLayout& L, cudaStream_t stream) {
@@ -297,10 +310,12 @@ moe_status do_dispatch(const moe_dims& d, const moe::DispatchSel& sel, const int
   const int nblk = moe::dispatch_blocks(R);
   int32_t* blk = at<int32_t>(ws, L.blk_counts);
   int32_t* bases = at<int32_t>(ws, L.bases);
-  MOE_RUN(moe::launch_dispatch_hist(idx, R, d.E, sel, blk, stream), "dispatch_hist");
+  int* status = at<int>(ws, 0);
+  MOE_RUN(moe::launch_dispatch_hist(idx, R, d.E, sel, blk, stream, status), "dispatch_hist");
   MOE_RUN(moe::launch_dispatch_scan(blk, nblk, sel, counts, offsets, bases, stream),
           "dispatch_scan");
-  MOE_RUN(moe::launch_dispatch_scatter(idx, R, d.E, sel, bases, offsets, psrc, pdst, stream),
+  MOE_RUN(moe::launch_dispatch_scatter(idx, R, d.E, sel, bases, offsets, psrc, pdst, stream,
+                                       status),
           "dispatch_scatter");
   return MOE_OK;
 }
@@ -353,10 +368,12 @@ moe_status do_ffn_bwd_sar(const moe_dims& d, const uint16_t* x, const uint16_t* 
   float* grow = at<float>(ws, L.gate_rows);
   float* part = at<float>(ws, L.dg_part);
   const int32_t* nvalid = offsets + d.E;
-  MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, R, d.T, d.h, xp, num_sms(), stream, nvalid),
+  int* status = at<int>(ws, 0);
+  MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, R, d.T, d.h, xp, num_sms(), stream, nvalid,
+                                  nullptr, nullptr, status),
           "permute_rows");
   MOE_RUN(moe::launch_gather_rows(dy, psrc, d.k, R, d.T, d.h, dyp, num_sms(), stream, nvalid,
-                                  gates, grow),
+                                  gates, grow, status),
           "permute_dy");
   if (R == 0) {
     const size_t wbytes = static_cast<size_t>(d.E) * d.h * d.f * 4;
@@ -372,7 +389,7 @@ moe_status do_ffn_bwd_sar(const moe_dims& d, const uint16_t* x, const uint16_t* 
   MOE_RUN(moe::gemm_fc1_dgrad(g, dA, dB, W1, W3, dX, stream), moe::kGemmNames[3]);
   MOE_RUN(moe::gemm_fc1_wgrad(g, xp, dA, dB, dW1, dW3, stream), moe::kGemmNames[5]);
   MOE_RUN(moe::launch_dg_reduce(part, moe::gemm_col_tiles(d.f), psrc, R, nvalid, dg, num_sms(),
-                                stream),
+                                stream, status),
           "dg_reduce");
   return MOE_OK;
 }
@@ -386,7 +403,7 @@ moe_status do_router_bwd(const moe_dims& d, const uint16_t* x, const float* Wg,
   float* partial = at<float>(ws, L.partial);
   MOE_RUN(moe::launch_transpose_wg(Wg, d.h, d.E, WgT, stream), "transpose_wg");
   MOE_RUN(moe::launch_token_grad(dX, pdst, idx, gates, dg, WgT, d.T, d.k, d.h, d.E, dl, dx,
-                                 num_sms(), stream),
+                                 num_sms(), stream, at<int>(ws, 0)),
           "token_grad");
   MOE_RUN(moe::launch_router_wgrad(x, dl, d.T, d.h, d.E, partial, dWg, stream), "router_wgrad");
   return MOE_OK;
@@ -405,8 +422,18 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace smaller than required";
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
     case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+    case MOE_ERR_DEVICE_INDEX:
+      return "MOE_ERR_DEVICE_INDEX: an expert id, permutation entry or offset read on the device "
+             "was out of range (the element was skipped)";
   }
   return "unknown moe_status";
+}
+
+int32_t moe_capacity_for(int32_t T, int32_t k, int32_t E, double factor) {
+  if (T < 0 || k < 1 || E < 1 || !(factor > 0.0)) return -1;
+  const double c = std::ceil(factor * static_cast<double>(T) * k / E);
+  if (!(c < 2147483647.0)) return -1;
+  return static_cast<int32_t>(c);
 }
 
 const char* moe_version(void) { return "libmoe_gb300 0.1 (sm_103a, tcgen05 GroupedGEMM)"; }
@@ -452,12 +479,14 @@ const char* moe_profile_kernel_name(int i) {
 }
 
 moe_status moe_read_device_status(void* ws, moe_stream_t stream) {
-  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (ws && !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  int* word = ws ? static_cast<int*>(ws) : moe::nows_status_word();
+  if (!word) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int v = 0;
   MOE_CU(cudaStreamSynchronize(s));
-  MOE_CU(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost));
-  MOE_CU(cudaMemset(ws, 0, sizeof(int)));
+  MOE_CU(cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost));
+  MOE_CU(cudaMemset(word, 0, sizeof(int)));
   return static_cast<moe_status>(v);
 }
 
@@ -470,8 +499,10 @@ moe_status moe_selftest_wait_timeout(void* ws, uint32_t limit_us, moe_stream_t s
 }
 
 moe_status moe_clear_device_status(void* ws, moe_stream_t stream) {
-  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
-  MOE_CU(cudaMemsetAsync(ws, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)));
+  if (ws && !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  int* word = ws ? static_cast<int*>(ws) : moe::nows_status_word();
+  if (!word) return MOE_ERR_CUDA;
+  MOE_CU(cudaMemsetAsync(word, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 
@@ -509,7 +540,8 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const moe_
     return st;
   if (x && x_perm)
     MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(rows_of(d)), d.T,
-                                    d.h, x_perm, num_sms(), stream, offsets + d.E),
+                                    d.h, x_perm, num_sms(), stream, offsets + d.E, nullptr,
+                                    nullptr, at<int>(ws, 0)),
             "permute_rows");
   return MOE_OK;
 }
@@ -535,7 +567,8 @@ moe_status moe_permute_local(const moe_dims* dims, const int32_t* topk_idx, int3
     return st;
   if (x && x_perm)
     MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(R), d.T, d.h, x_perm,
-                                    num_sms(), stream, offsets + (e_hi - e_lo)),
+                                    num_sms(), stream, offsets + (e_hi - e_lo), nullptr, nullptr,
+                                    at<int>(ws, 0)),
             "permute_rows");
   return MOE_OK;
 }
@@ -549,9 +582,11 @@ moe_status moe_unpermute(const moe_dims* dims, const int32_t* perm_dst, const mo
   if (!buf_ok(perm_dst, R) || !buf_ok(rows_perm, R) || !buf_ok(rows_assign, R))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int* status = moe::nows_status_word();
+  if (!status) return MOE_ERR_CUDA;
   MOE_RUN(moe::launch_gather_rows(rows_perm, perm_dst, 1, static_cast<long long>(rows_of(d)),
                                   static_cast<long long>(rows_of(d)), d.h, rows_assign, num_sms(),
-                                  stream),
+                                  stream, nullptr, nullptr, nullptr, status),
           "unpermute_rows");
   return MOE_OK;
 }
@@ -571,8 +606,11 @@ moe_status moe_expert_ffn_fwd(const moe_dims* dims, const moe_bf16* x, const int
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const WsLayout L = ws_layout(d, MOE_OP_EXPERT_FFN_FWD);
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
+  int* status = at<int>(ws, 0);
+  MOE_RUN(moe::launch_check_offsets(offsets, d.E, static_cast<long long>(R), status, stream),
+          "check_offsets");
   MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, static_cast<long long>(rows_of(d)), d.T, d.h,
-                                  xp, num_sms(), stream, offsets + d.E),
+                                  xp, num_sms(), stream, offsets + d.E, nullptr, nullptr, status),
           "permute_rows");
   return do_ffn_fwd(d, xp, offsets, W1, W3, W2, A, B, H, O, ws, stream);
 }
@@ -586,7 +624,10 @@ moe_status moe_combine(const moe_dims* dims, const moe_bf16* O, const float* gat
   if (!buf_ok(O, R) || !buf_ok(gates, R) || !buf_ok(perm_dst, R) || !buf_ok(y, T))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  MOE_RUN(moe::launch_combine(O, gates, perm_dst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
+  int* status = moe::nows_status_word();
+  if (!status) return MOE_ERR_CUDA;
+  MOE_RUN(moe::launch_combine(O, gates, perm_dst, d.T, d.k, d.h, y, num_sms(), stream, status),
+          "combine");
   return MOE_OK;
 }
 
@@ -612,11 +653,13 @@ moe_status moe_expert_ffn_bwd(const moe_dims* dims, const moe_bf16* x, const moe
   uint16_t* xp = at<uint16_t>(ws, L.x_perm);
   uint16_t* dO = at<uint16_t>(ws, L.dO);
   const long long nrows = static_cast<long long>(R);
+  int* status = at<int>(ws, 0);
+  MOE_RUN(moe::launch_check_offsets(offsets, d.E, nrows, status, stream), "check_offsets");
   MOE_RUN(moe::launch_gather_rows(x, perm_src, d.k, nrows, d.T, d.h, xp, num_sms(), stream,
-                                  offsets + d.E),
+                                  offsets + d.E, nullptr, nullptr, status),
           "permute_rows");
   MOE_RUN(moe::launch_bwd_prep(dy, O, gates, perm_src, nrows, d.k, d.h, dO, dg, num_sms(), stream,
-                               offsets + d.E),
+                               offsets + d.E, status),
           "bwd_prep");
   return do_ffn_bwd(d, xp, dO, offsets, W1, W3, W2, A, B, H, at<uint16_t>(ws, L.dA),
                     at<uint16_t>(ws, L.dB), dX_perm, dW1, dW3, dW2, ws, stream);
@@ -669,12 +712,15 @@ moe_status moe_layer_fwd(const moe_dims* dims, const moe_bf16* x, const float* W
                         pdst, ws, L, stream)) != MOE_OK)
     return st;
   MOE_RUN(moe::launch_gather_rows(x, psrc, d.k, static_cast<long long>(rows_of(d)), d.T, d.h, xp,
-                                  num_sms(), stream, offsets + d.E),
+                                  num_sms(), stream, offsets + d.E, nullptr, nullptr,
+                                  at<int>(ws, 0)),
           "permute_rows");
   if ((st = do_ffn_fwd(d, xp, offsets, W1, W3, W2, at<uint16_t>(saved, S.A),
                        at<uint16_t>(saved, S.B), H, O, ws, stream)) != MOE_OK)
     return st;
-  MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
+  MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream,
+                              at<int>(ws, 0)),
+          "combine");
   return MOE_OK;
 }
 
@@ -729,8 +775,10 @@ moe_status moe_quantize_rows_fp8(const moe_bf16* in, int64_t rows, int32_t n, co
     return MOE_ERR_INVALID_ARG;
   if (rows > 0 && !idx && src_rows < rows) return MOE_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int* status = moe::nows_status_word();
+  if (!status) return MOE_ERR_CUDA;
   MOE_RUN(moe::launch_quant_rows(in, idx, idx ? div : 1, rows, src_rows, n, q, scale, num_sms(),
-                                 stream),
+                                 stream, nullptr, nullptr, 0, nullptr, nullptr, nullptr, status),
           "quant_rows");
   return MOE_OK;
 }
@@ -774,7 +822,8 @@ moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x, const floa
   // e4m3 rows for FC1 and, in the same pass, the bf16 rows the backward's FC1
   // weight gradient takes
   MOE_RUN(moe::launch_quant_rows(x, psrc, d.k, R, d.T, d.h, Xq, sx, num_sms(), stream, nvalid,
-                                 nullptr, 0, at<uint16_t>(saved, S.x_perm)),
+                                 nullptr, 0, at<uint16_t>(saved, S.x_perm), nullptr, nullptr,
+                                 at<int>(ws, 0)),
           "permute_quant_x");
   if (R > 0) {
     const GemmProblem g = problem(d, offsets, ws);
@@ -789,7 +838,9 @@ moe_status moe_layer_fwd_fp8(const moe_dims* dims, const moe_bf16* x, const floa
                                   stream),
             "gg_fc2_fwd_fp8");
   }
-  MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream), "combine");
+  MOE_RUN(moe::launch_combine(O, gates, pdst, d.T, d.k, d.h, y, num_sms(), stream,
+                              at<int>(ws, 0)),
+          "combine");
   return MOE_OK;
 }
 
@@ -861,7 +912,7 @@ moe_status moe_layer_bwd_fp8(const moe_dims* dims, const moe_bf16* x, const moe_
   const long long R = static_cast<long long>(rows_of(d));
   const int32_t* nvalid = offsets + d.E;
   MOE_RUN(moe::launch_bwd_prep(dy, at<uint16_t>(saved, S.O), gates, psrc, R, d.k, d.h, dO, dg,
-                               num_sms(), stream, nvalid),
+                               num_sms(), stream, nvalid, at<int>(ws, 0)),
           "bwd_prep");
   if (R == 0) {
     const size_t wbytes = static_cast<size_t>(d.E) * d.h * d.f * 4;
@@ -926,7 +977,7 @@ moe_status moe_layer_bwd(const moe_dims* dims, const moe_bf16* x, const moe_bf16
     return do_router_bwd(d, x, Wg, idx, gates, dg, dX, pdst, dx, dWg, ws, L, stream);
   }
   MOE_RUN(moe::launch_bwd_prep(dy, at<uint16_t>(saved, S.O), gates, psrc, R, d.k, d.h, dO, dg,
-                               num_sms(), stream, offsets + d.E),
+                               num_sms(), stream, offsets + d.E, at<int>(ws, 0)),
           "bwd_prep");
   if ((st = do_ffn_bwd(d, at<uint16_t>(saved, S.x_perm), dO, offsets, W1, W3, W2,
                        at<uint16_t>(saved, S.A), at<uint16_t>(saved, S.B),

@@ -55,7 +55,8 @@ __device__ __forceinline__ uint32_t q2(float a, float b, float s) {
 // once.  With copy, the quantising pass also writes the bf16 row to copy[p]
 // (the permute of the same rows, fused).  With in1/q1, row src of in1 is
 // quantised into q1 with the same scale, the amax taken over both rows.  Rows
-// p >= *nvalid (when nvalid is given) are skipped.
+// p >= *nvalid (when nvalid is given) are skipped.  A source index outside
+// [0, src_rows) is recorded in *status and quantised as a zero row.
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ in,
                                                          const int32_t* __restrict__ idx, int div,
                                                          long long rows, long long src_rows,
@@ -65,7 +66,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
                                                          const float* __restrict__ amax_part,
                                                          int nt, uint4* __restrict__ copy,
                                                          const uint4* __restrict__ in1,
-                                                         uint2* __restrict__ q1) {
+                                                         uint2* __restrict__ q1,
+                                                         int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -74,8 +76,19 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     rows = nv < rows ? (nv < 0 ? 0 : nv) : rows;
   }
   for (long long p = gw; p < rows; p += nw) {
-    long long src = idx ? __ldg(idx + p) / div : p;
-    src = src < 0 ? 0 : (src >= src_rows ? src_rows - 1 : src);
+    const long long src = idx ? __ldg(idx + p) / div : p;
+    if (src < 0 || src >= src_rows) {
+      if (lane == 0) {
+        report_bad_index(status);
+        scale[p] = 1.f;
+      }
+      for (int c = lane; c < n8; c += 32) {
+        q[p * n8 + c] = make_uint2(0, 0);
+        if (copy) copy[p * n8 + c] = make_uint4(0, 0, 0, 0);
+        if (q1) q1[p * n8 + c] = make_uint2(0, 0);
+      }
+      continue;
+    }
     const uint4* r = in + src * n8;
     const uint4* r1 = in1 ? in1 + src * n8 : nullptr;
     float amax = 0.f;
@@ -135,7 +148,8 @@ __global__ void __launch_bounds__(kQrThreads) quant_rows_reg_kernel(
     const uint4* __restrict__ in, const int32_t* __restrict__ idx, int div, long long rows,
     long long src_rows, const int32_t* __restrict__ nvalid, int n8, uint2* __restrict__ q,
     float* __restrict__ scale, const float* __restrict__ amax_part, int nt,
-    uint4* __restrict__ copy, const uint4* __restrict__ in1, uint2* __restrict__ q1) {
+    uint4* __restrict__ copy, const uint4* __restrict__ in1, uint2* __restrict__ q1,
+    int* __restrict__ status) {
   __shared__ float red[kQrThreads / 32];
   const int t = threadIdx.x;
   const int lane = t & 31;
@@ -144,8 +158,19 @@ __global__ void __launch_bounds__(kQrThreads) quant_rows_reg_kernel(
     rows = nv < rows ? (nv < 0 ? 0 : nv) : rows;
   }
   for (long long p = blockIdx.x; p < rows; p += gridDim.x) {
-    long long src = idx ? __ldg(idx + p) / div : p;
-    src = src < 0 ? 0 : (src >= src_rows ? src_rows - 1 : src);
+    const long long src = idx ? __ldg(idx + p) / div : p;
+    if (src < 0 || src >= src_rows) {  // block-uniform: the whole block skips the row
+      if (t == 0) {
+        report_bad_index(status);
+        scale[p] = 1.f;
+      }
+      for (int c = t; c < n8; c += kQrThreads) {
+        q[p * n8 + c] = make_uint2(0, 0);
+        if (copy) copy[p * n8 + c] = make_uint4(0, 0, 0, 0);
+        if (PAIR) q1[p * n8 + c] = make_uint2(0, 0);
+      }
+      continue;
+    }
     const uint4* r = in + src * n8;
     const uint4* r1 = PAIR ? in1 + src * n8 : nullptr;
     uint4 v[NPT];
@@ -344,8 +369,9 @@ int grid_rows(long long rows, int num_sms) {
 cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                               long long src_rows, int n, uint8_t* q, float* scale, int num_sms,
                               cudaStream_t s, const int32_t* nvalid, const float* amax_part,
-                              int nt, uint16_t* copy, const uint16_t* in1, uint8_t* q1) {
-  if (rows == 0 || src_rows == 0) return cudaSuccess;
+                              int nt, uint16_t* copy, const uint16_t* in1, uint8_t* q1,
+                              int* status) {
+  if (rows == 0) return cudaSuccess;
   const int n8 = n / 8;
   const int need = (n8 + kQrThreads - 1) / kQrThreads;
   if (need <= kQrMaxNpt) {
@@ -361,10 +387,12 @@ cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, l
   if (npt == NPT_) {                                                                        \
     if (in1)                                                                                \
       quant_rows_reg_kernel<NPT_, true><<<grid, kQrThreads, 0, s>>>(                        \
-          i4, idx, div, rows, src_rows, nvalid, n8, q2p, scale, amax_part, nt, c4, i14, q12p); \
+          i4, idx, div, rows, src_rows, nvalid, n8, q2p, scale, amax_part, nt, c4, i14, q12p, \
+          status);                                                                          \
     else                                                                                    \
       quant_rows_reg_kernel<NPT_, false><<<grid, kQrThreads, 0, s>>>(                       \
-          i4, idx, div, rows, src_rows, nvalid, n8, q2p, scale, amax_part, nt, c4, i14, q12p); \
+          i4, idx, div, rows, src_rows, nvalid, n8, q2p, scale, amax_part, nt, c4, i14, q12p, \
+          status);                                                                          \
     return launched();                                                                      \
   }
     MOE_QR(1) MOE_QR(2) MOE_QR(4) MOE_QR(7) MOE_QR(8)
@@ -373,7 +401,7 @@ cudaError_t launch_quant_rows(const uint16_t* in, const int32_t* idx, int div, l
   quant_rows_kernel<<<grid_rows(rows, num_sms), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(in), idx, div, rows, src_rows, nvalid, n / 8,
       reinterpret_cast<uint2*>(q), scale, amax_part, nt, reinterpret_cast<uint4*>(copy),
-      reinterpret_cast<const uint4*>(in1), reinterpret_cast<uint2*>(q1));
+      reinterpret_cast<const uint4*>(in1), reinterpret_cast<uint2*>(q1), status);
   return launched();
 }
 

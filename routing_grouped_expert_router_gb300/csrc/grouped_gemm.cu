@@ -23,6 +23,9 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "grouped_gemm.cuh"
 #include "kernels.cuh"
@@ -30,7 +33,6 @@
 
 namespace moe {
 
-int g_pair_clusters = 0;  // co-resident CTA pairs of the last pair launch (diagnostics)
 
 const char* const kGemmNames[6] = {"gg_fc1_fwd_swiglu", "gg_fc2_fwd",
                                    "gg_fc2_dgrad_swiglu_bwd", "gg_fc1_dgrad",
@@ -1389,32 +1391,39 @@ bool pair_for(int epi) {
   return epi != EPI_SWIGLU && epi != EPI_SWIGLU_F8;
 }
 
+// Co-resident clusters of CTA pairs for a pair kernel on the current device,
+// computed once per (kernel, device); safe from several host threads.
+int coresident_pairs(const void* kern, cudaLaunchConfig_t cfg, int num_sms) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / 2;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find({kern, dev});
+  if (it != cache.end()) return it->second;
+  cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
+  cache[{kern, dev}] = n;
+  return n;
+}
+
 template <bool A_MN, bool B_MN, int NUM_B, int EPI, bool GROUP_K>
 cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num_sms,
                    cudaStream_t s) {
   if (tiles <= 0) return cudaSuccess;
   if (!pair_for(EPI)) {
     auto kern = gg_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-      attr_set = true;
-    }
+    const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(prm, maps);
     return launched();
   }
   {
     auto kern = gg2_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
-    static bool attr2_set = false;
-    if (!attr2_set) {
-      cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
-      if (e != cudaSuccess) return e;
-      attr2_set = true;
-    }
+    const cudaError_t ea = set_smem_once(reinterpret_cast<const void*>(kern), SMEM2_BYTES);
+    if (ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.blockDim = dim3(NUM_THREADS2, 1, 1);
@@ -1428,15 +1437,9 @@ cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // A persistent grid must fit on the GPU at once: SMs that cannot pair up
-    // inside their GPC host no cluster, so size the grid by what is co-resident.
-    static int max_clusters = 0;
-    if (max_clusters == 0) {
-      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
-      max_clusters = n;
-    }
-    g_pair_clusters = max_clusters;
+    // inside their GPC host no cluster, so size the grid by what is co-resident
+    // (looked up once per kernel and device).
+    const int max_clusters = coresident_pairs(reinterpret_cast<const void*>(kern), cfg, num_sms);
     const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm, maps);

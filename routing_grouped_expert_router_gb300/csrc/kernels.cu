@@ -7,6 +7,10 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -58,11 +62,11 @@ int grid_for(long long warps_needed, int num_sms, int warps_per_block, int block
 }
 
 // ------------------------------------------------------------------ router
-// The hidden dimension is cut into chunks of CH columns; each block stages one
-// chunk of the router weights in shared memory once and then streams every
-// token tile of its share through it.  With one chunk (E <= 8, h <= 4096) the
-// kernel finishes the routing itself; otherwise it writes fp32 partial logits
-// [chunk][T][EP] and router_select_kernel adds them in chunk order.
+// E <= 8: router_a1_kernel holds all of Wg in shared memory (h <= 4096) and
+// routes every token in one launch; for longer h, router_a_kernel stages one
+// chunk of the router weights per block.  E > 8: router_c_kernel, a tiled
+// fp32 GEMM split over h.  Split launches write fp32 partial logits
+// [chunk][T][EP] that router_select_warp_kernel adds in chunk order.
 
 // top-k of l[0..E) (descending, ties to the lower id) and renormalised gates
 // exp(l_j - l_top) / sum over the selected.
@@ -292,22 +296,20 @@ __global__ void __launch_bounds__(kRouterAThreads, 1) router_a_kernel(
 // 320 for a full butterfly) leaves lane l with sums 2l and 2l + 1 of the
 // TOK x 8 (token, expert) logits; they meet in shared memory, where lane u
 // selects token u's top-k.
-constexpr int kRouterA1Threads = 256;
-constexpr int kRouterA1Warps = kRouterA1Threads / 32;
 constexpr int kRouterA1Step = 256;  // columns per stage
-constexpr int kRouterA1NStage = 3;
 constexpr int kRouterA1MaxH = 4096;
-constexpr size_t router_a1_smem(int h, int tok) {
+constexpr size_t router_a1_smem(int h, int tok, int warps, int nst) {
   return static_cast<size_t>((h + 7) / 8) * kRouterASlice * 4 +
-         static_cast<size_t>(kRouterA1Warps) * kRouterA1NStage * tok * kRouterA1Step * 2 +
-         static_cast<size_t>(kRouterA1Warps) * 64 * 4;
+         static_cast<size_t>(warps) * nst * tok * kRouterA1Step * 2 +
+         static_cast<size_t>(warps) * 64 * 4;
 }
 
-template <int TOK>
-__global__ void __launch_bounds__(kRouterA1Threads, 1) router_a1_kernel(
+template <int TOK, int WARPS, int NSTAGE>
+__global__ void __launch_bounds__(WARPS * 32, 1) router_a1_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ Wg, const float* __restrict__ b,
     int T, int h, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ gates) {
-  constexpr int EP = 8, SLICE = kRouterASlice, NST = kRouterA1NStage, SC = kRouterA1Step;
+  constexpr int kRouterA1Warps = WARPS, kRouterA1Threads = WARPS * 32;
+  constexpr int EP = 8, SLICE = kRouterASlice, NST = NSTAGE, SC = kRouterA1Step;
   constexpr int XSTAGE = TOK * SC;  // bf16 per stage of one warp
   extern __shared__ float sw[];
   const int nslice = (h + 7) / 8;
@@ -445,178 +447,305 @@ __global__ void __launch_bounds__(kRouterA1Threads, 1) router_a1_kernel(
   cp_async_wait<0>();
 }
 
-// ---- E > 8: lanes own experts.  A group of GL = EP / 4 lanes handles TOK
-// tokens; lane i of a group owns the four consecutive experts 4i .. 4i + 3,
-// whose weights for one column are one conflict-free 16-byte shared-memory
-// load, so every unpacked x value feeds four FMAs.  Each warp stages its
-// tokens' x slice (XS columns) in shared memory and reads it as broadcasts;
-// the slice is stored token-interleaved (token u of group g at row u NG + g),
-// so the NG groups of a warp read adjacent rows, which the padded pitch puts
-// in different banks.  Every weight value a lane loads then feeds TOK tokens.
-// No cross-lane reduction.
-constexpr int kRouterBXs = 64;
-constexpr int kRouterBXsp = kRouterBXs + 8;  // padded row (bf16) of a staged x slice
-
+// ---- E > 8, tiled: the logits are a skinny fp32 GEMM of x [T, h] (bf16) and
+// Wg [h, EP], register-blocked on the CUDA cores.  A block computes BM tokens
+// x EP experts over one chunk of h; each thread an 8-token x 8-expert tile:
+// tokens tm + TMT u (u < 8; interleaved, so the rows a warp reads sit in
+// different banks) and experts 8 tn .. 8 tn + 7.  The chunk runs in steps of
+// BK = 32 columns through a 2-stage cp.async ring holding the x tile
+// [BM][32] bf16 (rows padded to 80 bytes) and the Wg tile [32][EP] fp32.  Per
+// 8 columns a thread reads its tokens' x as 8 16-byte loads and, per column,
+// its experts' weights as 2 16-byte loads: 24 shared-memory loads feed 512
+// FMAs.  Each (token, expert) sum runs over the chunk's columns in order; the
+// chunks' partial logits [chunk][T][EP] are added in chunk order by
+// router_select_warp_kernel.
 template <int EP>
-struct RouterB {
-  static constexpr int EPL = 4;                  // experts per lane
-  static constexpr int GL = EP / EPL;            // lanes per token group
-  static constexpr int NG = 32 / GL;             // token groups per warp
-  static constexpr int TOK = 8;                  // tokens per group
-  static constexpr int CH = 32768 / EP;          // columns per chunk (128 KiB of weights)
-  static constexpr int XROWS = NG * TOK;         // staged token rows per warp
-  static constexpr int SMEM = CH * EP * 4 + 8 * XROWS * kRouterBXsp * 2;
+struct RouterC {
+  static constexpr int TN = EP / 8;                     // threads along the experts
+  static constexpr int THREADS = EP == 16 ? 128 : 256;
+  static constexpr int TMT = THREADS / TN;              // threads along the tokens
+  static constexpr int BM = TMT * 8;                    // tokens per block
+  static constexpr int BK = 32;                         // columns per step
+  static constexpr int XP = BK + 8;                     // padded x row (bf16)
+  static constexpr int XSTAGE = BM * XP;                // bf16 per x stage
+  static constexpr int WSTAGE = BK * EP;                // fp32 per Wg stage
+  static constexpr int SMEM = 2 * (XSTAGE * 2 + WSTAGE * 4);
 };
 
 template <int EP>
-__global__ void __launch_bounds__(256, 1) router_b_kernel(const uint16_t* __restrict__ x,
-                                                          const float* __restrict__ Wg, int T,
-                                                          int h, int E, int nch,
-                                                          float* __restrict__ partial) {
-  using S = RouterB<EP>;
-  constexpr int TOK = S::TOK, EPL = S::EPL, XS = kRouterBXs, XSP = kRouterBXsp;
-  extern __shared__ float sw[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(sw + S::CH * EP);
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int g = lane / S::GL;
-  const int el = lane % S::GL;
+__global__ void __launch_bounds__(RouterC<EP>::THREADS, 2) router_c_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ Wg, int T, int h, int E, int nch,
+    float* __restrict__ partial) {
+  using S = RouterC<EP>;
+  constexpr int BM = S::BM, BK = S::BK, XP = S::XP, TMT = S::TMT, NT = S::THREADS;
+  extern __shared__ float sc[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sc);           // [2][BM][XP]
+  float* ws = sc + S::XSTAGE;                                // [2][BK][EP] (after 2 x stages)
+  const int tid = threadIdx.x;
+  const int tn = tid % S::TN;
+  const int tm = tid / S::TN;
   const int c = blockIdx.x % nch;
-  const int sub = blockIdx.x / nch;
-  const int bpc = gridDim.x / nch;
-  const int c0 = c * S::CH;
-  const int rows = min(S::CH, h - c0);
-  for (int q = threadIdx.x; q < rows * EP; q += 256) {
-    const int lr = q / EP;
-    const int e = q - lr * EP;
-    sw[q] = (e < E) ? __ldg(Wg + static_cast<size_t>(c0 + lr) * E + e) : 0.f;
-  }
-  __syncthreads();
-  uint16_t* xw = xs + warp * S::XROWS * XSP;
-  const int btile = 8 * S::XROWS;
-  for (int t0 = sub * btile; t0 < T; t0 += bpc * btile) {
-    const int tw = t0 + warp * S::XROWS;  // this warp's first token
-    float acc[TOK][EPL];
-#pragma unroll
-    for (int u = 0; u < TOK; ++u)
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) acc[u][i] = 0.f;
-    for (int cs = 0; cs < rows; cs += XS) {
-      // stage x[tw .. tw + XROWS)[c0 + cs .. + XS) (rows of 128 bytes)
-#pragma unroll
-      for (int r = 0; r < S::XROWS * (XS / 8) / 32; ++r) {
-        const int id = r * 32 + lane;
-        const int row = id / (XS / 8);
-        const int c8 = id % (XS / 8);
-        const int t = tw + row;
-        const bool ok = t < T && cs + 8 * c8 < rows;
-        const uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(
-                                 x + static_cast<size_t>(t) * h + c0 + cs + 8 * c8))
-                           : make_uint4(0, 0, 0, 0);
-        const int srow = (row % TOK) * S::NG + row / TOK;  // token-interleaved
-        *reinterpret_cast<uint4*>(xw + srow * XSP + 8 * c8) = v;
+  const int t0 = (blockIdx.x / nch) * BM;
+  // chunk c: BK-column steps [c S / nch, (c + 1) S / nch) of the S = ceil(h / BK)
+  const int S_all = (h + BK - 1) / BK;
+  const int s0 = static_cast<int>(static_cast<long long>(c) * S_all / nch);
+  const int s1 = static_cast<int>(static_cast<long long>(c + 1) * S_all / nch);
+  const int k0 = s0 * BK;
+  const int kend = min(h, s1 * BK);
+  const int nsteps = s1 - s0;
+
+  auto issue = [&](int st) {
+    if (st < nsteps) {
+      const int kc = k0 + st * BK;
+      const int slot = st & 1;
+      const uint32_t xb = smem_addr(xs + slot * S::XSTAGE);
+      // x tile: BM rows x 4 pieces of 16 bytes
+      for (int q = tid; q < BM * (BK / 8); q += NT) {
+        const int r = q / (BK / 8), p8 = q % (BK / 8);
+        const int t = t0 + r, col = kc + 8 * p8;
+        const bool ok = t < T && col < kend;
+        const uint16_t* src = ok ? x + static_cast<size_t>(t) * h + col : x;
+        cp_async16(xb + (r * XP + 8 * p8) * 2, src, ok);
       }
-      __syncwarp();
-#pragma unroll 1
-      for (int c8 = 0; c8 < XS / 8; ++c8) {
-        uint4 xq[TOK];
-#pragma unroll
-        for (int u = 0; u < TOK; ++u)
-          xq[u] = *reinterpret_cast<const uint4*>(xw + (u * S::NG + g) * XSP + 8 * c8);
-        const float4* wr = reinterpret_cast<const float4*>(sw + (cs + 8 * c8) * EP) + el;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 w = wr[j * (EP / 4)];
-#pragma unroll
-          for (int u = 0; u < TOK; ++u) {
-            const uint32_t q = j < 2 ? xq[u].x : j < 4 ? xq[u].y : j < 6 ? xq[u].z : xq[u].w;
-            const float xv = (j & 1) ? bf16_hi(q) : bf16_lo(q);
-            acc[u][0] = fmaf(xv, w.x, acc[u][0]);
-            acc[u][1] = fmaf(xv, w.y, acc[u][1]);
-            acc[u][2] = fmaf(xv, w.z, acc[u][2]);
-            acc[u][3] = fmaf(xv, w.w, acc[u][3]);
-          }
+      // Wg tile: BK rows x EP fp32 (experts past E read as 0)
+      if (E % 4 == 0) {
+        const uint32_t wb = smem_addr(ws + slot * S::WSTAGE);
+        for (int q = tid; q < BK * (EP / 4); q += NT) {
+          const int r = q / (EP / 4), e4 = q % (EP / 4);
+          const int row = kc + r;
+          const bool ok = row < kend && 4 * e4 < E;
+          const float* src = ok ? Wg + static_cast<size_t>(row) * E + 4 * e4 : Wg;
+          cp_async16(wb + (r * EP + 4 * e4) * 4, src, ok);
+        }
+      } else {
+        // rows of E floats are not 16-byte aligned: plain loads and stores
+        // (the slot was last read two steps ago, before the step's barrier)
+        float* wd = ws + slot * S::WSTAGE;
+        for (int q = tid; q < BK * EP; q += NT) {
+          const int r = q / EP, e = q % EP;
+          const int row = kc + r;
+          wd[q] = (row < kend && e < E) ? __ldg(Wg + static_cast<size_t>(row) * E + e) : 0.f;
         }
       }
-      __syncwarp();
     }
+    cp_async_commit();
+  };
+
+  float acc[8][8];
 #pragma unroll
-    for (int u = 0; u < TOK; ++u) {
-      const int t = tw + g * TOK + u;
-      if (t >= T) continue;
-      *reinterpret_cast<float4*>(partial + (static_cast<size_t>(c) * T + t) * EP + EPL * el) =
-          make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+  for (int u = 0; u < 8; ++u)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
+
+  issue(0);
+  for (int st = 0; st < nsteps; ++st) {
+    issue(st + 1);
+    cp_async_wait<1>();
+    __syncthreads();  // stage st is in shared memory for every thread
+    const uint16_t* xt = xs + (st & 1) * S::XSTAGE;
+    const float* wt = ws + (st & 1) * S::WSTAGE + 8 * tn;
+#pragma unroll
+    for (int k8 = 0; k8 < BK / 8; ++k8) {
+      uint4 xq[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        xq[u] = *reinterpret_cast<const uint4*>(xt + (tm + TMT * u) * XP + 8 * k8);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const float4 w0 = *reinterpret_cast<const float4*>(wt + (8 * k8 + kk) * EP);
+        const float4 w1 = *reinterpret_cast<const float4*>(wt + (8 * k8 + kk) * EP + 4);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t q = kk < 2 ? xq[u].x : kk < 4 ? xq[u].y : kk < 6 ? xq[u].z : xq[u].w;
+          const float xv = (kk & 1) ? bf16_hi(q) : bf16_lo(q);
+          acc[u][0] = fmaf(xv, w0.x, acc[u][0]);
+          acc[u][1] = fmaf(xv, w0.y, acc[u][1]);
+          acc[u][2] = fmaf(xv, w0.z, acc[u][2]);
+          acc[u][3] = fmaf(xv, w0.w, acc[u][3]);
+          acc[u][4] = fmaf(xv, w1.x, acc[u][4]);
+          acc[u][5] = fmaf(xv, w1.y, acc[u][5]);
+          acc[u][6] = fmaf(xv, w1.z, acc[u][6]);
+          acc[u][7] = fmaf(xv, w1.w, acc[u][7]);
+        }
+      }
     }
+    __syncthreads();  // every thread is done with stage st before it is refilled
+  }
+  cp_async_wait<0>();
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int t = t0 + tm + TMT * u;
+    if (t >= T) continue;
+    float4* dst = reinterpret_cast<float4*>(partial + (static_cast<size_t>(c) * T + t) * EP + 8 * tn);
+    dst[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+    dst[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
   }
 }
 
-// Thread per token: logits = sum of the chunks' partials (in chunk order) + b.
 template <int EP>
-__global__ void __launch_bounds__(128) router_select_kernel(const float* __restrict__ partial,
-                                                            int nch, const float* __restrict__ b,
-                                                            int T, int E, int k,
-                                                            int32_t* __restrict__ topk_idx,
-                                                            float* __restrict__ gates) {
-  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
-    float l[EP];
+cudaError_t router_c_launch(const uint16_t* x, const float* Wg, int T, int h, int E, int nch,
+                            float* partial, cudaStream_t s);
+
+// Chunks of h for a split-K launch of `tiles` output tiles over S k-steps:
+// the count with the shortest makespan on a 152-SM GPU at two blocks per SM,
+// modelled as (waves of blocks) x (steps per chunk + 2 steps of prologue and
+// epilogue).  A function of the shape only (the workspace is sized from it).
+int split_k_chunks(long long tiles, int S, int max_chunks = 32) {
+  const long long slots = 2 * 152;
+  int best = 1;
+  double best_t = -1.0;
+  for (int n = 1; n <= max_chunks && n <= S; ++n) {
+    const long long waves = (tiles * n + slots - 1) / slots;
+    const double t = static_cast<double>(waves) * (static_cast<double>(S) / n + 2.0);
+    if (best_t < 0 || t < best_t - 1e-9) {
+      best_t = t;
+      best = n;
+    }
+  }
+  return best;
+}
+
+template <int EP>
+int router_c_nch(int T, int h) {
+  const long long tiles = (T + RouterC<EP>::BM - 1) / RouterC<EP>::BM;
+  return split_k_chunks(tiles, (h + RouterC<EP>::BK - 1) / RouterC<EP>::BK);
+}
+
+// Warp per token: the logits of token t are the chunks' partials summed in
+// chunk order (lane l holds experts l and l + 32), plus b.  The top-k is k
+// rounds of a warp arg-max (larger logit first, the lower expert id on ties;
+// NaN counts as the smallest value), then lane 0 forms the renormalised gates
+// exactly as select_topk does.  The same values as the thread-per-token
+// kernel, with the whole warp reading each token's partials.
+template <int EP>
+__global__ void __launch_bounds__(256) router_select_warp_kernel(
+    const float* __restrict__ partial, int nch, const float* __restrict__ b, int T, int E, int k,
+    int32_t* __restrict__ topk_idx, float* __restrict__ gates) {
+  constexpr int PER = (EP + 31) / 32;
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int t = gw; t < T; t += nw) {
+    float l[PER];
 #pragma unroll
-    for (int e = 0; e < EP; ++e) l[e] = 0.f;
+    for (int i = 0; i < PER; ++i) l[i] = 0.f;
     for (int c = 0; c < nch; ++c) {
-      const float4* src =
-          reinterpret_cast<const float4*>(partial + (static_cast<size_t>(c) * T + t) * EP);
+      const float* src = partial + (static_cast<size_t>(c) * T + t) * EP;
 #pragma unroll
-      for (int e4 = 0; e4 < EP / 4; ++e4) {
-        const float4 v = __ldg(src + e4);
-        l[4 * e4 + 0] += v.x;
-        l[4 * e4 + 1] += v.y;
-        l[4 * e4 + 2] += v.z;
-        l[4 * e4 + 3] += v.w;
+      for (int i = 0; i < PER; ++i)
+        if (lane + 32 * i < EP) l[i] += __ldg(src + lane + 32 * i);
+    }
+    bool live[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      live[i] = e < E;
+      if (live[i] && b) l[i] += __ldg(b + e);
+    }
+    float sel_l[8];
+    int sel_e[8];
+    for (int j = 0; j < k; ++j) {
+      // this lane's best live candidate
+      float bv = -INFINITY;
+      int be = 1 << 30;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const float v = isnan(l[i]) ? -INFINITY : l[i];
+        const int e = lane + 32 * i;
+        if (live[i] && (v > bv || (v == bv && e < be))) {
+          bv = v;
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (lane + 32 * i == be) live[i] = false;
+      sel_e[j < 8 ? j : 7] = be;
+      // the logit itself (NaN kept as NaN, as select_topk would give)
+      const int owner = be & 31;
+      float lv = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (32 * i <= be && be < 32 * i + 32) lv = l[i];
+      sel_l[j < 8 ? j : 7] = __shfl_sync(kFull, lv, owner);
+    }
+    if (lane == 0) {
+      float sj[8];
+      float sum = 0.f;
+      for (int j = 0; j < k; ++j) {
+        sj[j] = expf(sel_l[j] - sel_l[0]);
+        sum += sj[j];
+      }
+      for (int j = 0; j < k; ++j) {
+        topk_idx[static_cast<size_t>(t) * k + j] = sel_e[j];
+        gates[static_cast<size_t>(t) * k + j] = sj[j] / sum;
       }
     }
-#pragma unroll
-    for (int e = 0; e < EP; ++e)
-      if (e < E && b) l[e] += __ldg(b + e);
-    select_topk<EP>(l, E, k, topk_idx + static_cast<size_t>(t) * k,
-                    gates + static_cast<size_t>(t) * k);
   }
 }
 
 int router_padded_e(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : 64; }
 
-int router_chunks(int h, int E) {
+int router_c_chunks(int T, int h, int ep) {
+  return ep == 16 ? router_c_nch<16>(T, h) : ep == 32 ? router_c_nch<32>(T, h) : router_c_nch<64>(T, h);
+}
+
+
+int router_chunks(int T, int h, int E) {
   const int ep = router_padded_e(E);
   if (ep == 8 && h <= kRouterA1MaxH) return 1;  // router_a1_kernel holds all of Wg
-  const int ch = ep == 8 ? kRouterACh : 32768 / ep;
-  return (h + ch - 1) / ch;
+  if (ep == 8) return (h + kRouterACh - 1) / kRouterACh;
+  return router_c_chunks(T, h, ep);
 }
 
 // router_a1_kernel<TOK>: the TOK whose items spread most evenly over the
 // grid's warps (fewest token slots on the busiest warp; ties to the larger
 // TOK), within the shared-memory limit.
-template <int TOK>
+template <int TOK, int WARPS, int NST>
 cudaError_t router_a1_launch(const uint16_t* x, const float* Wg, const float* b, int T, int h,
                              int E, int k, int32_t* idx, float* gates, int blocks,
                              cudaStream_t s) {
-  const size_t smem = router_a1_smem(h, TOK);
-  static int attr_smem = 0;
-  if (attr_smem < static_cast<int>(smem)) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        router_a1_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_smem = static_cast<int>(smem);
-  }
-  router_a1_kernel<TOK><<<blocks, kRouterA1Threads, smem, s>>>(x, Wg, b, T, h, E, k, idx, gates);
+  const size_t smem = router_a1_smem(h, TOK, WARPS, NST);
+  const cudaError_t e = set_smem_once(
+      reinterpret_cast<const void*>(router_a1_kernel<TOK, WARPS, NST>), static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  router_a1_kernel<TOK, WARPS, NST><<<blocks, WARPS * 32, smem, s>>>(x, Wg, b, T, h, E, k, idx,
+                                                                     gates);
   return launched();
+}
+
+// Warps per block and x stages per warp of router_a1_kernel: 8 warps with 3
+// stages, or 12 warps (TOK = 4) with MOE_ROUTER_A1=12 for measurement.
+void router_a1_shape(int& warps, int& nst) {
+  static const int v = [] {
+    const char* e = getenv("MOE_ROUTER_A1");
+    return (e && e[0] == '1' && e[1] == '2') ? 1 : 0;
+  }();
+  warps = v == 1 ? 12 : 8;
+  nst = 3;
 }
 
 cudaError_t router_a1_dispatch(const uint16_t* x, const float* Wg, const float* b, int T, int h,
                                int E, int k, int32_t* idx, float* gates, int num_sms,
                                cudaStream_t s) {
-  const long long nw = static_cast<long long>(num_sms) * kRouterA1Warps;
+  int warps = 8, nst = 3;
+  router_a1_shape(warps, nst);
+  const long long nw = static_cast<long long>(num_sms) * warps;
   int best = 4;
   long long best_slots = -1;
-  for (int tok = 4; tok <= 7; ++tok) {
-    if (router_a1_smem(h, tok) > 232448) continue;
+  // more warps leave fewer registers a thread: TOK = 4 only (no spills)
+  const int tok_max = warps == 8 ? 7 : 4;
+  for (int tok = 4; tok <= tok_max; ++tok) {
+    if (router_a1_smem(h, tok, warps, nst) > 232448) continue;
     const long long items = (T + tok - 1) / tok;
     const long long slots = (items + nw - 1) / nw * tok;
     if (best_slots < 0 || slots <= best_slots) {
@@ -626,42 +755,37 @@ cudaError_t router_a1_dispatch(const uint16_t* x, const float* Wg, const float* 
   }
   // blocks: enough warps for the items, at most one block per SM
   const long long items = (T + best - 1) / best;
-  int blocks = static_cast<int>((items + kRouterA1Warps - 1) / kRouterA1Warps);
+  int blocks = static_cast<int>((items + warps - 1) / warps);
   if (blocks > num_sms) blocks = num_sms;
-  switch (best) {
-    case 4: return router_a1_launch<4>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
-    case 5: return router_a1_launch<5>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
-    case 6: return router_a1_launch<6>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
-    default: return router_a1_launch<7>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
+#define MOE_A1(W, N)                                                                         \
+  switch (best) {                                                                            \
+    case 4: return router_a1_launch<4, W, N>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);  \
+    case 5: return router_a1_launch<5, W, N>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);  \
+    case 6: return router_a1_launch<6, W, N>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);  \
+    default: return router_a1_launch<7, W, N>(x, Wg, b, T, h, E, k, idx, gates, blocks, s); \
   }
+  if (warps == 12) return router_a1_launch<4, 12, 3>(x, Wg, b, T, h, E, k, idx, gates, blocks, s);
+  MOE_A1(8, 3)
+#undef MOE_A1
 }
 
 template <int EP>
-cudaError_t router_b_launch(const uint16_t* x, const float* Wg, int T, int h, int E, int nch,
-                            float* partial, int num_sms, cudaStream_t s) {
-  using S = RouterB<EP>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(router_b_kernel<EP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int tiles = (T + 8 * S::XROWS - 1) / (8 * S::XROWS);
-  int bpc = num_sms / nch;
-  if (bpc < 1) bpc = 1;
-  if (bpc > tiles) bpc = tiles;
-  router_b_kernel<EP><<<nch * bpc, 256, S::SMEM, s>>>(x, Wg, T, h, E, nch, partial);
+cudaError_t router_c_launch(const uint16_t* x, const float* Wg, int T, int h, int E, int nch,
+                            float* partial, cudaStream_t s) {
+  using S = RouterC<EP>;
+  const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(router_c_kernel<EP>), S::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (T + S::BM - 1) / S::BM;
+  router_c_kernel<EP><<<static_cast<int>(tiles * nch), S::THREADS, S::SMEM, s>>>(x, Wg, T, h, E,
+                                                                                 nch, partial);
   return launched();
 }
 
 template <int EP>
 cudaError_t router_select_launch(const float* partial, int nch, const float* b, int T, int E,
                                  int k, int32_t* idx, float* gates, int num_sms, cudaStream_t s) {
-  long long blocks = (T + 127) / 128;
-  if (blocks > num_sms * 8) blocks = num_sms * 8;
-  router_select_kernel<EP><<<static_cast<int>(blocks), 128, 0, s>>>(partial, nch, b, T, E, k, idx,
-                                                                   gates);
+  const int grid = grid_for(T, num_sms, 8, 16);
+  router_select_warp_kernel<EP><<<grid, 256, 0, s>>>(partial, nch, b, T, E, k, idx, gates);
   return launched();
 }
 
@@ -674,7 +798,8 @@ cudaError_t router_select_launch(const float* partial, int nch, const float* b, 
 //   + sizes of earlier warps (this round) + lanes below it in its own group.
 // An assignment is kept when its expert lies in the local range
 // [e_lo, e_lo + EL) and its rank is below `cap`; kept ones go to permuted row
-// offsets[e] + rank, the others get perm_dst = -1.
+// offsets[e] + rank, the others get perm_dst = -1.  An expert id outside
+// [0, E) is recorded in *status and the assignment is not placed.
 constexpr int kDispThreads = 256;
 constexpr int kDispWarps = kDispThreads / 32;
 constexpr int kDispMaxE = 256;
@@ -684,7 +809,7 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
     const int32_t* __restrict__ topk_idx, long long n, int E, int e_lo, int EL, int cap,
     int32_t* __restrict__ blk_counts, const int32_t* __restrict__ bases,
     const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
-    int32_t* __restrict__ perm_dst) {
+    int32_t* __restrict__ perm_dst, int* __restrict__ status) {
   __shared__ int running[kDispMaxE];
   __shared__ int wc[kDispWarps][kDispMaxE];
   const int tid = threadIdx.x;
@@ -700,9 +825,14 @@ __global__ void __launch_bounds__(kDispThreads) dispatch_kernel(
     const bool valid = a < n;
     int le = -1;  // local expert, -1 = not placed
     if (valid) {
-      int e = __ldg(topk_idx + a);
-      e = e < 0 ? 0 : (e >= E ? E - 1 : e);  // keep every index in range
-      le = (e >= e_lo && e < e_lo + EL) ? e - e_lo : -1;
+      const int e = __ldg(topk_idx + a);
+      if (e < 0 || e >= E) {
+        // an expert id out of range: reported (once, by the histogram pass)
+        // and not placed
+        if (!WRITE) report_bad_index(status);
+      } else {
+        le = (e >= e_lo && e < e_lo + EL) ? e - e_lo : -1;
+      }
     }
     const unsigned grp = __match_any_sync(kFull, le);
     const int lrank = __popc(grp & lt_mask);
@@ -764,14 +894,16 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t* __res
 // --------------------------------------------------------------- row moves
 // Warp per row, 16-byte pieces.
 // Rows p < *nvalid (all `rows` when nvalid is NULL); a negative index gives a
-// zero row.  With gsrc/gdst, also gdst[p] = gsrc[idx[p]] (a value per row).
+// zero row, and so does a source index past src_rows (recorded in *status).
+// With gsrc/gdst, also gdst[p] = gsrc[idx[p]] (a value per row).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ in,
                                                           const int32_t* __restrict__ idx, int div,
                                                           long long rows, long long src_rows,
                                                           const int32_t* __restrict__ nvalid,
                                                           int h8, uint4* __restrict__ out,
                                                           const float* __restrict__ gsrc,
-                                                          float* __restrict__ gdst) {
+                                                          float* __restrict__ gdst,
+                                                          int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -782,13 +914,14 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   for (long long p = gw; p < rows; p += nw) {
     const long long i = __ldg(idx + p);
     uint4* d = out + p * h8;
-    if (gdst && lane == 0) gdst[p] = i < 0 ? 0.f : __ldg(gsrc + i);
-    if (i < 0) {
+    const long long src = i / div;
+    const bool bad = i >= 0 && src >= src_rows;
+    if (bad && lane == 0) report_bad_index(status);
+    if (gdst && lane == 0) gdst[p] = (i < 0 || bad) ? 0.f : __ldg(gsrc + i);
+    if (i < 0 || bad) {
       for (int c = lane; c < h8; c += 32) d[c] = make_uint4(0, 0, 0, 0);
       continue;
     }
-    long long src = i / div;
-    src = src >= src_rows ? src_rows - 1 : src;  // stay inside `in`
     const uint4* s = in + src * h8;
 #pragma unroll 4
     for (int c = lane; c < h8; c += 32) d[c] = __ldg(s + c);
@@ -796,11 +929,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }
 
 // y[t] = sum_j g[t,j] * O[perm_dst[t*k+j]], fp32 in slot order.  K = k.
+// A row index past T*k is recorded in *status and its slot adds nothing.
 template <int K>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ O,
                                                       const float* __restrict__ gates,
                                                       const int32_t* __restrict__ perm_dst, int T,
-                                                      int h8, uint4* __restrict__ y) {
+                                                      int h8, uint4* __restrict__ y,
+                                                      int* __restrict__ status) {
   constexpr int k = K;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -813,10 +948,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     for (int j = 0; j < K; ++j) {
       {
         const long long r = __ldg(perm_dst + static_cast<size_t>(t) * k + j);
+        const bool bad = r >= static_cast<long long>(T) * k;
+        if (bad && lane == 0) report_bad_index(status);
         // a dropped slot (r < 0) adds nothing and reads no row
-        kept[j] = r >= 0;
-        rows[j] = r < 0 ? 0 : (r >= static_cast<long long>(T) * k ? static_cast<long long>(T) * k - 1 : r);
-        g[j] = r < 0 ? 0.f : __ldg(gates + static_cast<size_t>(t) * k + j);
+        kept[j] = r >= 0 && !bad;
+        rows[j] = kept[j] ? r : 0;
+        g[j] = kept[j] ? __ldg(gates + static_cast<size_t>(t) * k + j) : 0.f;
       }
     }
     // four 16-byte pieces per lane per step: 4 * k loads in flight
@@ -847,7 +984,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   }
 }
 
-// dO[p] = bf16(g[a] * dy[t]); dg[a] = <dy[t], O[p]>.
+// dO[p] = bf16(g[a] * dy[t]); dg[a] = <dy[t], O[p]>.  An assignment index
+// outside [0, rows) is recorded in *status; that row's dO is zero.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ dy,
                                                        const uint4* __restrict__ O,
                                                        const float* __restrict__ gates,
@@ -855,7 +993,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
                                                        long long rows,
                                                        const int32_t* __restrict__ nvalid, int k,
                                                        int h8, uint4* __restrict__ dO,
-                                                       float* __restrict__ dg) {
+                                                       float* __restrict__ dg,
+                                                       int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -865,8 +1004,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
     rows = nv < rows ? (nv < 0 ? 0 : nv) : rows;
   }
   for (long long p = gw; p < rows; p += nw) {
-    int a = __ldg(perm_src + p);
-    a = a < 0 ? 0 : (a >= total ? static_cast<int>(total - 1) : a);
+    const int a = __ldg(perm_src + p);
+    if (a < 0 || a >= total) {
+      if (lane == 0) report_bad_index(status);
+      for (int c = lane; c < h8; c += 32) dO[p * h8 + c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
     const long long t = a / k;
     const float g = __ldg(gates + a);
     float dot = 0.f;
@@ -893,7 +1036,8 @@ __global__ void __launch_bounds__(256) dg_reduce_kernel(const float* __restrict_
                                                         const int32_t* __restrict__ perm_src,
                                                         long long rows,
                                                         const int32_t* __restrict__ nvalid,
-                                                        float* __restrict__ dg) {
+                                                        float* __restrict__ dg,
+                                                        int* __restrict__ status) {
   const long long nv = __ldg(nvalid);
   const long long n = nv < rows ? (nv < 0 ? 0 : nv) : rows;
   for (long long p = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; p < n;
@@ -901,8 +1045,11 @@ __global__ void __launch_bounds__(256) dg_reduce_kernel(const float* __restrict_
     const float* q = part + p * nt;
     float s = 0.f;
     for (int i = 0; i < nt; ++i) s += __ldg(q + i);
-    long long a = __ldg(perm_src + p);
-    a = a < 0 ? 0 : (a >= rows ? rows - 1 : a);
+    const long long a = __ldg(perm_src + p);
+    if (a < 0 || a >= rows) {
+      report_bad_index(status);
+      continue;
+    }
     dg[a] = s;
   }
 }
@@ -925,7 +1072,7 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
     const float4* __restrict__ dX, const int32_t* __restrict__ perm_dst,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ gates,
     const float* __restrict__ dg, const float4* __restrict__ WgT, int T, int h8, int E,
-    float* __restrict__ dl, uint4* __restrict__ dx) {
+    float* __restrict__ dl, uint4* __restrict__ dx, int* __restrict__ status) {
   constexpr int U = K <= 2 ? 2 : 1;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -940,11 +1087,13 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
     for (int j = 0; j < K; ++j) {
       const size_t a = static_cast<size_t>(t) * K + j;
       const long long r = __ldg(perm_dst + a);
-      kept[j] = r >= 0;  // a dropped slot has no expert output: dg = 0, no dX
-      rows[j] = r < 0 ? 0 : (r >= R ? R - 1 : r);
       const int e = __ldg(topk_idx + a);
-      ex[j] = e < 0 ? 0 : (e >= E ? E - 1 : e);
-      g[j] = __ldg(gates + a);
+      // out-of-range entries are recorded; such a slot adds nothing
+      if ((r >= R || e < 0 || e >= E) && lane == 0) report_bad_index(status);
+      kept[j] = r >= 0 && r < R;  // a dropped slot has no expert output: dg = 0, no dX
+      rows[j] = kept[j] ? r : 0;
+      ex[j] = (e < 0 || e >= E) ? -1 : e;
+      g[j] = ex[j] < 0 ? 0.f : __ldg(gates + a);
       d[j] = kept[j] ? __ldg(dg + a) : 0.f;
     }
     // dl_j = g_j (dg_j - sum_i g_i dg_i), evaluated as g_j sum_i g_i (dg_j - dg_i)
@@ -994,6 +1143,7 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
         }
 #pragma unroll
         for (int j = 0; j < K; ++j) {
+          if (ex[j] < 0) continue;
           const size_t wo = (static_cast<size_t>(ex[j]) * h8 + c) * 2;
           const float4 w0 = __ldg(WgT + wo);
           const float4 w1 = __ldg(WgT + wo + 1);
@@ -1008,77 +1158,126 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
   }
 }
 
-// dWg partials: block = (column tile, token chunk of kWgChunk); thread owns
-// CPT consecutive columns (2 for E <= 8, so a warp's x loads are whole
-// 128-byte lines) and EP experts; dl rows of the chunk are staged in shared
-// memory.
-constexpr int kWgChunk = 256;
-constexpr int kWgStage = 32;
-
+// dWg = x^T dl as a register-blocked fp32 GEMM on the CUDA cores (M = h
+// columns of x, N = EP experts, K = T tokens), split over token chunks.  A
+// block computes BM columns x EP experts over one chunk; each thread 8
+// consecutive columns x 8 experts.  Tokens run in steps of BK = 16 through a
+// 2-stage cp.async ring holding the x tile [BK][BM] bf16 (rows of x as they
+// lie in memory) and the dl tile [BK][EP] fp32.  Per token a thread reads its
+// 8 columns of x as one 16-byte load and its 8 experts of dl as two: 3 loads
+// feed 64 FMAs.  Each (column, expert) sum runs over the chunk's tokens in
+// order; router_wgrad_reduce_kernel adds the chunks in order.
 template <int EP>
-struct WgShape {
-  static constexpr int CPT = EP <= 8 ? 2 : 16 / EP >= 1 ? 16 / EP : 1;  // columns per thread
-  static constexpr int COLS = 256 * CPT;             // columns per block
+struct WgradC {
+  static constexpr int TN = EP / 8;
+  static constexpr int THREADS = EP <= 16 ? 128 : 256;
+  static constexpr int TMT = THREADS / TN;
+  static constexpr int BM = TMT * 8;                 // columns per block
+  static constexpr int BK = 16;                      // tokens per step
+  static constexpr int XSTAGE = BK * BM;             // bf16
+  static constexpr int DSTAGE = BK * EP;             // fp32
+  static constexpr int SMEM = 2 * (XSTAGE * 2 + DSTAGE * 4);
 };
 
 template <int EP>
-__global__ void __launch_bounds__(256) router_wgrad_kernel(const uint16_t* __restrict__ x,
-                                                           const float* __restrict__ dl, int T,
-                                                           int h, int E,
-                                                           float* __restrict__ partial) {
-  constexpr int CPT = WgShape<EP>::CPT;
-  __shared__ float sdl[kWgStage][EP];
-  const int i0 = blockIdx.x * WgShape<EP>::COLS + threadIdx.x * CPT;  // first column
-  const int chunk = blockIdx.y;
-  const int t0 = chunk * kWgChunk;
-  const int t1 = min(T, t0 + kWgChunk);
-  float acc[CPT][EP];
-#pragma unroll
-  for (int c = 0; c < CPT; ++c)
-#pragma unroll
-    for (int e = 0; e < EP; ++e) acc[c][e] = 0.f;
-  for (int ts = t0; ts < t1; ts += kWgStage) {
-    __syncthreads();
-    for (int q = threadIdx.x; q < kWgStage * EP; q += 256) {
-      const int tt = ts + q / EP;
-      const int e = q % EP;
-      sdl[q / EP][e] = (tt < t1 && e < E) ? dl[static_cast<size_t>(tt) * E + e] : 0.f;
-    }
-    __syncthreads();
-    if (i0 < h) {
-      const int n = min(kWgStage, t1 - ts);
-      for (int u = 0; u < n; ++u) {
-        const uint16_t* xr = x + static_cast<size_t>(ts + u) * h + i0;
-        float xv[CPT];
-        if constexpr (CPT == 8) {
-          unpack8(__ldg(reinterpret_cast<const uint4*>(xr)), xv);
-        } else if constexpr (CPT == 4) {
-          const uint2 q = __ldg(reinterpret_cast<const uint2*>(xr));
-          xv[0] = bf16_lo(q.x);
-          xv[1] = bf16_hi(q.x);
-          xv[2] = bf16_lo(q.y);
-          xv[3] = bf16_hi(q.y);
-        } else if constexpr (CPT == 2) {
-          const uint32_t q = __ldg(reinterpret_cast<const uint32_t*>(xr));
-          xv[0] = bf16_lo(q);
-          xv[1] = bf16_hi(q);
-        } else {
-          xv[0] = __uint_as_float(static_cast<uint32_t>(__ldg(xr)) << 16);
+__global__ void __launch_bounds__(WgradC<EP>::THREADS, 2) router_wgrad_c_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ dl, int T, int h, int E, int nch,
+    float* __restrict__ partial) {
+  using S = WgradC<EP>;
+  constexpr int BM = S::BM, BK = S::BK, NT = S::THREADS;
+  extern __shared__ float wc[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(wc);   // [2][BK][BM]
+  float* ds = wc + S::XSTAGE;                        // [2][BK][EP] after the two x stages
+  const int tid = threadIdx.x;
+  const int tn = tid % S::TN;
+  const int tm = tid / S::TN;
+  const int c = blockIdx.x % nch;
+  const int i0 = (blockIdx.x / nch) * BM;
+  const int S_all = (T + BK - 1) / BK;
+  const int s0 = static_cast<int>(static_cast<long long>(c) * S_all / nch);
+  const int s1 = static_cast<int>(static_cast<long long>(c + 1) * S_all / nch);
+  const int nsteps = s1 - s0;
+
+  auto issue = [&](int st) {
+    if (st < nsteps) {
+      const int tb = (s0 + st) * BK;
+      const int slot = st & 1;
+      const uint32_t xb = smem_addr(xs + slot * S::XSTAGE);
+      for (int q = tid; q < BK * (BM / 8); q += NT) {
+        const int r = q / (BM / 8), p8 = q % (BM / 8);
+        const int t = tb + r, col = i0 + 8 * p8;
+        const bool ok = t < T && col < h;
+        const uint16_t* src = ok ? x + static_cast<size_t>(t) * h + col : x;
+        cp_async16(xb + (r * BM + 8 * p8) * 2, src, ok);
+      }
+      if (E % 4 == 0) {
+        const uint32_t db = smem_addr(ds + slot * S::DSTAGE);
+        for (int q = tid; q < BK * (EP / 4); q += NT) {
+          const int r = q / (EP / 4), e4 = q % (EP / 4);
+          const int t = tb + r;
+          const bool ok = t < T && 4 * e4 < E;
+          const float* src = ok ? dl + static_cast<size_t>(t) * E + 4 * e4 : dl;
+          cp_async16(db + (r * EP + 4 * e4) * 4, src, ok);
         }
-#pragma unroll
-        for (int c = 0; c < CPT; ++c)
-#pragma unroll
-          for (int e = 0; e < EP; ++e) acc[c][e] = fmaf(xv[c], sdl[u][e], acc[c][e]);
+      } else {
+        float* dd = ds + slot * S::DSTAGE;
+        for (int q = tid; q < BK * EP; q += NT) {
+          const int r = q / EP, e = q % EP;
+          const int t = tb + r;
+          dd[q] = (t < T && e < E) ? __ldg(dl + static_cast<size_t>(t) * E + e) : 0.f;
+        }
       }
     }
+    cp_async_commit();
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
+
+  issue(0);
+  for (int st = 0; st < nsteps; ++st) {
+    issue(st + 1);
+    cp_async_wait<1>();
+    __syncthreads();
+    const uint16_t* xt = xs + (st & 1) * S::XSTAGE + 8 * tm;
+    const float* dt = ds + (st & 1) * S::DSTAGE + 8 * tn;
+#pragma unroll 4
+    for (int r = 0; r < BK; ++r) {
+      const uint4 xq = *reinterpret_cast<const uint4*>(xt + r * BM);
+      const float4 d0 = *reinterpret_cast<const float4*>(dt + r * EP);
+      const float4 d1 = *reinterpret_cast<const float4*>(dt + r * EP + 4);
+      float xv[8];
+      unpack8(xq, xv);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc[u][0] = fmaf(xv[u], d0.x, acc[u][0]);
+        acc[u][1] = fmaf(xv[u], d0.y, acc[u][1]);
+        acc[u][2] = fmaf(xv[u], d0.z, acc[u][2]);
+        acc[u][3] = fmaf(xv[u], d0.w, acc[u][3]);
+        acc[u][4] = fmaf(xv[u], d1.x, acc[u][4]);
+        acc[u][5] = fmaf(xv[u], d1.y, acc[u][5]);
+        acc[u][6] = fmaf(xv[u], d1.z, acc[u][6]);
+        acc[u][7] = fmaf(xv[u], d1.w, acc[u][7]);
+      }
+    }
+    __syncthreads();
   }
-  if (i0 < h) {
+  cp_async_wait<0>();
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      float* dst = partial + (static_cast<size_t>(chunk) * h + i0 + c) * E;
+  for (int u = 0; u < 8; ++u) {
+    const int col = i0 + 8 * tm + u;
+    if (col >= h) break;
+    float* dst = partial + (static_cast<size_t>(c) * h + col) * E + 8 * tn;
+    if (E % 4 == 0 && 8 * tn + 8 <= E) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
+    } else {
 #pragma unroll
-      for (int e = 0; e < EP; ++e)
-        if (e < E) dst[e] = acc[c][e];
+      for (int j = 0; j < 8; ++j)
+        if (8 * tn + j < E) dst[j] = acc[u][j];
     }
   }
 }
@@ -1097,7 +1296,7 @@ __global__ void router_wgrad_reduce_kernel(const float* __restrict__ partial, in
 }  // namespace
 
 size_t router_partial_bytes(int T, int h, int E) {
-  const int nch = router_chunks(h, E);
+  const int nch = router_chunks(T, h, E);
   if (router_padded_e(E) == 8 && nch == 1) return 0;
   return static_cast<size_t>(nch) * T * router_padded_e(E) * sizeof(float);
 }
@@ -1107,17 +1306,12 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
                           cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int ep = router_padded_e(E);
-  const int nch = router_chunks(h, E);
+  const int nch = router_chunks(T, h, E);
   cudaError_t err;
   if (ep == 8 && nch == 1) return router_a1_dispatch(x, Wg, b, T, h, E, k, idx, gates, num_sms, s);
   if (ep == 8) {
-    static bool attr = false;
-    if (!attr) {
-      err = cudaFuncSetAttribute(router_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kRouterASmem);
-      if (err != cudaSuccess) return err;
-      attr = true;
-    }
+    err = set_smem_once(reinterpret_cast<const void*>(router_a_kernel), kRouterASmem);
+    if (err != cudaSuccess) return err;
     const int tiles = (T + kRouterATile - 1) / kRouterATile;
     int bpc = num_sms / nch;
     if (bpc < 1) bpc = 1;
@@ -1128,9 +1322,9 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
     if (err != cudaSuccess || nch == 1) return err;
     return router_select_launch<8>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
   }
-  if (ep == 16) err = router_b_launch<16>(x, Wg, T, h, E, nch, partial, num_sms, s);
-  else if (ep == 32) err = router_b_launch<32>(x, Wg, T, h, E, nch, partial, num_sms, s);
-  else err = router_b_launch<64>(x, Wg, T, h, E, nch, partial, num_sms, s);
+  if (ep == 16) err = router_c_launch<16>(x, Wg, T, h, E, nch, partial, s);
+  else if (ep == 32) err = router_c_launch<32>(x, Wg, T, h, E, nch, partial, s);
+  else err = router_c_launch<64>(x, Wg, T, h, E, nch, partial, s);
   if (err != cudaSuccess) return err;
   if (ep == 16) return router_select_launch<16>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
   if (ep == 32) return router_select_launch<32>(partial, nch, b, T, E, k, idx, gates, num_sms, s);
@@ -1139,12 +1333,13 @@ cudaError_t launch_router(const uint16_t* x, const float* Wg, const float* b, in
 
 
 cudaError_t launch_dispatch_hist(const int32_t* topk_idx, long long n, int E,
-                                 const DispatchSel& sel, int32_t* blk_counts, cudaStream_t s) {
+                                 const DispatchSel& sel, int32_t* blk_counts, cudaStream_t s,
+                                 int* status) {
   const int nblk = dispatch_blocks(n);
   if (nblk == 0) return cudaSuccess;
   dispatch_kernel<false><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, sel.e_lo, sel.count,
                                                         sel.capacity, blk_counts, nullptr, nullptr,
-                                                        nullptr, nullptr);
+                                                        nullptr, nullptr, status);
   return launched();
 }
 
@@ -1159,42 +1354,42 @@ cudaError_t launch_dispatch_scan(const int32_t* blk_counts, int nblk, const Disp
 cudaError_t launch_dispatch_scatter(const int32_t* topk_idx, long long n, int E,
                                     const DispatchSel& sel, const int32_t* bases,
                                     const int32_t* offsets, int32_t* perm_src, int32_t* perm_dst,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, int* status) {
   const int nblk = dispatch_blocks(n);
   if (nblk == 0) return cudaSuccess;
   dispatch_kernel<true><<<nblk, kDispThreads, 0, s>>>(topk_idx, n, E, sel.e_lo, sel.count,
                                                        sel.capacity, nullptr, bases, offsets,
-                                                       perm_src, perm_dst);
+                                                       perm_src, perm_dst, status);
   return launched();
 }
 
 cudaError_t launch_gather_rows(const uint16_t* in, const int32_t* idx, int div, long long rows,
                                long long src_rows, int h, uint16_t* out, int num_sms,
                                cudaStream_t s, const int32_t* nvalid, const float* gsrc,
-                               float* gdst) {
-  if (rows == 0 || src_rows == 0) return cudaSuccess;
+                               float* gdst, int* status) {
+  if (rows == 0) return cudaSuccess;
   const int grid = grid_for(rows, num_sms, 8, 16);
   gather_rows_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(in), idx, div, rows,
                                           src_rows, nvalid, h / 8, reinterpret_cast<uint4*>(out),
-                                          gsrc, gdst);
+                                          gsrc, gdst, status);
   return launched();
 }
 
 cudaError_t launch_combine(const uint16_t* O, const float* gates, const int32_t* perm_dst, int T,
-                           int k, int h, uint16_t* y, int num_sms, cudaStream_t s) {
+                           int k, int h, uint16_t* y, int num_sms, cudaStream_t s, int* status) {
   if (T == 0) return cudaSuccess;
   const int grid = grid_for(T, num_sms, 8, 16);
   const uint4* o = reinterpret_cast<const uint4*>(O);
   uint4* yy = reinterpret_cast<uint4*>(y);
   switch (k) {
-    case 1: combine_kernel<1><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
-    case 2: combine_kernel<2><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
-    case 3: combine_kernel<3><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
-    case 4: combine_kernel<4><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
-    case 5: combine_kernel<5><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
-    case 6: combine_kernel<6><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
-    case 7: combine_kernel<7><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
-    default: combine_kernel<8><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy); break;
+    case 1: combine_kernel<1><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
+    case 2: combine_kernel<2><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
+    case 3: combine_kernel<3><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
+    case 4: combine_kernel<4><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
+    case 5: combine_kernel<5><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
+    case 6: combine_kernel<6><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
+    case 7: combine_kernel<7><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
+    default: combine_kernel<8><<<grid, 256, 0, s>>>(o, gates, perm_dst, T, h / 8, yy, status); break;
   }
   return launched();
 }
@@ -1218,23 +1413,26 @@ cudaError_t launch_wait_timeout_probe(int* status, unsigned long long limit_ns, 
 }
 
 cudaError_t launch_dg_reduce(const float* part, int nt, const int32_t* perm_src, long long rows,
-                             const int32_t* nvalid, float* dg, int num_sms, cudaStream_t s) {
+                             const int32_t* nvalid, float* dg, int num_sms, cudaStream_t s,
+                             int* status) {
   if (rows == 0) return cudaSuccess;
   long long blocks = (rows + 255) / 256;
   const long long cap = static_cast<long long>(num_sms) * 8;
   dg_reduce_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, s>>>(part, nt, perm_src,
-                                                                                 rows, nvalid, dg);
+                                                                                 rows, nvalid, dg,
+                                                                                 status);
   return launched();
 }
 
 cudaError_t launch_bwd_prep(const uint16_t* dy, const uint16_t* O, const float* gates,
                             const int32_t* perm_src, long long rows, int k, int h, uint16_t* dO,
-                            float* dg, int num_sms, cudaStream_t s, const int32_t* nvalid) {
+                            float* dg, int num_sms, cudaStream_t s, const int32_t* nvalid,
+                            int* status) {
   if (rows == 0) return cudaSuccess;
   const int grid = grid_for(rows, num_sms, 8, 16);
   bwd_prep_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(dy),
                                        reinterpret_cast<const uint4*>(O), gates, perm_src, rows,
-                                       nvalid, k, h / 8, reinterpret_cast<uint4*>(dO), dg);
+                                       nvalid, k, h / 8, reinterpret_cast<uint4*>(dO), dg, status);
   return launched();
 }
 
@@ -1249,7 +1447,7 @@ cudaError_t launch_transpose_wg(const float* Wg, int h, int E, float* WgT, cudaS
 cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
                               const int32_t* topk_idx, const float* gates, const float* dg,
                               const float* WgT, int T, int k, int h, int E, float* dl,
-                              uint16_t* dx, int num_sms, cudaStream_t s) {
+                              uint16_t* dx, int num_sms, cudaStream_t s, int* status) {
   if (T == 0) return cudaSuccess;
   const int grid = grid_for(T, num_sms, 8, 16);
   const float4* d4 = reinterpret_cast<const float4*>(dX_perm);
@@ -1257,34 +1455,106 @@ cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
   uint4* o = reinterpret_cast<uint4*>(dx);
   const int h8 = h / 8;
   switch (k) {
-    case 1: token_grad_kernel<1><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
-    case 2: token_grad_kernel<2><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
-    case 3: token_grad_kernel<3><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
-    case 4: token_grad_kernel<4><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
-    case 5: token_grad_kernel<5><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
-    case 6: token_grad_kernel<6><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
-    case 7: token_grad_kernel<7><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
-    default: token_grad_kernel<8><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o); break;
+    case 1: token_grad_kernel<1><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    case 2: token_grad_kernel<2><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    case 3: token_grad_kernel<3><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    case 4: token_grad_kernel<4><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    case 5: token_grad_kernel<5><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    case 6: token_grad_kernel<6><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    case 7: token_grad_kernel<7><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    default: token_grad_kernel<8><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
   }
   return launched();
 }
 
-int wgrad_router_chunks(int T) { return (T + kWgChunk - 1) / kWgChunk; }
+template <int EP>
+int wgrad_c_nch(int T, int h) {
+  const long long tiles = (h + WgradC<EP>::BM - 1) / WgradC<EP>::BM;
+  return split_k_chunks(tiles, (T + WgradC<EP>::BK - 1) / WgradC<EP>::BK, 128);
+}
+
+int wgrad_c_chunks(int T, int h, int E) {
+  const int ep = router_padded_e(E);
+  return ep == 8 ? wgrad_c_nch<8>(T, h)
+                 : ep == 16 ? wgrad_c_nch<16>(T, h)
+                            : ep == 32 ? wgrad_c_nch<32>(T, h) : wgrad_c_nch<64>(T, h);
+}
+
+template <int EP>
+cudaError_t router_wgrad_c_launch(const uint16_t* x, const float* dl, int T, int h, int E,
+                                  int nch, float* partial, cudaStream_t s) {
+  using S = WgradC<EP>;
+  const cudaError_t e =
+      set_smem_once(reinterpret_cast<const void*>(router_wgrad_c_kernel<EP>), S::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (h + S::BM - 1) / S::BM;
+  router_wgrad_c_kernel<EP><<<static_cast<int>(tiles * nch), S::THREADS, S::SMEM, s>>>(
+      x, dl, T, h, E, nch, partial);
+  return launched();
+}
+
+int wgrad_router_chunks(int T, int h, int E) { return T > 0 ? wgrad_c_chunks(T, h, E) : 0; }
+
+namespace {
+__global__ void check_offsets_kernel(const int32_t* __restrict__ offsets, int E, long long rows,
+                                     int* __restrict__ status) {
+  bool ok = true;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    const long long o = __ldg(offsets + e);
+    if (o < 0 || o > rows || (e == 0 && o != 0) || (e > 0 && o < __ldg(offsets + e - 1)))
+      ok = false;
+  }
+  if (!ok) report_bad_index(status);
+}
+
+// the status word of the calls without a workspace, one per device
+__device__ int g_nows_status = 0;
+std::mutex g_nows_mu;
+int* g_nows_addr[64] = {nullptr};
+}  // namespace
+
+cudaError_t launch_check_offsets(const int32_t* offsets, int E, long long rows, int* status,
+                                 cudaStream_t s) {
+  check_offsets_kernel<<<1, 256, 0, s>>>(offsets, E, rows, status);
+  return launched();
+}
+
+cudaError_t set_smem_once(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;  // (kernel, device) -> bytes set
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNoDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = done[{kern, dev}];
+  if (have >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
+int* nows_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_nows_mu);
+  if (!g_nows_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_nows_status) != cudaSuccess) return nullptr;
+    g_nows_addr[dev] = static_cast<int*>(p);
+  }
+  return g_nows_addr[dev];
+}
 
 cudaError_t launch_router_wgrad(const uint16_t* x, const float* dl, int T, int h, int E,
                                 float* partial, float* dWg, cudaStream_t s) {
-  const int nchunks = wgrad_router_chunks(T);
+  const int nchunks = wgrad_router_chunks(T, h, E);
   if (nchunks > 0) {
-    auto cols = [&](int c) { return dim3((h + c - 1) / c, nchunks); };
-    if (E <= 8)
-      router_wgrad_kernel<8><<<cols(WgShape<8>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
-    else if (E <= 16)
-      router_wgrad_kernel<16><<<cols(WgShape<16>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
-    else if (E <= 32)
-      router_wgrad_kernel<32><<<cols(WgShape<32>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
-    else
-      router_wgrad_kernel<64><<<cols(WgShape<64>::COLS), 256, 0, s>>>(x, dl, T, h, E, partial);
-    cudaError_t e = launched();
+    const int ep = router_padded_e(E);
+    cudaError_t e;
+    if (ep == 8) e = router_wgrad_c_launch<8>(x, dl, T, h, E, nchunks, partial, s);
+    else if (ep == 16) e = router_wgrad_c_launch<16>(x, dl, T, h, E, nchunks, partial, s);
+    else if (ep == 32) e = router_wgrad_c_launch<32>(x, dl, T, h, E, nchunks, partial, s);
+    else e = router_wgrad_c_launch<64>(x, dl, T, h, E, nchunks, partial, s);
     if (e != cudaSuccess) return e;
   }
   const long long n = static_cast<long long>(h) * E;

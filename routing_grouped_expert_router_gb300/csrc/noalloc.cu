@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "../../include/moe.h"
+#include "api_internal.h"
 #include "kernels.cuh"
 
 namespace {
@@ -58,6 +59,11 @@ moe_status scratch_address(void** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// a launcher's result, reported to the measurement hook like every other entry point's
+bool ran(cudaError_t e, cudaStream_t s, const char* name) {
+  return e == cudaSuccess && moe_api::note(s, name);
+}
 bool buf_ok(const void* p, size_t n) { return n == 0 ? (p == nullptr || aligned16(p)) : (p && aligned16(p)); }
 
 }  // namespace
@@ -66,13 +72,10 @@ extern "C" moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* t
                                           const moe_bf16* x, int32_t* counts, int32_t* offsets,
                                           int32_t* perm_src, int32_t* perm_dst, moe_bf16* x_perm,
                                           moe_stream_t stream_) {
-  if (!dims) return MOE_ERR_INVALID_ARG;
+  // the same checks as moe_permute
+  moe_status st = moe_api::check_dims(dims, false);
+  if (st != MOE_OK) return st;
   const moe_dims& d = *dims;
-  if (d.T < 0 || d.h <= 0 || d.f <= 0 || d.E <= 0 || d.k <= 0 || d.capacity < 0)
-    return MOE_ERR_INVALID_ARG;
-  if (d.k > 8 || d.E > moe::kRouterMaxE || d.h % 64 != 0 || d.f % 64 != 0 ||
-      static_cast<long long>(d.T) * d.k >= (1ll << 31))
-    return MOE_ERR_UNSUPPORTED;
   const long long R = static_cast<long long>(d.T) * d.k;
   if (!buf_ok(topk_idx, R) || !buf_ok(counts, 1) || !buf_ok(offsets, 1) ||
       !buf_ok(perm_src, R) || !buf_ok(perm_dst, R))
@@ -85,25 +88,28 @@ extern "C" moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* t
   if (2 * part > kScratchBytes) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch
 
   void* scratch = nullptr;
-  moe_status st = scratch_address(&scratch);
+  st = scratch_address(&scratch);
   if (st != MOE_OK) return st;
+  // index errors go to the per-device status word of the calls without a workspace
+  int* status = moe::nows_status_word();
+  if (!status) return MOE_ERR_CUDA;
   int32_t* blk_counts = static_cast<int32_t*>(scratch);
   int32_t* bases = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(scratch) + part);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_);
   const moe::DispatchSel sel{0, d.E, d.capacity > 0 ? d.capacity : INT_MAX};
-  if (moe::launch_dispatch_hist(topk_idx, R, d.E, sel, blk_counts, s) != cudaSuccess ||
-      moe::launch_dispatch_scan(blk_counts, nblk, sel, counts, offsets, bases, s) != cudaSuccess ||
-      moe::launch_dispatch_scatter(topk_idx, R, d.E, sel, bases, offsets, perm_src, perm_dst, s) !=
-          cudaSuccess)
+  if (!ran(moe::launch_dispatch_hist(topk_idx, R, d.E, sel, blk_counts, s, status), s,
+           "dispatch_hist") ||
+      !ran(moe::launch_dispatch_scan(blk_counts, nblk, sel, counts, offsets, bases, s), s,
+           "dispatch_scan") ||
+      !ran(moe::launch_dispatch_scatter(topk_idx, R, d.E, sel, bases, offsets, perm_src, perm_dst,
+                                        s, status),
+           s, "dispatch_scatter"))
     return MOE_ERR_CUDA;
-  if (x && x_perm) {
-    int sms = 148, dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (moe::launch_gather_rows(x, perm_src, d.k, R, d.T, d.h, x_perm, sms, s, offsets + d.E) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
+  if (x && x_perm &&
+      !ran(moe::launch_gather_rows(x, perm_src, d.k, R, d.T, d.h, x_perm, moe_api::num_sms(), s,
+                                   offsets + d.E, nullptr, nullptr, status),
+           s, "permute_rows"))
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -1,8 +1,15 @@
 """Host-side checks of the C ABI (no GPU): the library builds, loads, exports
-every declared entry point, and rejects bad arguments before any launch."""
+every declared entry point, and rejects bad arguments before any launch.
+
+The argument checks pass fake device addresses that only a host-side
+rejection keeps from ever reaching a kernel.  On a machine with a GPU a
+regression there would launch kernels on those addresses, so those tests run
+only where no CUDA device is present (the CPU suite)."""
 import ctypes
+import re
 
 import pytest
+import torch
 
 from routing_grouped_expert_router_gb300 import binding as mb
 from routing_grouped_expert_router_gb300 import build as mbuild
@@ -25,14 +32,26 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert "sm_103a" in mb.moe_version()
-    for code in range(6):
+    for code in range(7):
         s = mb.status_string(code)
         assert s.startswith("MOE_")
+    assert mb.status_string(mb.MOE_ERR_DEVICE_INDEX).startswith("MOE_ERR_DEVICE_INDEX")
     assert mb.status_string(99) == "unknown moe_status"
+
+
+def test_status_codes_match_the_header():
+    src = open(mb.HEADER).read()
+    codes = dict((n, int(v)) for n, v in re.findall(r"\b(MOE_(?:OK|ERR_\w+)) = (\d+)", src))
+    assert len(codes) == 7
+    for name, value in codes.items():
+        assert getattr(mb, name) == value, name
 
 
 FAKE = 1 << 20          # aligned, non-null address; never dereferenced
 MISALIGNED = FAKE + 8
+# calls with FAKE pointers: only where no device can run a kernel on them
+no_device = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake device addresses: host-only check")
 
 
 def _d(**kw):
@@ -56,6 +75,7 @@ def _d(**kw):
     (dict(T=1 << 29, k=8), mb.MOE_ERR_UNSUPPORTED),
     (dict(capacity=-1), mb.MOE_ERR_INVALID_ARG),
 ])
+@no_device
 def test_bad_dims_rejected(lib, kw, code):
     d = _d(**kw)
     st = lib.moe_route(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None)
@@ -91,6 +111,7 @@ def test_null_and_misaligned_pointers(lib):
         == mb.MOE_ERR_INVALID_ARG
 
 
+@no_device
 @pytest.mark.parametrize("op", range(7))
 def test_workspace_too_small(lib, op):
     d = _d()
@@ -134,6 +155,7 @@ def test_sizes_cover_tensors(lib):
 
 @pytest.mark.parametrize("lo,hi,ok", [(0, 8, True), (3, 4, True), (-1, 4, False), (4, 4, False),
                                       (5, 3, False), (0, 9, False)])
+@no_device
 def test_permute_local_range_checked(lib, lo, hi, ok):
     d = _d()
     need = lib.moe_workspace_bytes(ctypes.byref(d), mb.OP_PERMUTE)
@@ -145,11 +167,28 @@ def test_permute_local_range_checked(lib, lo, hi, ok):
     assert st == (mb.MOE_ERR_WORKSPACE if ok else mb.MOE_ERR_INVALID_ARG)
 
 
-def test_capacity_helper():
+def test_capacity_for(lib):
     assert mb.capacity_for(16384, 2, 8, 1.0) == 4096
     assert mb.capacity_for(10, 3, 4, 1.25) == 10   # ceil(9.375)
+    assert mb.capacity_for(0, 2, 8, 1.0) == 0
+    assert lib.moe_capacity_for(10, 0, 4, 1.0) == -1
+    assert lib.moe_capacity_for(10, 2, 0, 1.0) == -1
+    assert lib.moe_capacity_for(10, 2, 4, 0.0) == -1
+    assert lib.moe_capacity_for(1 << 30, 8, 1, 4.0) == -1      # past int32
+    with pytest.raises(mb.MoeError):
+        mb.capacity_for(10, 2, 4, -1.0)
     assert mb.dims(4, 64, 64, 4, 2, capacity=3).capacity == 3
     assert mb.dims(4, 64, 64, 4, 2).capacity == 0
+
+
+@no_device
+def test_status_word_without_workspace_needs_a_device(lib):
+    """moe_read_device_status(NULL) reads the per-device word of the calls
+    without a workspace: with no device it reports MOE_ERR_CUDA, and a
+    misaligned workspace is an argument error."""
+    assert lib.moe_read_device_status(None, None) == mb.MOE_ERR_CUDA
+    assert lib.moe_clear_device_status(None, None) == mb.MOE_ERR_CUDA
+    assert lib.moe_read_device_status(FAKE + 16, None) == mb.MOE_ERR_INVALID_ARG
 
 
 def test_saved_bytes_follow_sar_formula(lib):
@@ -174,6 +213,7 @@ def test_saved_bytes_follow_sar_formula(lib):
     assert lib.moe_saved_bytes(ctypes.byref(d)) == 0
 
 
+@no_device
 def test_fp8_shape_and_argument_checks(lib):
     d = _d(h=192)                                # h not a multiple of 128
     assert lib.moe_fp8_weight_bytes(ctypes.byref(d)) == 0
@@ -196,6 +236,7 @@ def test_fp8_shape_and_argument_checks(lib):
         == mb.MOE_ERR_INVALID_ARG           # rows beyond the source without idx
 
 
+@no_device
 def test_selftest_arguments_checked(lib):
     assert lib.moe_selftest_wait_timeout(None, 10, None) == mb.MOE_ERR_INVALID_ARG
     assert lib.moe_selftest_wait_timeout(FAKE + 16, 10, None) == mb.MOE_ERR_INVALID_ARG

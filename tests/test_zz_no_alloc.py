@@ -71,10 +71,21 @@ def test_noalloc_matches_workspace_entry_point(shape):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
     mbuild.build()
     lib = mb.load()
-    # ceil(T*k/1024) * E = 2049 * 64 > 131072
-    d = mb.dims((1 << 18) + 128, 64, 64, 64, 8)
-    P = 1 << 20
-    st = lib.moe_permute_noalloc(ctypes.byref(d), P, None, P, P, P, P, None, None)
+    # ceil(T*k/1024) * E = 2049 * 64 > 131072.  Real buffers of the declared
+    # sizes (about 8 MB each): were the size check ever to pass, the call
+    # would compute on them instead of touching memory it does not own.
+    T, E, k = (1 << 18) + 128, 64, 8
+    d = mb.dims(T, 64, 64, E, k)
+    R = T * k
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx = torch.zeros(R, **i32)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    psrc, pdst = torch.empty(R, **i32), torch.empty(R, **i32)
+    st = lib.moe_permute_noalloc(ctypes.byref(d), idx.data_ptr(), None, counts.data_ptr(),
+                                 offsets.data_ptr(), psrc.data_ptr(), pdst.data_ptr(), None, None)
+    torch.cuda.synchronize()
     assert st == mb.MOE_ERR_UNSUPPORTED
