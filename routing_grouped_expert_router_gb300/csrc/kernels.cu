@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "kernels.cuh"
@@ -52,6 +53,23 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Blocks of `threads` threads of `kern` that fit on one SM at once, looked up
+// once per (kernel, device).
+int resident_blocks(const void* kern, int threads) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find({kern, dev});
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess || n < 1)
+    n = 1;
+  cache[{kern, dev}] = n;
+  return n;
 }
 
 int grid_for(long long warps_needed, int num_sms, int warps_per_block, int blocks_per_sm) {
@@ -453,7 +471,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) router_a1_kernel(
 // tokens tm + TMT u (u < 8; interleaved, so the rows a warp reads sit in
 // different banks) and experts 8 tn .. 8 tn + 7.  The chunk runs in steps of
 // BK = 32 columns through a 2-stage cp.async ring holding the x tile
-// [BM][32] bf16 (rows padded to 80 bytes) and the Wg tile [32][EP] fp32.  Per
+// [BM][BK] bf16 (rows padded by 16 bytes) and the Wg tile [BK][EP] fp32.  Per
 // 8 columns a thread reads its tokens' x as 8 16-byte loads and, per column,
 // its experts' weights as 2 16-byte loads: 24 shared-memory loads feed 512
 // FMAs.  Each (token, expert) sum runs over the chunk's columns in order; the
@@ -466,6 +484,7 @@ struct RouterC {
   static constexpr int TMT = THREADS / TN;              // threads along the tokens
   static constexpr int BM = TMT * 8;                    // tokens per block
   static constexpr int BK = 32;                         // columns per step
+  static constexpr int MINB = 2;                        // blocks per SM
   static constexpr int XP = BK + 8;                     // padded x row (bf16)
   static constexpr int XSTAGE = BM * XP;                // bf16 per x stage
   static constexpr int WSTAGE = BK * EP;                // fp32 per Wg stage
@@ -473,7 +492,7 @@ struct RouterC {
 };
 
 template <int EP>
-__global__ void __launch_bounds__(RouterC<EP>::THREADS, 2) router_c_kernel(
+__global__ void __launch_bounds__(RouterC<EP>::THREADS, RouterC<EP>::MINB) router_c_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ Wg, int T, int h, int E, int nch,
     float* __restrict__ partial) {
   using S = RouterC<EP>;
@@ -499,7 +518,7 @@ __global__ void __launch_bounds__(RouterC<EP>::THREADS, 2) router_c_kernel(
       const int kc = k0 + st * BK;
       const int slot = st & 1;
       const uint32_t xb = smem_addr(xs + slot * S::XSTAGE);
-      // x tile: BM rows x 4 pieces of 16 bytes
+      // x tile: BM rows x BK / 8 pieces of 16 bytes
       for (int q = tid; q < BM * (BK / 8); q += NT) {
         const int r = q / (BK / 8), p8 = q % (BK / 8);
         const int t = t0 + r, col = kc + 8 * p8;
@@ -587,11 +606,11 @@ cudaError_t router_c_launch(const uint16_t* x, const float* Wg, int T, int h, in
                             float* partial, cudaStream_t s);
 
 // Chunks of h for a split-K launch of `tiles` output tiles over S k-steps:
-// the count with the shortest makespan on a 152-SM GPU at two blocks per SM,
+// the count with the shortest makespan on a 152-SM GPU at blocks_per_sm blocks per SM,
 // modelled as (waves of blocks) x (steps per chunk + 2 steps of prologue and
 // epilogue).  A function of the shape only (the workspace is sized from it).
-int split_k_chunks(long long tiles, int S, int max_chunks = 32) {
-  const long long slots = 2 * 152;
+int split_k_chunks(long long tiles, int S, int max_chunks = 32, int blocks_per_sm = 2) {
+  const long long slots = static_cast<long long>(blocks_per_sm) * 152;
   int best = 1;
   double best_t = -1.0;
   for (int n = 1; n <= max_chunks && n <= S; ++n) {
@@ -608,7 +627,7 @@ int split_k_chunks(long long tiles, int S, int max_chunks = 32) {
 template <int EP>
 int router_c_nch(int T, int h) {
   const long long tiles = (T + RouterC<EP>::BM - 1) / RouterC<EP>::BM;
-  return split_k_chunks(tiles, (h + RouterC<EP>::BK - 1) / RouterC<EP>::BK);
+  return split_k_chunks(tiles, (h + RouterC<EP>::BK - 1) / RouterC<EP>::BK, 32, RouterC<EP>::MINB);
 }
 
 // Warp per token: the logits of token t are the chunks' partials summed in
@@ -1065,8 +1084,15 @@ __global__ void transpose_wg_kernel(const float* __restrict__ Wg, int h, int E,
   }
 }
 
-// Router backward per token + dx, warp per token (K = k).  U 16-byte pieces of
-// the row per lane per step keep 2 * U * K fp32 loads of dX_perm in flight.
+// Router backward per token + dx (K = k).  A work item is one token and a
+// piece of its row: NSTEP steps of 32 lanes x U 16-byte pieces; U pieces per
+// lane per step keep 2 * U * K fp32 loads of dX_perm in flight.  For K <= 2
+// an item is two steps, so that the grid's warps finish together (a warp per
+// token left some warps one token longer than the rest); for K >= 3 the item
+// is the whole row, because there the per-item work (K permutation entries,
+// gates and dg, the k x k router gradient) measured slower when repeated per
+// piece.  Every item recomputes its token's router gradient; the first item
+// of a token writes its dl row.
 template <int K>
 __global__ void __launch_bounds__(256) token_grad_kernel(
     const float4* __restrict__ dX, const int32_t* __restrict__ perm_dst,
@@ -1074,11 +1100,19 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
     const float* __restrict__ dg, const float4* __restrict__ WgT, int T, int h8, int E,
     float* __restrict__ dl, uint4* __restrict__ dx, int* __restrict__ status) {
   constexpr int U = K <= 2 ? 2 : 1;
+  constexpr bool SPLIT = K <= 2;   // items are row pieces of NSTEP steps
+  constexpr int NSTEP = 2;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const long long R = static_cast<long long>(T) * K;
-  for (int t = gw; t < T; t += nw) {
+  // items per token
+  const int per = SPLIT ? (h8 + 32 * U * NSTEP - 1) / (32 * U * NSTEP) : 1;
+  using Item = typename std::conditional<SPLIT, long long, int>::type;
+  const Item items = static_cast<Item>(T) * per;
+  for (Item item = gw; item < items; item += nw) {
+    const int t = static_cast<int>(SPLIT ? item / per : item);
+    const int cb = SPLIT ? static_cast<int>(item - static_cast<Item>(t) * per) : 0;
     long long rows[K];
     int ex[K];
     bool kept[K];
@@ -1089,7 +1123,7 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
       const long long r = __ldg(perm_dst + a);
       const int e = __ldg(topk_idx + a);
       // out-of-range entries are recorded; such a slot adds nothing
-      if ((r >= R || e < 0 || e >= E) && lane == 0) report_bad_index(status);
+      if ((r >= R || e < 0 || e >= E) && lane == 0 && cb == 0) report_bad_index(status);
       kept[j] = r >= 0 && r < R;  // a dropped slot has no expert output: dg = 0, no dX
       rows[j] = kept[j] ? r : 0;
       ex[j] = (e < 0 || e >= E) ? -1 : e;
@@ -1108,14 +1142,17 @@ __global__ void __launch_bounds__(256) token_grad_kernel(
         if (i != j) acc = fmaf(g[i], d[j] - d[i], acc);
       dlj[j] = g[j] * acc;
     }
-    for (int e = lane; e < E; e += 32) {
-      float v = 0.f;
+    if (cb == 0) {
+      for (int e = lane; e < E; e += 32) {
+        float v = 0.f;
 #pragma unroll
-      for (int j = 0; j < K; ++j)
-        if (ex[j] == e) v = dlj[j];
-      dl[static_cast<size_t>(t) * E + e] = v;
+        for (int j = 0; j < K; ++j)
+          if (ex[j] == e) v = dlj[j];
+        dl[static_cast<size_t>(t) * E + e] = v;
+      }
     }
-    for (int c0 = lane; c0 < h8; c0 += 32 * U) {
+    const int cend = SPLIT ? min(h8, (cb + 1) * 32 * U * NSTEP) : h8;
+    for (int c0 = cb * 32 * U * NSTEP + lane; c0 < cend; c0 += 32 * U) {
       float4 q[U][K][2];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -1449,20 +1486,27 @@ cudaError_t launch_token_grad(const float* dX_perm, const int32_t* perm_dst,
                               const float* WgT, int T, int k, int h, int E, float* dl,
                               uint16_t* dx, int num_sms, cudaStream_t s, int* status) {
   if (T == 0) return cudaSuccess;
-  const int grid = grid_for(T, num_sms, 8, 16);
   const float4* d4 = reinterpret_cast<const float4*>(dX_perm);
   const float4* w4 = reinterpret_cast<const float4*>(WgT);
   uint4* o = reinterpret_cast<uint4*>(dx);
   const int h8 = h / 8;
+  // k <= 2: one wave of resident blocks whose warps stride over the row
+  // pieces (a grid of T / 8 blocks left a partial second wave); k >= 3: a
+  // block per 8 tokens, up to 16 blocks per SM
+  auto go = [&](auto kern) {
+    const int per_sm = k <= 2 ? resident_blocks(reinterpret_cast<const void*>(kern), 256) : 16;
+    const int grid = grid_for(T, num_sms, 8, per_sm);
+    kern<<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status);
+  };
   switch (k) {
-    case 1: token_grad_kernel<1><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
-    case 2: token_grad_kernel<2><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
-    case 3: token_grad_kernel<3><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
-    case 4: token_grad_kernel<4><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
-    case 5: token_grad_kernel<5><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
-    case 6: token_grad_kernel<6><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
-    case 7: token_grad_kernel<7><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
-    default: token_grad_kernel<8><<<grid, 256, 0, s>>>(d4, perm_dst, topk_idx, gates, dg, w4, T, h8, E, dl, o, status); break;
+    case 1: go(token_grad_kernel<1>); break;
+    case 2: go(token_grad_kernel<2>); break;
+    case 3: go(token_grad_kernel<3>); break;
+    case 4: go(token_grad_kernel<4>); break;
+    case 5: go(token_grad_kernel<5>); break;
+    case 6: go(token_grad_kernel<6>); break;
+    case 7: go(token_grad_kernel<7>); break;
+    default: go(token_grad_kernel<8>); break;
   }
   return launched();
 }
