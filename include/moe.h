@@ -168,14 +168,14 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx,
 
 /* moe_permute with no workspace argument (the pages have no counterpart; this
  * is an interface convenience).  For callers that cannot allocate device
- * memory when they dispatch: code running while a stream is captured into a
- * CUDA graph, or a runtime that owns a fixed memory budget.  Same arguments
+ * memory when they dispatch, such as a runtime that owns a fixed memory
+ * budget.  Same arguments
  * and outputs as moe_permute minus ws/ws_bytes.  Its scratch is a 1 MiB array
  * in the library's device memory (held by every GPU that loads the library
  * until exit), so it supports ceil(T*k / 1024) * E <= 131072 and returns
  * MOE_ERR_UNSUPPORTED beyond that.  The first call on a device looks up the
- * array's device address; make it before any stream capture.  The address is
- * kept for the life of the process: after a cudaDeviceReset, restart the
+ * array's device address (a host-side runtime query).  The address is kept
+ * for the life of the process: after a cudaDeviceReset, restart the
  * process before calling this again.  All calls share the array: calls that
  * overlap on the GPU race.  Index errors (an expert id out of range) go to the
  * per-device status word of the calls without a workspace.  Allocates

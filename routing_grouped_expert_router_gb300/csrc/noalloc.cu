@@ -1,10 +1,9 @@
 // noalloc.cu -- moe_permute_noalloc: the dispatch step without a workspace.
 //
 // Some callers cannot call cudaMalloc at the point where they dispatch
-// tokens: code that runs while a stream is being captured into a CUDA graph
-// (allocation is not a capturable operation), or a host runtime or plugin
-// that owns a fixed device-memory budget and hands its kernels only their
-// inputs and outputs.  For them this entry point keeps its scratch memory --
+// tokens, such as a host runtime or plugin that owns a fixed device-memory
+// budget and hands its kernels only their inputs and outputs.  For them this
+// entry point keeps its scratch memory --
 // the per-block expert counts and the per-block base offsets of the stable
 // scatter -- in one fixed-size array that lives in the library's own device
 // memory.  Every GPU that loads the library holds that array until the
@@ -12,8 +11,7 @@
 //
 // The array is a host-side stand-in in host code, not a device address; the
 // address kernels need is looked up with cudaGetSymbolAddress, once per
-// device, on the first call made with that device current.  That first call
-// should therefore come before any stream capture.
+// device, on the first call made with that device current.
 //
 // All calls share the one array and it keeps whatever the last call left in
 // it.  Nothing in it has to start at zero: each call writes every entry it

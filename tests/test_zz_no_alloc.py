@@ -1,9 +1,9 @@
 """moe_permute_noalloc: dispatch for callers that cannot allocate device
-memory (for example while a stream is being captured into a CUDA graph, or
-inside a runtime that owns a fixed memory budget).  Its scratch is a fixed
-array in the library, so the test checks that two calls in a row -- the
-second one reusing whatever the first left in that array -- give exactly the
-outputs of the regular entry point, which takes a caller workspace.
+memory (for example inside a runtime that owns a fixed memory budget).  Its
+scratch is a fixed array in the library, so the test checks that two calls in
+a row -- the second one reusing whatever the first left in that array -- give
+exactly the outputs of the regular entry point, which takes a caller
+workspace.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test."""
