@@ -1424,8 +1424,7 @@ cudaError_t launch(const Params& prm, const Maps& maps, long long tiles, int num
     auto kern = gg2_kernel<A_MN, B_MN, NUM_B, EPI, GROUP_K>;
     const cudaError_t ea = set_smem_once(reinterpret_cast<const void*>(kern), SMEM2_BYTES);
     if (ea != cudaSuccess) return ea;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NUM_THREADS2, 1, 1);
     cfg.dynamicSmemBytes = SMEM2_BYTES;
     cfg.stream = s;
