@@ -520,13 +520,18 @@ __device__ __forceinline__ void zero_wgrad_row(const Params& p, const Tile& tl, 
 
 // Zero k-rows kv..63 of an MN-major 128-wide A tile (two 64-column chunks):
 // they hold the next expert's rows (or the zero fill) and must add nothing.
+// The rows past kv are contiguous in each chunk, so a lane clears 16-byte
+// words i and i + 32 ... of both chunks with no index arithmetic beyond the
+// stride (an earlier form divided by the chunk length per word, which put
+// about a thousand cycles per ragged tile on the path to the MMA).
 __device__ __forceinline__ void zero_a_tail(uint8_t* a_tile, int kv, int lane) {
-  const int per_chunk = (BK - kv) * 8;  // 16-byte words per chunk
-  for (int w = lane; w < per_chunk * 2; w += 32) {
-    const int ch = w / per_chunk;
-    const int rem = w - ch * per_chunk;
-    *reinterpret_cast<uint4*>(a_tile + ch * CHUNK_BYTES + kv * 128 + rem * 16) =
-        make_uint4(0, 0, 0, 0);
+  const int n = (BK - kv) * 8;  // 16-byte words per chunk
+  uint4* c0 = reinterpret_cast<uint4*>(a_tile + kv * 128);
+  uint4* c1 = reinterpret_cast<uint4*>(a_tile + CHUNK_BYTES + kv * 128);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int i = lane; i < n; i += 32) {
+    c0[i] = z;
+    c1[i] = z;
   }
   fence_proxy_async_smem();
   __syncwarp();
