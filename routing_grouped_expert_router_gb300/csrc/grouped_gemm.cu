@@ -182,8 +182,18 @@ __device__ __forceinline__ bool decode(const Params& p, const int* off, const in
   if (!GROUP_K) {
     const int total = NT * cum[p.E];
     if (t >= total) return false;
-    int e = 0;
-    while (NT * cum[e + 1] <= t) ++e;
+    // the expert whose tiles hold t: the last e with NT cum[e] <= t, which has
+    // rows (cum is non-decreasing and t < NT cum[E]).  A binary search: every
+    // warp role decodes each of its tiles, and a scan over 64 experts in
+    // shared memory cost up to a couple of thousand cycles per tile.
+    int e = 0, hi = p.E - 1;
+    while (e < hi) {
+      const int mid = (e + hi + 1) >> 1;
+      if (NT * cum[mid] <= t)
+        e = mid;
+      else
+        hi = mid - 1;
+    }
     const int local = t - NT * cum[e];
     const int mt = cum[e + 1] - cum[e];
     tl.e = e;
