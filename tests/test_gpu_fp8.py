@@ -311,3 +311,104 @@ def test_fp8_backward_rejects_sar(lib):
                              run.dx, run.dWg, run.dW1, run.dW3, run.dW2,
                              workspace(mb.dims_of(cfg, has_bias=False), mb.OP_LAYER_BWD_FP8))
     assert err.value.status == mb.MOE_ERR_UNSUPPORTED
+
+
+def test_fp8_backward_fullsize_sampled(lib):
+    """The FP8 backward (e4m3 FC1 dgrad) at the full Mixtral-shaped size, after
+    the bf16 forward, in the bench's launch configuration (`--fp8-dgrad`).
+
+    Bit-exact: the row codes and scales of W1/W3 for two experts.  A token
+    sample S (the first and last tokens, the edge rows of every expert, random
+    tokens): each token's dx row depends on that token alone, so the oracle's
+    expert forward and FP8 expert backward run on S's rows only, one expert
+    at a time, and the router side of dx follows from them.  A second
+    backward with dy zeroed outside S gives weight gradients from S alone,
+    which the oracle computes in full for every expert S reaches."""
+    from routing_grouped_expert_router_gb300 import synth
+    from routing_grouped_expert_router_gb300.configs import CONFIGS
+    cfg = CONFIGS["mixtral8x7b"]
+    T, h, f, E, k = cfg.T, cfg.h, cfg.f, cfg.E, cfg.k
+    inp = synth.make_layer(cfg, "cuda")
+    x_cpu, _ = oracle.condition_router_margins(
+        inp["x"].cpu(), inp["Wg"].cpu(), inp["b"].cpu(), k,
+        lambda r, a: synth.replacement_x_rows(cfg, r, a))
+    inp["x"] = x_cpu.cuda()
+    d = mb.dims_of(cfg)
+    run = LayerRun(d)
+    run.fwd(inp)
+    qwb = _bwd_weights(d, inp)
+    wsb = workspace(d, mb.OP_LAYER_BWD_FP8)
+
+    def bwd(dy):
+        mb.moe_layer_bwd_fp8(d, inp["x"], dy, inp["Wg"], inp["W2"], qwb, run.saved, run.dx,
+                             run.dWg, run.dW1, run.dW3, run.dW2, wsb)
+        torch.cuda.synchronize()
+        assert mb.moe_read_device_status(wsb) == mb.MOE_OK and run.status() == mb.MOE_OK
+
+    bwd(inp["dy"])
+    Wg_cpu, b_cpu = inp["Wg"].cpu(), inp["b"].cpu()
+    idx, gates, _ = ref.route(x_cpu, Wg_cpu, b_cpu, k)
+    counts, offsets, psrc, pdst = ref.dispatch(idx, E)
+    np.testing.assert_array_equal(run.saved_view("topk_idx").cpu().numpy(), idx)
+
+    # W1/W3 row codes and scales of the largest and the smallest expert
+    W1r = _bview(d, qwb, "W1r", (E, h, f), torch.uint8)
+    W3r = _bview(d, qwb, "W3r", (E, h, f), torch.uint8)
+    s13r = _bview(d, qwb, "s13r", (E, h), torch.float32).cpu().numpy()
+    big, small = int(np.argmax(counts)), int(np.argmin(counts))
+    for e in {big, small}:
+        q1, q3, s13 = ref.quantize_rows_joint_e4m3(oracle.as_f64(inp["W1"][e]),
+                                                  oracle.as_f64(inp["W3"][e]))
+        np.testing.assert_array_equal(_codes(W1r[e]), q1)
+        np.testing.assert_array_equal(_codes(W3r[e]), q3)
+        np.testing.assert_array_equal(s13r[e], s13)
+
+    # the token sample
+    toks = {0, T - 1}
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for r in (lo, hi - 1, lo + ((hi - lo - 1) // 256) * 256):
+            if lo <= r < hi:
+                toks.add(int(psrc[r]) // k)
+    rng = np.random.default_rng(cfg.seed)
+    while len(toks) < 64:
+        toks.add(int(rng.integers(0, T)))
+    S = np.array(sorted(toks))
+    St = torch.from_numpy(S)
+    n = len(S)
+    dx_S = run.dx[St].cpu()
+
+    # the masked backward: dy zeroed outside S
+    mask = torch.zeros(T, 1, dtype=torch.bfloat16, device="cuda")
+    mask[St.cuda()] = 1
+    bwd(inp["dy"] * mask)
+
+    # the oracle on S, one expert at a time
+    xS = x_cpu[St]
+    dyS = oracle.as_f64(inp["dy"][St.cuda()].cpu())
+    gS = gates[S].astype(np.float64)
+    iS = idx[S]
+    dg = np.zeros(n * k)
+    dX = np.zeros((n * k, h))
+    for e in sorted(set(iS.ravel().tolist())):
+        slots = np.nonzero(iS.ravel() == e)[0]
+        rows = slots // k
+        one = np.array([0, len(slots)], np.int32)
+        W = (inp["W1"][e:e + 1].cpu(), inp["W3"][e:e + 1].cpu(), inp["W2"][e:e + 1].cpu())
+        A, B, H, O = ref.expert_ffn_fwd(xS[torch.from_numpy(rows)], one, *W)
+        dg[slots] = np.sum(dyS[rows] * O, axis=1)
+        dO = ref.bf16_round(np.float32(gS.ravel()[slots])[:, None] * np.float32(dyS[rows]))
+        bw = ref.expert_ffn_bwd_fp8(dO, xS[torch.from_numpy(rows)], one, *W, A, B, H)
+        dX[slots] = bw["dX_perm"]
+        assert rel_l2(oracle.as_f64(run.dW1[e]), bw["dW1"][0]) <= TOL_W, e
+        assert rel_l2(oracle.as_f64(run.dW3[e]), bw["dW3"][0]) <= TOL_W, e
+        assert rel_l2(oracle.as_f64(run.dW2[e]), bw["dW2"][0]) <= TOL_W, e
+    tg = ref.token_grads(xS, Wg_cpu, iS, gates[S], np.arange(n * k, dtype=np.int32), dg, dX)
+    assert rel_l2(dx_S.double().numpy(), tg["dx"]) <= TOL_Y
+    for i in range(n):
+        assert rel_l2(dx_S[i].double().numpy(), tg["dx"][i]) <= 2e-2, int(S[i])
+    assert rel_l2(oracle.as_f64(run.dWg), tg["dWg"]) <= TOL_W
+    # the masked run leaves every other dx row exactly zero
+    others = torch.ones(T, dtype=torch.bool)
+    others[St] = False
+    assert torch.all(run.dx.cpu()[others] == 0)
