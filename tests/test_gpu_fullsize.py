@@ -206,3 +206,30 @@ def _check_fullsize(cfg, capacity=0, sar=False, ntok=64):
         for q in range(len(cols)):
             assert rel_l2(g1[:, q], w["dW1"][:, q]) <= TOL_ROW, (e, int(cols[q]))
             assert rel_l2(g2[q], w["dW2"][q]) <= TOL_ROW, (e, int(cols[q]))
+
+
+@pytest.mark.parametrize("name", ["mixtral8x7b", "deepseekmoe", "hunyuan"])
+def test_fullsize_bitwise_deterministic(lib, name):
+    """Two runs of the full layer on the same inputs give bitwise the same y, dx
+    and gradients: every split reduction (the router's and router weight
+    gradient's chunks, the GEMMs' tile order) has a fixed order at these sizes
+    too, whatever the chunk counts the shapes pick.  Two layer instances, so
+    no buffer is shared between the runs."""
+    cfg = CONFIGS[name]
+    inp = synth.make_layer(cfg, "cuda")
+    d = mb.dims_of(cfg)
+    outs = []
+    for _ in range(2):
+        run = LayerRun(d)
+        run.fwd(inp)
+        run.bwd(inp)
+        torch.cuda.synchronize()
+        assert run.status() == mb.MOE_OK
+        outs.append(run)
+    a, b = outs
+    for key in ("y", "dx"):
+        assert torch.equal(getattr(a, key).view(torch.int16), getattr(b, key).view(torch.int16)), key
+    for key in ("dWg", "dW1", "dW3", "dW2"):
+        assert torch.equal(getattr(a, key).view(torch.int32), getattr(b, key).view(torch.int32)), key
+    for key in ("topk_idx", "perm_src", "perm_dst"):
+        assert torch.equal(a.saved_view(key), b.saved_view(key)), key
