@@ -137,6 +137,55 @@ def test_all_tokens_on_one_expert(lib):
         assert rel_l2(out[key].numpy(), g[key]) <= TOL_W, key
 
 
+@pytest.mark.parametrize("E,k,h", [(8, 2, 256), (16, 3, 192), (64, 6, 128), (8, 2, 4160)])
+def test_zero_upstream_gradient_gives_exact_zeros(lib, E, k, h):
+    """dy = 0: every gradient is exactly zero (dx, dWg and all expert weight
+    gradients; the gate gradients and the router backward vanish too), for
+    each router kernel family (E = 8 with h <= 4096 and h > 4096, E = 16..64)."""
+    cfg = small_config(name="dy0", T=333, h=h, f=192, E=E, k=k, seed=21)
+    inp = conditioned_inputs(cfg)
+    inp["dy"] = torch.zeros_like(inp["dy"])
+    run = LayerRun(mb.dims_of(cfg, has_bias=False))
+    dev = _to(inp, "cuda")
+    for t in (run.dx, run.dWg, run.dW1, run.dW3, run.dW2):
+        t.fill_(7)
+    run.fwd(dev)
+    run.bwd(dev)
+    torch.cuda.synchronize()
+    assert run.status() == mb.MOE_OK
+    for name in ("dx", "dWg", "dW1", "dW3", "dW2"):
+        assert torch.all(getattr(run, name) == 0), name
+
+
+@pytest.mark.parametrize("E,k,h", [(8, 2, 256), (16, 3, 192), (64, 6, 128), (8, 2, 4160)])
+def test_zero_tokens_tie_to_the_lowest_experts(lib, E, k, h):
+    """x = 0 (no bias): every logit is exactly 0, so every token ties across all
+    E experts.  Ties go to the lower id: every token takes experts 0..k-1 in
+    that order with gates exactly 1/k, the dispatch is the identity order
+    within each of those experts, and y = 0 exactly (A = B = H = 0)."""
+    cfg = small_config(name="x0", T=257, h=h, f=192, E=E, k=k, seed=22)
+    inp = conditioned_inputs(cfg)
+    inp["x"] = torch.zeros_like(inp["x"])
+    run = LayerRun(mb.dims_of(cfg, has_bias=False))
+    dev = _to(inp, "cuda")
+    run.fwd(dev)
+    torch.cuda.synchronize()
+    assert run.status() == mb.MOE_OK
+    T = cfg.T
+    idx = run.saved_view("topk_idx").cpu()
+    assert torch.equal(idx, torch.arange(k, dtype=torch.int32).repeat(T, 1))
+    gates = run.saved_view("gates").cpu()
+    np.testing.assert_array_equal(gates.numpy(), np.full((T, k), np.float32(1.0) / np.float32(k)))
+    counts = run.saved_view("counts").cpu()
+    assert torch.equal(counts[:k], torch.full((k,), T, dtype=torch.int32))
+    assert torch.all(counts[k:] == 0)
+    # within expert j the rows are the tokens in order: perm_src[j T + t] = t k + j
+    psrc = run.saved_view("perm_src").cpu().view(k, T)
+    want = torch.arange(T, dtype=torch.int32)[None, :] * k + torch.arange(k, dtype=torch.int32)[:, None]
+    assert torch.equal(psrc, want)
+    assert torch.all(run.y == 0)
+
+
 def test_empty_batch(lib):
     d = mb.dims(0, 128, 128, 8, 2)
     run = LayerRun(d)
