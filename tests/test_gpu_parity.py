@@ -186,6 +186,54 @@ def test_zero_tokens_tie_to_the_lowest_experts(lib, E, k, h):
     assert torch.all(run.y == 0)
 
 
+def _layer_outputs(cfg, inp):
+    run = LayerRun(mb.dims_of(cfg, has_bias=False))
+    run.fwd(inp)
+    run.bwd(inp)
+    torch.cuda.synchronize()
+    assert run.status() == mb.MOE_OK
+    return run
+
+
+@pytest.mark.parametrize("name", ["mixtral_mid", "deepseek_mid"])
+def test_exact_scaling(lib, name):
+    """Power-of-two scalings commute with every rounding on the path: W2 -> 2 W2
+    gives y -> 2 y exactly, and dy -> 2 dy gives every gradient times 2
+    exactly (the fp32 sums see exactly doubled terms)."""
+    cfg, inp = _inputs(name)
+    dev = _to(inp, "cuda")
+    base = _layer_outputs(cfg, dev)
+    w2 = dict(dev)
+    w2["W2"] = dev["W2"] * 2
+    assert torch.equal((w2["W2"].float() / 2).to(torch.bfloat16), dev["W2"])
+    run = _layer_outputs(cfg, w2)
+    assert torch.equal(run.y.float(), 2 * base.y.float())
+    dy2 = dict(dev)
+    dy2["dy"] = dev["dy"] * 2
+    run = _layer_outputs(cfg, dy2)
+    assert torch.equal(run.y, base.y)
+    for key in ("dx", "dWg", "dW1", "dW3", "dW2"):
+        assert torch.equal(getattr(run, key).float(), 2 * getattr(base, key).float()), key
+
+
+@pytest.mark.parametrize("name", ["mixtral_mid", "hunyuan_mid"])
+def test_token_permutation_permutes_rows_exactly(lib, name):
+    """Permuting the tokens permutes y and dx rows bitwise: a row's router
+    logits, its expert rows' dot products and its combine all run in an order
+    that does not depend on the row's position in the batch."""
+    cfg, inp = _inputs(name)
+    dev = _to(inp, "cuda")
+    base = _layer_outputs(cfg, dev)
+    perm = torch.randperm(cfg.T, generator=torch.Generator().manual_seed(5)).cuda()
+    pd = dict(dev)
+    pd["x"] = dev["x"][perm].contiguous()
+    pd["dy"] = dev["dy"][perm].contiguous()
+    run = _layer_outputs(cfg, pd)
+    assert torch.equal(run.y.view(torch.int16), base.y[perm].view(torch.int16))
+    assert torch.equal(run.dx.view(torch.int16), base.dx[perm].view(torch.int16))
+    assert torch.equal(run.saved_view("topk_idx"), base.saved_view("topk_idx")[perm])
+
+
 def test_empty_batch(lib):
     d = mb.dims(0, 128, 128, 8, 2)
     run = LayerRun(d)
