@@ -417,6 +417,14 @@ const char* moe_profile_kernel_name(int i);
  * more than one kernel: the router and the router weight gradient run two). */
 int64_t moe_kernel_launches(void);
 
+/* Failure-injection hook for tests: the n-th kernel launch from now on the
+ * calling host thread is reported as failed (cudaErrorLaunchFailure), so the
+ * entry point that made it returns MOE_ERR_CUDA at that point without
+ * launching the rest of its sequence.  The kernel itself runs normally and no
+ * device state is touched: the failure exists only on the host.  n <= 0
+ * clears a pending injection; the hook clears itself once it fires. */
+void moe_test_fail_launch_after(int n);
+
 /* Library build string (arch, version). */
 const char* moe_version(void);
 

@@ -86,6 +86,7 @@ _SIGS = {
     "moe_profile_events": (_I, [_P, _I]),
     "moe_profile_kernel_name": (ctypes.c_char_p, [_I]),
     "moe_kernel_launches": (ctypes.c_int64, []),
+    "moe_test_fail_launch_after": (None, [ctypes.c_int]),
     "moe_selftest_wait_timeout": (_I, [_P, ctypes.c_uint32, _P]),
     "moe_fp8_weight_bytes": (_SZ, [_D]),
     "moe_quantize_weights_fp8": (_I, [_D, _P, _P, _P, _P, _P]),
@@ -278,6 +279,10 @@ def moe_selftest_wait_timeout(ws, limit_us: int, stream=None):
 
 def moe_kernel_launches() -> int:
     return int(load().moe_kernel_launches())
+
+
+def moe_test_fail_launch_after(n: int) -> None:
+    load().moe_test_fail_launch_after(int(n))
 
 
 def moe_fp8_weight_bytes(d) -> int:

@@ -473,6 +473,8 @@ int moe_profile_events(moe_event_t* events, int capacity) {
 
 int64_t moe_kernel_launches(void) { return moe::kernel_launches(); }
 
+void moe_test_fail_launch_after(int n) { moe::fail_launch_after(n); }
+
 const char* moe_profile_kernel_name(int i) {
   if (i < 0 || i >= 4096) return "";
   return g_prof.names[i] ? g_prof.names[i] : "";

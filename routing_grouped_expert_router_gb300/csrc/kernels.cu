@@ -20,13 +20,21 @@ namespace moe {
 
 namespace {
 thread_local long long g_launches = 0;
+thread_local long long g_fail_at = -1;  // launch count that reports a failure (test hook)
 }  // namespace
 
 long long kernel_launches() { return g_launches; }
 
+void fail_launch_after(int n) { g_fail_at = n > 0 ? g_launches + n : -1; }
+
 cudaError_t launched() {
   ++g_launches;
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (g_fail_at >= 0 && g_launches == g_fail_at) {
+    g_fail_at = -1;
+    return e != cudaSuccess ? e : cudaErrorLaunchFailure;
+  }
+  return e;
 }
 namespace {
 

@@ -13,6 +13,9 @@ namespace moe {
 // and returns cudaGetLastError().
 long long kernel_launches();
 cudaError_t launched();
+// Test hook: the n-th launch from now on this thread reports
+// cudaErrorLaunchFailure from launched() (the kernel itself runs); n <= 0 clears.
+void fail_launch_after(int n);
 
 // The code a kernel records in its status word when an index it reads from
 // device memory (an expert id, a permutation entry) is outside its range.

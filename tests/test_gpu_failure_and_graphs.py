@@ -5,6 +5,10 @@
   MOE_ERR_DEVICE_TIMEOUT in the workspace status word and returns.  The host
   reads the status, and the same context then runs a layer correctly.  Nothing
   faults, traps or hangs.
+* A launch failure injected on the host (moe_test_fail_launch_after) makes the
+  entry point that hit it return MOE_ERR_CUDA at that launch, wherever it falls
+  in the forward or the backward; the next layer on the same context runs
+  clean and matches the oracle.
 * The layer is a fixed sequence of launches with no host synchronisation or
   allocation, so moe_layer_fwd + moe_layer_bwd capture into a CUDA graph; the
   replay gives bitwise the eager results.
@@ -92,3 +96,39 @@ def test_layer_captures_into_a_cuda_graph(lib):
         a, b = out[key], ref[key]
         assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.uint8) if b.dtype == torch.bfloat16 else b), key
+
+
+@pytest.mark.parametrize("n", [1, 4, 8, 12, 17])
+def test_injected_launch_failure_is_reported_and_the_context_recovers(lib, n):
+    cfg, inp, dev = _inputs()
+    d = mb.dims_of(cfg, has_bias=False)
+    run = LayerRun(d)
+    before = mb.moe_kernel_launches()
+    mb.moe_test_fail_launch_after(n)
+    with pytest.raises(mb.MoeError) as err:
+        run.fwd(dev)
+        run.bwd(dev)
+    assert err.value.status == mb.MOE_ERR_CUDA
+    assert mb.moe_kernel_launches() - before == n  # nothing launched after the failure
+    torch.cuda.synchronize()
+    run.fwd(dev)
+    run.bwd(dev)
+    torch.cuda.synchronize()
+    assert run.status() == mb.MOE_OK
+    y, ctx = ref.layer_fwd(inp["x"], inp["Wg"], None, inp["W1"], inp["W3"], inp["W2"], cfg.k)
+    g = ref.layer_bwd(inp["dy"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ctx)
+    out = run.outputs()
+    assert rel_l2(out["y"].double().numpy(), y) <= 5e-3
+    assert rel_l2(out["dx"].double().numpy(), g["dx"]) <= 5e-3
+    assert rel_l2(out["dW1"].numpy(), g["dW1"]) <= 1e-2
+
+
+def test_cleared_injection_does_not_fire(lib):
+    cfg, inp, dev = _inputs()
+    run = LayerRun(mb.dims_of(cfg, has_bias=False))
+    mb.moe_test_fail_launch_after(3)
+    mb.moe_test_fail_launch_after(0)
+    run.fwd(dev)
+    run.bwd(dev)
+    torch.cuda.synchronize()
+    assert run.status() == mb.MOE_OK

@@ -247,3 +247,13 @@ def test_selftest_arguments_checked(lib):
 def test_profile_hook_without_events(lib):
     assert mb.moe_profile_events(None, 0) == 0
     assert mb.moe_profile_kernel_name(-1) == ""
+
+
+def test_launch_failure_hook_is_host_only(lib):
+    """The failure-injection hook only sets a host-side counter: setting and
+    clearing it needs no device and launches nothing."""
+    before = lib.moe_kernel_launches()
+    mb.moe_test_fail_launch_after(5)
+    mb.moe_test_fail_launch_after(0)
+    mb.moe_test_fail_launch_after(-3)
+    assert lib.moe_kernel_launches() == before
